@@ -1,0 +1,145 @@
+"""Plain fp64 CPU oracle for Transformer-XL relative attention and Tail_M.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference leg of ``bench.py`` may import this package.  It
+shares no code with the CUDA library and never imports it.
+
+Functions
+---------
+attn(q, k, v, r_k, u, vb, scale, ...)
+    The relative attention forward, computed by ``txl_oracle.c`` with one
+    loop per (query, key) pair and the four-term score a+b+c+d ("Transformer-XL"
+    notes, zty624, section "Relative Positional Encoding"), the rectangular
+    mask allow(i, j) <=> j <= M+i (same notes, section "Causal Mask With
+    Memory") and the distance convention of the position sequence M+L-1..0
+    ("Transformer-XL模型 核心源码阅读笔记", section "Build the model",
+    MemTransformerLM._forward).
+mem_update(mem, hid, mem_len, ext_len=0)
+    Tail_M: keep the newest ``mem_len`` rows of [mem; hid] along the sequence
+    axis, with the index arithmetic of MemTransformerLM._update_mems in the
+    source-reading notes (end = mlen + max(0, qlen - ext_len),
+    beg = max(0, end - mem_len)) and the batch-major layout of the
+    "Transformer-XL" notes, section "Batched Tensor Contract".
+sinusoid(pos, demb)
+    Is NOT here: the sinusoid is input preparation and lives in the seeded
+    workload module.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "txl_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc into oracle/liboracle.so (portable flags:
+    no -march, no FMA contraction, so x86 and Arm give the same results)."""
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.oracle_attn_f64.argtypes = [dp, dp, dp, dp, dp, dp,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                            dp, dp, ip, ctypes.c_int, ctypes.c_int]
+            lib.oracle_attn_f64.restype = ctypes.c_int
+            lib.oracle_num_cores.argtypes = []
+            lib.oracle_num_cores.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact conversion to a contiguous fp64 numpy array (bf16/fp32 -> fp64 is exact)."""
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_cores() -> int:
+    return int(_load().oracle_num_cores())
+
+
+def attn(q, k, v, r_k, u, vb, scale: float, pairs=None, want_scores: bool = False,
+         nthreads: int = 0):
+    """Relative attention forward in fp64.
+
+    q [B,H,L,dh]; k, v [B,H,M+L,dh]; r_k [M+L,H,dh] (row r <-> distance
+    M+L-1-r); u, vb [H,dh].  ``pairs`` optionally lists flat b*H+h indices to
+    compute (other rows of the result are NaN).  Returns ``out`` [B,H,L,dh]
+    or ``(out, scores)`` with scores [B,H,L,M+L] (-inf where masked).
+    """
+    q, k, v, r_k, u, vb = (_f64(t) for t in (q, k, v, r_k, u, vb))
+    B, H, L, dh = q.shape
+    K = k.shape[2]
+    M = K - L
+    if k.shape != (B, H, K, dh) or v.shape != k.shape:
+        raise ValueError("k, v must be [B,H,M+L,dh]")
+    if r_k.shape != (K, H, dh) or u.shape != (H, dh) or vb.shape != (H, dh):
+        raise ValueError("r_k must be [M+L,H,dh]; u, vb [H,dh]")
+    out = np.full((B, H, L, dh), np.nan)
+    scores = np.full((B, H, L, K), np.nan) if want_scores else None
+    if pairs is not None:
+        parr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32))
+        if parr.size and (parr.min() < 0 or parr.max() >= B * H):
+            raise ValueError("pair index out of range")
+        pp = parr.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+        npairs = int(parr.size)
+    else:
+        parr, pp, npairs = None, None, 0
+    rc = _load().oracle_attn_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r_k), _ptr(u), _ptr(vb),
+        B, H, L, M, dh, float(scale), _ptr(out),
+        _ptr(scores) if scores is not None else None,
+        pp, npairs, int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle_attn_f64 failed ({rc})")
+    return (out, scores) if want_scores else out
+
+
+def mem_update(mem, hid, mem_len: int, ext_len: int = 0) -> np.ndarray:
+    """Tail_M of [mem; hid] along axis 1 (batch-major [B, len, d]).
+
+    Works on any dtype bit-for-bit: it only slices.  ``mem`` may hold fewer
+    than ``mem_len`` rows (the growth phase); the result holds
+    min(mem_len, mlen + qlen - ext_len) rows.
+    """
+    mem = np.asarray(mem)
+    hid = np.asarray(hid)
+    mlen, qlen = mem.shape[1], hid.shape[1]
+    if mem_len == 0:
+        return hid[:, :0].copy()
+    end = mlen + max(0, qlen - ext_len)
+    beg = max(0, end - mem_len)
+    cat = np.concatenate([mem, hid], axis=1)
+    return np.ascontiguousarray(cat[:, beg:end])

@@ -1,0 +1,333 @@
+"""Pins of the fp64 oracle to facts fixed outside the oracle itself.
+
+Each test would fail for a plausible mistake in the oracle: a wrong mask
+boundary (mask picture, one-hot probe), a wrong distance or R-row order
+(golden labels, the pages' pad/reshape/slice shift), a dropped or mis-signed
+term among a, b, c, d (SDPA reductions, rel-shift cross-check), a wrong
+softmax or PV (textbook causal attention, closed-form mean), a wrong memory
+roll (explicit row lists) and a wrong recurrence (whole-sequence brute force).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import txl_workloads as W
+from conftest import read_golden_rows
+
+RNG = np.random.default_rng(12345)
+
+
+def rnd(*shape, std=1.0):
+    return RNG.normal(0.0, std, size=shape)
+
+
+def parse_mask_picture():
+    rows = read_golden_rows("mask_M3_L4.txt")
+    pic = []
+    for ln in rows:
+        cells = ln.split(":", 1)[1].replace("|", " ").split()
+        pic.append([c in ("m", "x") for c in cells])
+    return np.array(pic, dtype=bool)
+
+
+def parse_rel_ids():
+    return np.array([[int(t) for t in ln.split()] for ln in read_golden_rows("rel_ids_M3_L4.txt")])
+
+
+# --------------------------------------------------------------------------
+# mask: the M=3, L=4 picture, through the one-hot-V probe
+# --------------------------------------------------------------------------
+def test_mask_picture_one_hot_probe():
+    """k=0, u=0, r_k=0 make every score 0, so with V_j = e_j the output row is
+    the probability row: uniform on the visible keys, exactly 0 elsewhere."""
+    pic = parse_mask_picture()
+    L, K = pic.shape
+    M = K - L
+    assert (M, L) == (3, 4)
+    dh = 8
+    q = rnd(1, 1, L, dh)
+    k = np.zeros((1, 1, K, dh))
+    v = np.zeros((1, 1, K, dh))
+    for j in range(K):
+        v[0, 0, j, j] = 1.0
+    r = np.zeros((K, 1, dh))
+    u = np.zeros((1, dh))
+    vb = rnd(1, dh)
+    out = oracle.attn(q, k, v, r, u, vb, scale=0.125)[0, 0]
+    probs = out[:, :K]
+    assert np.array_equal(probs > 0, pic)
+    for i in range(L):
+        nvis = pic[i].sum()
+        np.testing.assert_allclose(probs[i][pic[i]], 1.0 / nvis, rtol=0, atol=1e-15)
+        assert np.all(probs[i][~pic[i]] == 0.0)
+
+
+def test_mask_count_matches_visible_pair_formula():
+    for (M, L) in [(3, 4), (0, 5), (7, 2), (128, 128)]:
+        wl = W.Workload("t", 1, 1, 1, L, M, "f32", 1, 1, 0, 1.0, 1.0)
+        K = M + L
+        q = np.zeros((1, 1, L, 1)); k = np.zeros((1, 1, K, 1)); v = np.zeros((1, 1, K, 1))
+        r = np.zeros((K, 1, 1)); z = np.zeros((1, 1))
+        _, s = oracle.attn(q, k, v, r, z, z, 1.0, want_scores=True)
+        assert int(np.isfinite(s).sum()) == wl.visible_pairs()
+
+
+# --------------------------------------------------------------------------
+# distance convention: golden labels and the pages' own pad/reshape/slice
+# --------------------------------------------------------------------------
+def test_distance_labels_golden():
+    """Labelled R (R_row[0] = its distance, v = e_0, q = k = u = 0) makes the
+    score scale * distance; it must equal the page's reference labels."""
+    ids = parse_rel_ids()
+    L, K = ids.shape
+    M = K - L
+    dh = 4
+    r = np.zeros((K, 1, dh))
+    for row in range(K):
+        r[row, 0, 0] = K - 1 - row  # the distance this row encodes
+    vb = np.zeros((1, dh)); vb[0, 0] = 1.0
+    z = np.zeros((1, dh))
+    q = np.zeros((1, 1, L, dh)); k = np.zeros((1, 1, K, dh)); v = rnd(1, 1, K, dh)
+    scale = 0.37
+    _, s = oracle.attn(q, k, v, r, z, vb, scale, want_scores=True)
+    s = s[0, 0]
+    vis = np.isfinite(s)
+    assert np.array_equal(vis, parse_mask_picture())
+    np.testing.assert_allclose(s[vis], scale * ids[vis], rtol=0, atol=1e-14)
+    assert np.all(ids[vis] >= 0)
+
+
+def pages_rel_shift(x):
+    """The shift described in the source-reading notes (RelMultiHeadAttn):
+    prepend one zero column, view the [q, k+1] block as [k+1, q], drop the
+    first row and view the rest back as [q, k].  Written from that
+    description for a single [q, k] matrix."""
+    ql, kl = x.shape
+    padded = np.concatenate([np.zeros((ql, 1)), x], axis=1)
+    flat = padded.reshape(-1)
+    return flat.reshape(kl + 1, ql)[1:].reshape(ql, kl)
+
+
+@pytest.mark.parametrize("M,L", [(3, 4), (5, 5), (0, 6), (9, 3)])
+def test_position_terms_match_pages_rel_shift(M, L):
+    """With k = u = 0 the score is scale*(b+d) = scale*(q+v).R_dist.  The
+    pages compute (q+v)R^T against R rows ordered by the position sequence
+    M+L-1..0 and align it with the pad/reshape/slice shift; on every visible
+    entry that must equal the oracle's direct distance indexing."""
+    K = M + L
+    dh = 6
+    H = 2
+    q = rnd(1, H, L, dh); k = np.zeros((1, H, K, dh)); v = rnd(1, H, K, dh)
+    r = rnd(K, H, dh); u = np.zeros((H, dh)); vb = rnd(H, dh)
+    scale = 0.5
+    _, s = oracle.attn(q, k, v, r, u, vb, scale, want_scores=True)
+    for h in range(H):
+        raw = (q[0, h] + vb[h]) @ r[:, h, :].T   # [L, K], column r <-> distance K-1-r
+        shifted = pages_rel_shift(raw)
+        vis = np.isfinite(s[0, h])
+        np.testing.assert_allclose(s[0, h][vis], scale * shifted[vis], rtol=1e-13, atol=1e-13)
+
+
+def test_scores_depend_on_distance_only_when_content_is_zero():
+    M, L, dh = 4, 5, 3
+    K = M + L
+    q = np.zeros((1, 1, L, dh)); k = np.zeros((1, 1, K, dh)); v = rnd(1, 1, K, dh)
+    r = rnd(K, 1, dh); z = np.zeros((1, dh)); vb = rnd(1, dh)
+    _, s = oracle.attn(q, k, v, r, z, vb, 0.9, want_scores=True)
+    s = s[0, 0]
+    by_dist = {}
+    for i in range(L):
+        for j in range(K):
+            if np.isfinite(s[i, j]):
+                by_dist.setdefault(M + i - j, []).append(s[i, j])
+    for vals in by_dist.values():
+        assert max(vals) - min(vals) < 1e-14
+
+
+# --------------------------------------------------------------------------
+# content terms, mask, softmax and PV against textbook attention (SDPA)
+# --------------------------------------------------------------------------
+def sdpa64(qm, km, vm, scale, allow):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return torch.nn.functional.scaled_dot_product_attention(
+        t(qm), t(km), t(vm), attn_mask=t(allow), scale=scale).numpy()
+
+
+def positions_allow(M, L):
+    """Visibility from positions: key positions -M..L-1, query 0..L-1, a key is
+    visible when its position does not exceed the query's."""
+    key_pos = np.arange(-M, L)
+    q_pos = np.arange(L)
+    return key_pos[None, :] <= q_pos[:, None]
+
+
+@pytest.mark.parametrize("M,L", [(0, 7), (5, 6), (12, 4)])
+def test_content_terms_match_textbook_attention(M, L):
+    """r_k = 0 leaves a + c = (q+u).k_j: textbook attention with query q+u."""
+    B, H, dh = 2, 3, 8
+    K = M + L
+    q = rnd(B, H, L, dh); k = rnd(B, H, K, dh); v = rnd(B, H, K, dh)
+    r = np.zeros((K, H, dh)); u = rnd(H, dh, std=0.5); vb = rnd(H, dh)
+    scale = 1 / math.sqrt(dh)
+    out = oracle.attn(q, k, v, r, u, vb, scale)
+    ref = sdpa64(q + u[None, :, None, :], k, v, scale, positions_allow(M, L))
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_global_content_bias_alone():
+    """q = 0, r_k = 0: the score is scale * u.k_j (term c alone)."""
+    M, L, H, dh = 3, 5, 2, 4
+    K = M + L
+    q = np.zeros((1, H, L, dh)); k = rnd(1, H, K, dh); v = rnd(1, H, K, dh)
+    r = np.zeros((K, H, dh)); u = rnd(H, dh); vb = rnd(H, dh)
+    out = oracle.attn(q, k, v, r, u, vb, 0.7)
+    qq = np.broadcast_to(u[None, :, None, :], (1, H, L, dh))
+    ref = sdpa64(qq, k, v, 0.7, positions_allow(M, L))
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_m0_is_causal_attention():
+    """M = 0 with r_k = u = 0 is ordinary causal softmax attention."""
+    B, H, L, dh = 1, 2, 9, 16
+    q = rnd(B, H, L, dh); k = rnd(B, H, L, dh); v = rnd(B, H, L, dh)
+    z = np.zeros((H, dh))
+    out = oracle.attn(q, k, v, np.zeros((L, H, dh)), z, rnd(H, dh), 0.25)
+    t = lambda a: torch.from_numpy(a)
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=True,
+                                                           scale=0.25).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_closed_form_mean_of_visible_values():
+    """k = 0, u = 0, r_k = 0: out[i] = mean of V over the M+i+1 visible keys."""
+    M, L, dh = 5, 6, 3
+    K = M + L
+    q = rnd(2, 2, L, dh); k = np.zeros((2, 2, K, dh)); v = rnd(2, 2, K, dh)
+    out = oracle.attn(q, k, v, np.zeros((K, 2, dh)), np.zeros((2, dh)), rnd(2, dh), 1.0)
+    for i in range(L):
+        np.testing.assert_allclose(out[:, :, i], v[:, :, :M + i + 1].mean(axis=2), atol=1e-14)
+
+
+def test_pairs_subset_matches_full():
+    M, L, B, H, dh = 4, 3, 3, 2, 5
+    K = M + L
+    args = (rnd(B, H, L, dh), rnd(B, H, K, dh), rnd(B, H, K, dh), rnd(K, H, dh), rnd(H, dh), rnd(H, dh))
+    full = oracle.attn(*args, 0.3)
+    part = oracle.attn(*args, 0.3, pairs=[5, 0, 3])
+    for bh in (0, 3, 5):
+        b, h = divmod(bh, H)
+        assert np.array_equal(part[b, h], full[b, h])
+    assert np.isnan(part[0, 1]).all()
+
+
+# --------------------------------------------------------------------------
+# Tail_M against explicit row lists
+# --------------------------------------------------------------------------
+def rows_tail(mem_rows, hid_rows, mem_len):
+    allrows = list(mem_rows) + list(hid_rows)
+    return allrows[len(allrows) - min(mem_len, len(allrows)):] if mem_len else []
+
+
+@pytest.mark.parametrize("M,L,mlen", [(6, 4, 6), (4, 6, 4), (5, 5, 5), (0, 3, 0),
+                                      (8, 3, 2), (3200 // 100, 128 // 100 + 1, 32)])
+def test_tail_m_rows(M, L, mlen):
+    B, d = 2, 3
+    mem = RNG.integers(0, 1 << 16, size=(B, mlen, d)).astype(np.uint16)
+    hid = RNG.integers(0, 1 << 16, size=(B, L, d)).astype(np.uint16)
+    new = oracle.mem_update(mem, hid, M)
+    for b in range(B):
+        exp = rows_tail([mem[b, t] for t in range(mlen)], [hid[b, t] for t in range(L)], M)
+        assert new.shape[1] == len(exp)
+        for t, row in enumerate(exp):
+            assert np.array_equal(new[b, t], row)
+    assert new.dtype == np.uint16
+
+
+def test_tail_m_ext_len():
+    """ext_len > 0 keeps the cache ext_len tokens shorter at the end."""
+    mem = np.arange(4)[None, :, None]
+    hid = 10 + np.arange(5)[None, :, None]
+    new = oracle.mem_update(mem, hid, mem_len=4, ext_len=2)
+    assert new[0, :, 0].tolist() == [2, 3, 10, 11, 12][-4:]
+
+
+# --------------------------------------------------------------------------
+# the recurrence: segment-by-segment with memory == whole sequence at once
+# --------------------------------------------------------------------------
+def sinusoid64(pos, demb):
+    inv = 1.0 / (10000.0 ** (np.arange(0.0, demb, 2.0) / demb))
+    a = np.asarray(pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.sin(a), np.cos(a)], axis=1)
+
+
+def test_recurrence_matches_whole_sequence_brute_force():
+    """Attention-only stack: B=1, H=2, d_h=16, L=4, M=4, 3 layers, 3 segments.
+    Segment-recurrent (oracle attention + Tail_M, memory starting empty)
+    versus a whole-sequence computation over absolute positions where token t
+    of segment s sees positions max(0, s*L - M) .. t with distance t - p."""
+    B, H, dh, L, Mmax, NL, S = 1, 2, 16, 4, 4, 3, 3
+    d = H * dh
+    T = L * S
+    scale = 1 / math.sqrt(dh)
+    Wq, Wk, Wv, Wr = (rnd(NL, d, d, std=1 / math.sqrt(d)) for _ in range(4))
+    u = rnd(H, dh, std=0.3); vb = rnd(H, dh, std=0.3)
+    X0 = rnd(B, T, d)
+
+    def heads(x):  # [B, T, d] -> [B, H, T, dh]
+        return x.reshape(x.shape[0], x.shape[1], H, dh).transpose(0, 2, 1, 3)
+
+    def merge(o):  # [B, H, T, dh] -> [B, T, d]
+        return o.transpose(0, 2, 1, 3).reshape(o.shape[0], o.shape[2], d)
+
+    # whole sequence, absolute positions
+    X = X0
+    for n in range(NL):
+        Q = heads(X @ Wq[n]); Kf = heads(X @ Wk[n]); Vf = heads(X @ Wv[n])
+        out = np.zeros((B, H, T, dh))
+        for t in range(T):
+            lo = max(0, (t // L) * L - Mmax)
+            ps = np.arange(lo, t + 1)
+            Rt = (sinusoid64(t - ps, d) @ Wr[n]).reshape(len(ps), H, dh)
+            for h in range(H):
+                s = np.array([(Q[0, h, t] + u[h]) @ Kf[0, h, p] + (Q[0, h, t] + vb[h]) @ Rt[c, h]
+                              for c, p in enumerate(ps)]) * scale
+                w = np.exp(s - s.max()); w /= w.sum()
+                out[0, h, t] = w @ Vf[0, h, ps]
+        X = merge(out)
+    brute_last = X[:, (S - 1) * L:]
+
+    # segment recurrent through the oracle
+    mems = [np.zeros((B, 0, d)) for _ in range(NL)]
+    for sgi in range(S):
+        h_in = X0[:, sgi * L:(sgi + 1) * L]
+        for n in range(NL):
+            mem = mems[n]
+            M = mem.shape[1]
+            cat = np.concatenate([mem, h_in], axis=1)
+            q = heads(h_in @ Wq[n]); k = heads(cat @ Wk[n]); v = heads(cat @ Wv[n])
+            r = (sinusoid64(np.arange(M + L - 1, -1, -1), d) @ Wr[n]).reshape(M + L, H, dh)
+            o = oracle.attn(q, k, v, r, u, vb, scale)
+            mems[n] = oracle.mem_update(mem, h_in, Mmax)
+            h_in = merge(o)
+    np.testing.assert_allclose(h_in, brute_last, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# input recipe: the sinusoid table
+# --------------------------------------------------------------------------
+def test_sinusoid_distance_zero_and_layout():
+    emb = W.sinusoid(torch.tensor([0.0, 1.0, 2.0]), 8).double().numpy()
+    assert np.array_equal(emb[0], np.r_[np.zeros(4), np.ones(4)])
+    np.testing.assert_allclose(emb[1, 0], math.sin(1.0), atol=1e-7)
+    np.testing.assert_allclose(emb[1, 4], math.cos(1.0), atol=1e-7)
+    np.testing.assert_allclose(emb[2, 1], math.sin(2.0 / 10000 ** (2 / 8)), atol=1e-7)
+
+
+def test_workload_flop_and_byte_counts():
+    wl = W.WORKLOADS["base512_bf16"]
+    assert wl.visible_pairs() == 393472
+    assert wl.attn_flops() == 6 * 64 * 22 * 8 * 393472
+    assert wl.mem_update_bytes() == 2 * 22 * 512 * 512 * 2
