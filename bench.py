@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the Transformer-XL relative-attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: for every segment
+and every layer of the workload, the fused relative-attention kernel
+(txl_attn_fwd) followed by the in-place Tail_M memory roll (txl_mem_update),
+in the multi-segment driver's order, on one stream.  The per-call inputs
+(Q, K, V projected by the harness, the layer input h) are produced once by
+running the chain (projections in fp32 on the GPU with TF32 off, cast to
+bf16) and stay resident in HBM; a step replays the launch sequence over
+them as one CUDA graph.  Each step reads more than the 129 MB L2 holds
+(several GB for the default workload), so no explicit flush is needed.
+
+Output: one JSON line on rank 0 (see the keys below).  ``--impl reference``
+times the fp64 CPU oracle instead (the reference arm of this method).
+
+Multi-GPU: the path shards over independent replicas (batch rows carry their
+own memories; there is no exchange step), so N ranks each run the same
+workload (weak scaling) and ``value`` = units of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import txl_workloads as W  # noqa: E402
+
+METRIC = "rel-attn TFLOP/s & tokens/s per segment (1×GB300) and % of bf16 tensor peak"
+DEFAULT_WORKLOAD = "base512_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples SM clock, power and throttle reasons with nvidia-smi while the
+    timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return
+        ident = None
+        try:
+            ident = str(torch.cuda.get_device_properties(device_index).uuid)
+            if not ident.startswith("GPU-"):
+                ident = "GPU-" + ident
+        except Exception:
+            ident = None
+        cmd = [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if ident:
+            cmd += ["-i", ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        rows = []
+        for t, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[3], parts[4:9]))
+            except ValueError:
+                continue
+        in_win = [r for r in rows if self.t_start and self.t_stop and
+                  self.t_start - 0.05 <= r[0] <= self.t_stop + 0.05]
+        use = in_win if in_win else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            flags = r[4][1:]
+            for nm, fl in zip(names, flags):
+                if fl.lower() in ("active", "1"):
+                    reasons.add(nm)
+        pw = []
+        for r in use:
+            try:
+                pw.append(float(r[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_in_timed_region": len(in_win),
+                "power_w_max": max(pw) if pw else None}
+
+
+# --------------------------------------------------------------------- our arm
+def build_calls(wl: W.Workload, dev):
+    """Runs the chain once (harness projections + our kernels) and returns the
+    per-call resident inputs.  Layer n+1's input is the head-merged output of
+    layer n; memories roll by Tail_M between segments."""
+    import transformer_xl_relative_attn_gb300 as txl
+    dt = wl.torch_dtype
+    params = W.make_params(wl)
+    lws = [W.LayerWeights(*(getattr(lw, f).to(dev) for f in ("W_q", "W_k", "W_v", "W_r")))
+           for lw in params.layers]
+    mems = [m.to(device=dev, dtype=dt) for m in W.initial_memories(wl)]
+    mems0 = [m.clone() for m in mems]
+    rks = [W.project_r(lw, wl.M, wl.L, wl.H, device=dev).to(dt) for lw in lws]
+    u = params.u.to(device=dev, dtype=dt)
+    vb = params.v.to(device=dev, dtype=dt)
+    calls = []
+    for s in range(wl.segments):
+        h = W.segment_input(wl, s).to(device=dev, dtype=dt)
+        for n in range(wl.layers):
+            q, k, v = W.project_qkv(lws[n], mems[n], h, wl.H)
+            q, k, v = q.to(dt), k.to(dt), v.to(dt)
+            out = torch.empty_like(q)
+            txl.attn_fwd(q, k, v, rks[n], u, vb, wl.scale, out=out)
+            txl.mem_update(mems[n], h)
+            calls.append({"n": n, "q": q, "k": k, "v": v, "h": h, "out": out})
+            h = W.merge_heads(out)
+    torch.cuda.synchronize()
+    txl.check_status()
+    for m, m0 in zip(mems, mems0):
+        m.copy_(m0)
+    return calls, mems, rks, u, vb
+
+
+def run_ours(args, wl: W.Workload):
+    import transformer_xl_relative_attn_gb300 as txl
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    txl.load()
+    peaks, peak_src = load_peaks()
+
+    calls, mems, rks, u, vb = build_calls(wl, dev)
+    n_calls = len(calls)
+    stream = torch.cuda.Stream(device=dev)
+
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in calls]
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in calls]
+
+    def step(timed_events: bool):
+        for c, ea, eb in zip(calls, ev_a, ev_b):
+            if timed_events:
+                ea.record()
+            txl.attn_fwd(c["q"], c["k"], c["v"], rks[c["n"]], u, vb, wl.scale, out=c["out"])
+            if timed_events:
+                eb.record()
+            txl.mem_update(mems[c["n"]], c["h"])
+
+    # capture one step as a CUDA graph (warm the launch path first)
+    with torch.cuda.stream(stream):
+        step(False)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(True)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    txl.check_status()
+
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.2)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    barrier(ws)
+    time.sleep(0.1)
+    sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
+    txl.check_status()
+    elapsed_max = reduce_max(elapsed_ms, ws)
+
+    flops_call = wl.attn_flops()
+    flops_step = flops_call * n_calls
+    tokens_step = wl.B * wl.L * wl.segments
+    value = ws * flops_step * args.steps / (elapsed_max * 1e-3) / 1e12
+    ms_per_step = elapsed_max / args.steps
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = flops_call / (attn_avg_ms * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) hidden states and memories, N(0,0.02) weights, "
+                "sinusoid R; harness projections)",
+        "config": {
+            "workload": wl.name, "B": wl.B, "H": wl.H, "d_h": wl.dh, "L": wl.L, "M": wl.M,
+            "layers": wl.layers, "segments": wl.segments,
+            "calls_per_step": {"txl_attn_fwd": n_calls, "txl_mem_update": n_calls},
+            "global_batch": wl.B * ws, "seq_len": wl.L, "mem_len": wl.M,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "l2": "inputs larger than L2: each step reads "
+                  f"{sum(sum(c[x].numel() * c[x].element_size() for x in ('q', 'k', 'v', 'h')) for c in calls) / 1e9:.2f} GB",
+            "step": "CUDA graph of all (segment, layer) attention + Tail_M launches",
+        },
+        "tokens_per_s": round(ws * tokens_step * args.steps / (elapsed_max * 1e-3), 1),
+        "pct_bf16_peak": round(100.0 * value / ws / peak_tf, 2),
+        "roofline": {
+            "kernel": "attn_tc_bf16_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak_tf,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tf, 4),
+            "traffic": None,
+            "peak_source": f"bf16_tflops_sustained ({peak_src})",
+            "flops_per_launch": flops_call,
+            "avg_launch_ms": round(attn_avg_ms, 5),
+            "launches_averaged": len(attn_ms),
+            "attn_share_of_step": round(sum(attn_ms) / ms_per_step, 4),
+        },
+        "gpu_launches": 2 * n_calls * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = measure_e2e(args, wl, calls, graph, stream, flops_step, ws)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"], result["parity"] = cpu_baseline_and_parity(wl, calls, rks, u, vb)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, wl, calls, graph, stream, flops_step, ws):
+    """Same metric end to end: each step copies every input of the step from
+    pinned host memory, replays the step and reads every output back."""
+    ins = [(c[x], c[x].cpu().pin_memory()) for c in calls for x in ("q", "k", "v", "h")]
+    outs = [(c["out"], torch.empty(c["out"].shape, dtype=c["out"].dtype).pin_memory()) for c in calls]
+    h2d = sum(d.numel() * d.element_size() for d, _ in ins)
+    d2h = sum(d.numel() * d.element_size() for d, _ in outs)
+    steps = max(3, min(args.steps, 10))
+
+    def one():
+        with torch.cuda.stream(stream):
+            for d, hbuf in ins:
+                d.copy_(hbuf, non_blocking=True)
+            graph.replay()
+            for d, hbuf in outs:
+                hbuf.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = reduce_max(time.perf_counter() - t0, ws)
+    return {"value": round(ws * flops_step * steps / el / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(1e3 * el / steps, 3)}
+
+
+def cpu_baseline_and_parity(wl, calls, rks, u, vb):
+    """Times the fp64 oracle on the first call of the workload (segment 0,
+    layer 0, every (batch row, head) pair) on all host cores, and re-checks
+    that call's GPU output against it."""
+    import oracle
+    c = calls[0]
+    host = [t.cpu() for t in (c["q"], c["k"], c["v"], rks[0], u, vb)]
+    t0 = time.perf_counter()
+    ref = oracle.attn(*host, wl.scale)
+    el = time.perf_counter() - t0
+    got = c["out"].float().cpu().double().numpy()
+    err = float(np.abs(got - ref).max())
+    tol = 1e-2 * float(np.abs(ref).max()) + 1e-3
+    cb = {"value": round(wl.attn_flops() / el / 1e12, 6), "unit": "TFLOP/s",
+          "cores": oracle.num_cores(), "kind": "oracle",
+          "sample": f"one txl_attn_fwd call of {wl.name} (segment 0, layer 0, all {wl.B * wl.H} "
+                    f"(b,h) pairs), fp64, {el:.2f} s wall"}
+    par = {"call": "segment 0, layer 0", "max_abs_err": err, "tol": tol, "ok": err <= tol}
+    return cb, par
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args, wl: W.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    ci, _, _ = W.first_call_inputs(wl)
+    n = wl.B * wl.H
+    per_pair_flops = 6 * wl.dh * wl.visible_pairs()
+    rng = np.random.default_rng(0)
+    # size one step to about 0.2-0.5 s of oracle time on this host
+    k_pairs = max(1, min(n, 2 * oracle.num_cores()))
+    host = (ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb)
+
+    def one():
+        pairs = rng.choice(n, size=k_pairs, replace=False)
+        oracle.attn(*host, ci.scale, pairs=pairs)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = per_pair_flops * k_pairs * args.steps / el / 1e12
+    sample = (f"{k_pairs} random (b,h) pairs of the first {wl.name} call per step "
+              f"(of {n}), fp64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "d_h": wl.dh, "L": wl.L, "M": wl.M},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

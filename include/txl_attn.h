@@ -1,0 +1,148 @@
+/*
+ * txl_attn.h -- C ABI of the GB300 (sm_103a) Transformer-XL relative
+ * attention library (libtxl.so).
+ *
+ * The operation is relative multi-head attention over a per-layer recurrence
+ * memory, as defined by:
+ *   - "Transformer-XL" course notes (zty624.github.io), sections
+ *     "Segment-Level Recurrence", "Batched Tensor Contract",
+ *     "Causal Mask With Memory", "Relative Positional Encoding" and
+ *     "Relative Shift Trick";
+ *   - "Transformer-XL模型 核心源码阅读笔记" (CSDN source-reading notes),
+ *     section "Build the model": RelPartialLearnableMultiHeadAttn.forward and
+ *     MemTransformerLM._forward / _update_mems.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, contiguous, row-major, on the current CUDA
+ *     device; every pointer argument is a DEVICE pointer.  The caller owns
+ *     every buffer; the library never allocates, frees or retains them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise the host, except
+ *     txl_sync_status().
+ *   - Return value: TXL_OK (0) on success, a negative txl_status otherwise.
+ *     Argument errors are detected on the host before anything is launched.
+ *     No kernel traps or asserts: a device-side wait that runs past its
+ *     time limit records TXL_ERR_DEVICE_TIMEOUT in a device status word,
+ *     which txl_sync_status() reports and clears.
+ *   - dtype: TXL_BF16 (inputs and output bf16, fp32 accumulation on the
+ *     tensor cores) or TXL_F32 (inputs and output fp32, fp32 CUDA-core path).
+ */
+#ifndef TXL_ATTN_H
+#define TXL_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum txl_dtype {
+    TXL_F32 = 0,
+    TXL_BF16 = 1
+};
+
+enum txl_status {
+    TXL_OK = 0,
+    TXL_ERR_INVALID_ARG = -1,    /* null pointer, B/H/L <= 0, M < 0, bad dtype */
+    TXL_ERR_UNSUPPORTED = -2,    /* a size this build has no kernel for (see each call) */
+    TXL_ERR_MISALIGNED = -3,     /* a base pointer is not 16-byte aligned */
+    TXL_ERR_ALIAS = -4,          /* an output overlaps an input it must not overlap */
+    TXL_ERR_LAUNCH = -5,         /* the CUDA launch itself failed */
+    TXL_ERR_DEVICE_TIMEOUT = -6, /* a bounded device-side wait expired (reported by txl_sync_status) */
+    TXL_ERR_WORKSPACE = -7,      /* workspace pointer null/misaligned or smaller than required */
+    TXL_ERR_CUDA = -8            /* a CUDA runtime/driver call failed (e.g. tensor-map encoding) */
+};
+
+/*
+ * Relative attention forward for one layer and one segment.
+ *
+ *   q      [B, H, L, d_h]      queries of the current segment only
+ *   k, v   [B, H, M+L, d_h]    keys / values: rows 0..M-1 are the memory
+ *                              (previous segment, stop-gradient), rows
+ *                              M..M+L-1 the current segment
+ *   r_k    [M+L, H, d_h]       projected sinusoid position table; row r holds
+ *                              relative distance M+L-1-r (distance 0 last)
+ *   u_bias [H, d_h]            global content bias u   (r_w_bias)
+ *   v_bias [H, d_h]            global position bias v  (r_r_bias)
+ *   out    [B, H, L, d_h]      result
+ *
+ * For query i in [0,L) and key j in [0,M+L):
+ *   visible(i,j) <=> j <= M+i          (all memory keys, causal current keys)
+ *   s(i,j) = scale * ((q_i+u).k_j + (q_i+v).r_k[M+L-1-(M+i-j)])
+ *   out_i  = sum_j softmax_j(s(i,.)) v_j   over visible j only.
+ * M = 0 is ordinary causal attention with a relative bias.
+ *
+ * bf16: d_h must be 64 (TXL_ERR_UNSUPPORTED otherwise); fp32: 1 <= d_h <= 256.
+ * All pointers 16-byte aligned (TXL_ERR_MISALIGNED).  `out` must not overlap
+ * any input (TXL_ERR_ALIAS).  This entry point allocates nothing and never
+ * splits the keys of a query tile across CTAs; txl_attn_fwd_ws may.
+ */
+int txl_attn_fwd(const void* q, const void* k, const void* v, const void* r_k,
+                 const void* u_bias, const void* v_bias,
+                 int B, int H, int L, int M, int d_h, float scale, void* out,
+                 int dtype, void* stream);
+
+/*
+ * Scratch bytes txl_attn_fwd_ws needs for these sizes (0 when the call runs
+ * without splitting the keys).  Never negative; 0 also for invalid sizes.
+ */
+size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype);
+
+/*
+ * txl_attn_fwd with caller-provided scratch: `workspace` (device, 256-byte
+ * aligned, at least txl_attn_workspace_bytes(...) bytes) holds the partial
+ * results of the split-key path.  The library then allocates nothing.
+ * TXL_ERR_WORKSPACE if the buffer is missing, misaligned or too small.
+ * Concurrent calls must use distinct workspaces.
+ */
+int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k,
+                    const void* u_bias, const void* v_bias,
+                    int B, int H, int L, int M, int d_h, float scale, void* out,
+                    int dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Tail_M memory roll, in place ("Transformer-XL" notes, section
+ * "Segment-Level Recurrence": M_{tau+1} = Tail_M([M_tau; H_tau]); source notes
+ * MemTransformerLM._update_mems with ext_len = 0 and a full memory).
+ *
+ *   mems [B, M, d]   memory of one layer, overwritten with the newest M rows
+ *                    of the sequence-axis concatenation [mems; hids]
+ *   hids [B, L, d]   hidden states of the current segment (layer input)
+ *
+ * When L >= M the result is hids[:, L-M:]; when L < M it is
+ * [mems[:, L:]; hids].  Bit-exact copy for any element type; dtype only
+ * fixes the element size (TXL_BF16: 2 bytes, TXL_F32: 4 bytes).  M = 0 is a
+ * no-op.  `mems` must not overlap `hids` (TXL_ERR_ALIAS).  Any alignment is
+ * accepted; 16-byte aligned rows of a multiple of 16 bytes take the
+ * vectorised path.
+ */
+int txl_mem_update(void* mems, const void* hids, int B, int L, int M, int d,
+                   int dtype, void* stream);
+
+/*
+ * Waits for `stream`, then reports and clears the device status word:
+ * TXL_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, TXL_ERR_CUDA if the stream reports a CUDA error, TXL_OK otherwise.
+ */
+int txl_sync_status(void* stream);
+
+/* Human-readable name of a txl_status value (static string). */
+const char* txl_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int txl_version(void);
+
+/*
+ * Test hook for the failure-detection path.  kind = 1 makes the NEXT bf16
+ * attention launch withhold one internal completion signal, so its waiting
+ * warps hit their time limit, record TXL_ERR_DEVICE_TIMEOUT and exit cleanly
+ * (the GPU context stays usable).  kind = 0 clears it.  The hook disarms
+ * itself after one launch.  Not for production use.
+ */
+int txl_debug_inject(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TXL_ATTN_H */

@@ -1,0 +1,17 @@
+"""GB300-native (sm_103a) Transformer-XL relative attention over a per-layer
+recurrence memory.
+
+Public API (all computation runs in libtxl.so's CUDA kernels):
+    attn_fwd, attn_fwd_ws, attn_workspace_bytes   relative attention forward
+    mem_update                                    Tail_M memory roll, in place
+    sync_status, check_status                     device status word
+    SegmentDriver                                 multi-segment, multi-layer driver
+"""
+from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_ws, attn_workspace_bytes,
+                   check_status, debug_inject, header_functions, load, mem_update, status_string,
+                   sync_status, version, LIB_PATH)
+from .driver import SegmentDriver
+
+__all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_ws", "attn_workspace_bytes",
+           "check_status", "debug_inject", "header_functions", "load", "mem_update",
+           "status_string", "sync_status", "version", "SegmentDriver", "LIB_PATH"]

@@ -1,0 +1,205 @@
+"""ctypes binding of libtxl.so (include/txl_attn.h).  Argument marshalling only:
+every step of the computation runs in the library's CUDA kernels.  There is
+no CPU fallback: if the library is missing, every call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libtxl.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "txl_attn.h")
+
+TXL_F32 = 0
+TXL_BF16 = 1
+
+STATUS = {
+    0: "TXL_OK",
+    -1: "TXL_ERR_INVALID_ARG",
+    -2: "TXL_ERR_UNSUPPORTED",
+    -3: "TXL_ERR_MISALIGNED",
+    -4: "TXL_ERR_ALIAS",
+    -5: "TXL_ERR_LAUNCH",
+    -6: "TXL_ERR_DEVICE_TIMEOUT",
+    -7: "TXL_ERR_WORKSPACE",
+    -8: "TXL_ERR_CUDA",
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TxlError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        name = STATUS.get(code, str(code))
+        super().__init__(f"{what}: {name} ({status_string(code)})")
+
+
+def load() -> ctypes.CDLL:
+    """Loads libtxl.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "(the CUDA library is required; there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.txl_attn_fwd.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
+        lib.txl_attn_fwd.restype = i
+        lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
+        lib.txl_attn_fwd_ws.restype = i
+        lib.txl_attn_workspace_bytes.argtypes = [i] * 6
+        lib.txl_attn_workspace_bytes.restype = sz
+        lib.txl_mem_update.argtypes = [vp, vp] + [i] * 5 + [vp]
+        lib.txl_mem_update.restype = i
+        lib.txl_sync_status.argtypes = [vp]
+        lib.txl_sync_status.restype = i
+        lib.txl_status_string.argtypes = [i]
+        lib.txl_status_string.restype = ctypes.c_char_p
+        lib.txl_version.argtypes = []
+        lib.txl_version.restype = i
+        lib.txl_debug_inject.argtypes = [i]
+        lib.txl_debug_inject.restype = i
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/txl_attn.h declares."""
+    with open(HEADER, encoding="utf-8") as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(txl_\w+)\s*\(", text, flags=re.M)
+
+
+def status_string(code: int) -> str:
+    return load().txl_status_string(int(code)).decode()
+
+
+def version() -> tuple[int, int]:
+    v = load().txl_version()
+    return v >> 16, v & 0xFFFF
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TXL_BF16
+    if t.dtype == torch.float32:
+        return TXL_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32 only")
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, shape: tuple, dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _attn_args(q, k, v, r_k, u, vb, scale, out):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d_h]")
+    B, H, L, dh = q.shape
+    K = k.shape[2] if k.dim() == 4 else -1
+    M = K - L
+    if M < 0:
+        raise ValueError("k must be [B, H, M+L, d_h] with M >= 0")
+    dt = q.dtype
+    _need(q, "q", (B, H, L, dh), dt)
+    _need(k, "k", (B, H, K, dh), dt)
+    _need(v, "v", (B, H, K, dh), dt)
+    _need(r_k, "r_k", (K, H, dh), dt)
+    _need(u, "u", (H, dh), dt)
+    _need(vb, "v_bias", (H, dh), dt)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (B, H, L, dh), dt)
+    if scale is None:
+        scale = dh ** -0.5
+    return B, H, L, M, dh, float(scale), out
+
+
+def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None) -> torch.Tensor:
+    """Relative attention forward (txl_attn_fwd).  Shapes: q [B,H,L,dh];
+    k, v [B,H,M+L,dh] (memory rows first); r_k [M+L,H,dh] (row r <->
+    distance M+L-1-r); u, vb [H,dh].  Returns out [B,H,L,dh]."""
+    B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    rc = load().txl_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                             u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(),
+                             _dtype_code(q), _stream(stream, q.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_attn_fwd")
+    return out
+
+
+def attn_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16) -> int:
+    code = TXL_BF16 if dtype == torch.bfloat16 else TXL_F32
+    return int(load().txl_attn_workspace_bytes(B, H, L, M, dh, code))
+
+
+def attn_fwd_ws(q, k, v, r_k, u, vb, workspace, scale=None, out=None, stream=None):
+    """txl_attn_fwd_ws: like attn_fwd with caller-owned scratch (a uint8 CUDA
+    tensor of at least attn_workspace_bytes(...) bytes, or None when 0)."""
+    B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    wp = workspace.data_ptr() if workspace is not None else 0
+    wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().txl_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                                u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(),
+                                _dtype_code(q), wp, wn, _stream(stream, q.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_attn_fwd_ws")
+    return out
+
+
+def mem_update(mems: torch.Tensor, hids: torch.Tensor, stream=None) -> torch.Tensor:
+    """Tail_M roll in place (txl_mem_update): mems [B,M,d] <- newest M rows of
+    [mems; hids], hids [B,L,d].  Returns mems."""
+    if mems.dim() != 3 or hids.dim() != 3:
+        raise ValueError("mems must be [B, M, d] and hids [B, L, d]")
+    B, M, d = mems.shape
+    L = hids.shape[1]
+    _need(mems, "mems", (B, M, d), mems.dtype)
+    _need(hids, "hids", (B, L, d), mems.dtype)
+    rc = load().txl_mem_update(mems.data_ptr(), hids.data_ptr(), B, L, M, d, _dtype_code(mems),
+                               _stream(stream, mems.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_mem_update")
+    return mems
+
+
+def sync_status(stream=None, device=None) -> int:
+    """Waits for the stream and returns (and clears) the device status code."""
+    dev = device if device is not None else torch.cuda.current_device()
+    return int(load().txl_sync_status(_stream(stream, dev)))
+
+
+def check_status(stream=None) -> None:
+    rc = sync_status(stream)
+    if rc != 0:
+        raise TxlError(rc, "device status")
+
+
+def debug_inject(kind: int) -> None:
+    rc = load().txl_debug_inject(int(kind))
+    if rc != 0:
+        raise TxlError(rc, "txl_debug_inject")

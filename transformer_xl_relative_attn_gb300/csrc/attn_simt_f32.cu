@@ -1,0 +1,107 @@
+// fp32 relative attention on CUDA cores (the TXL_F32 path).
+//
+// One warp owns one query row i of one (batch row, head).  Keys are swept in
+// chunks of 32, one key per lane, with an online softmax: each lane forms
+//   s(i,j) = scale * ((q_i+u).k_j + (q_i+v).R[M+L-1-(M+i-j)])
+// for its key ("Transformer-XL模型 核心源码阅读笔记", section "Build the
+// model", RelPartialLearnableMultiHeadAttn.forward: AC + BD after the shift),
+// keys past M+i are masked ("Transformer-XL" notes, section "Causal Mask With
+// Memory"), and the chunk's probabilities are broadcast lane by lane while
+// each lane accumulates its own output columns.  The relative shift is the
+// row index M+L-1-(M+i-j) of R; no shifted score matrix is formed.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace txl {
+
+constexpr int kSimtMaxD = 256;
+constexpr int kSimtWarps = 4;
+
+__global__ void __launch_bounds__(32 * kSimtWarps)
+attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                     const float* __restrict__ v, const float* __restrict__ r,
+                     const float* __restrict__ ub, const float* __restrict__ vb, int B, int H,
+                     int L, int M, int dh, float scale, float* __restrict__ out) {
+    __shared__ float s_qu[kSimtWarps][kSimtMaxD];
+    __shared__ float s_qv[kSimtWarps][kSimtMaxD];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kSimtWarps + warp;
+    if (row >= (long long)B * H * L) return;
+    const int i = (int)(row % L);
+    const long long bh = row / L;
+    const int h = (int)(bh % H);
+    const int K = M + L;
+    const float* qi = q + row * dh;
+    for (int t = lane; t < dh; t += 32) {
+        const float x = qi[t];
+        s_qu[warp][t] = x + ub[h * dh + t];
+        s_qv[warp][t] = x + vb[h * dh + t];
+    }
+    __syncwarp();
+    const float* kb = k + bh * (long long)K * dh;
+    const float* vbase = v + bh * (long long)K * dh;
+    const int nvis = M + i + 1;  // keys 0..M+i are visible
+    const int ncol = (dh + 31) / 32;
+    float acc[kSimtMaxD / 32];
+#pragma unroll
+    for (int c = 0; c < kSimtMaxD / 32; ++c) acc[c] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    for (int j0 = 0; j0 < nvis; j0 += 32) {
+        const int j = j0 + lane;
+        float s = -INFINITY;
+        if (j < nvis) {
+            const int dist = M + i - j;
+            const float* kj = kb + (long long)j * dh;
+            const float* rj = r + ((long long)(K - 1 - dist) * H + h) * dh;
+            float ac = 0.f, bd = 0.f;
+            for (int t = 0; t < dh; ++t) {
+                ac = fmaf(s_qu[warp][t], kj[t], ac);
+                bd = fmaf(s_qv[warp][t], rj[t], bd);
+            }
+            s = scale * (ac + bd);
+        }
+        float cm = s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        const float mn = fmaxf(m, cm);
+        const float alpha = expf(m - mn);  // 0 on the first chunk (m = -inf)
+        const float p = (j < nvis) ? expf(s - mn) : 0.f;
+        float ps = p;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        l = l * alpha + ps;
+        m = mn;
+#pragma unroll
+        for (int c = 0; c < kSimtMaxD / 32; ++c) acc[c] *= alpha;
+        const int nk = min(32, nvis - j0);
+        for (int jj = 0; jj < nk; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, p, jj);
+            const float* vj = vbase + (long long)(j0 + jj) * dh;
+#pragma unroll
+            for (int c = 0; c < kSimtMaxD / 32; ++c) {
+                const int t = lane + 32 * c;
+                if (c < ncol && t < dh) acc[c] = fmaf(pj, vj[t], acc[c]);
+            }
+        }
+    }
+    const float inv = 1.f / l;
+    float* o = out + row * dh;
+#pragma unroll
+    for (int c = 0; c < kSimtMaxD / 32; ++c) {
+        const int t = lane + 32 * c;
+        if (c < ncol && t < dh) o[t] = acc[c] * inv;
+    }
+}
+
+cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
+                                 const float* ub, const float* vb, int B, int H, int L, int M,
+                                 int dh, float scale, float* out, cudaStream_t stream) {
+    const long long rows = (long long)B * H * L;
+    const long long blocks = (rows + kSimtWarps - 1) / kSimtWarps;
+    if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    attn_simt_f32_kernel<<<(unsigned)blocks, 32 * kSimtWarps, 0, stream>>>(
+        q, k, v, r, ub, vb, B, H, L, M, dh, scale, out);
+    return cudaGetLastError();
+}
+
+}  // namespace txl

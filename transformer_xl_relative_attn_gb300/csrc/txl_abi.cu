@@ -1,0 +1,177 @@
+// extern "C" entry points of libtxl.so (declared in include/txl_attn.h):
+// argument validation on the host, then one asynchronous launch on the
+// caller's stream.  Nothing here allocates device memory.
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "txl_attn.h"
+#include "txl_device.cuh"
+
+namespace txl {
+__device__ int g_dev_status = 0;
+
+cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int M, size_t row_bytes,
+                          cudaStream_t stream);
+cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
+                                 const float* ub, const float* vb, int B, int H, int L, int M,
+                                 int dh, float scale, float* out, cudaStream_t stream);
+cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
+                                const void* ub, const void* vb, int B, int H, int L, int M,
+                                float scale, void* out, int inject, int* status,
+                                cudaStream_t stream);
+}  // namespace txl
+
+namespace {
+
+int g_inject = 0;
+
+// Device address of the status word on the current device (looked up per
+// call: cheap, and correct when the caller switches devices).
+int* dev_status_ptr() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, txl::g_dev_status) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+int elem_size(int dtype) { return dtype == TXL_F32 ? 4 : (dtype == TXL_BF16 ? 2 : 0); }
+
+int check_attn_args(const void* q, const void* k, const void* v, const void* r_k,
+                    const void* u_bias, const void* v_bias, int B, int H, int L, int M, int d_h,
+                    const void* out, int dtype) {
+    const int es = elem_size(dtype);
+    if (!es) return TXL_ERR_INVALID_ARG;
+    if (!q || !k || !v || !r_k || !u_bias || !v_bias || !out) return TXL_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || L <= 0 || M < 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
+    if (dtype == TXL_BF16 && d_h != 64) return TXL_ERR_UNSUPPORTED;
+    if (dtype == TXL_F32 && d_h > 256) return TXL_ERR_UNSUPPORTED;
+    // index arithmetic in the kernels uses 32-bit row counts per (b, h)
+    const long long K = (long long)M + L;
+    if (K >= (1ll << 30) || (long long)B * H >= (1ll << 30)) return TXL_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(r_k) || !aligned16(u_bias) ||
+        !aligned16(v_bias) || !aligned16(out))
+        return TXL_ERR_MISALIGNED;
+    const size_t nq = (size_t)B * H * L * d_h * es;
+    const size_t nkv = (size_t)B * H * K * d_h * es;
+    const size_t nr = (size_t)K * H * d_h * es;
+    const size_t nb = (size_t)H * d_h * es;
+    if (overlap(out, nq, q, nq) || overlap(out, nq, k, nkv) || overlap(out, nq, v, nkv) ||
+        overlap(out, nq, r_k, nr) || overlap(out, nq, u_bias, nb) || overlap(out, nq, v_bias, nb))
+        return TXL_ERR_ALIAS;
+    return TXL_OK;
+}
+
+int launch_attn(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                const void* v_bias, int B, int H, int L, int M, int d_h, float scale, void* out,
+                int dtype, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == TXL_BF16) {
+        int* status = dev_status_ptr();
+        if (!status) return TXL_ERR_CUDA;
+        const int inject = g_inject;
+        g_inject = 0;
+        e = txl::launch_attn_tc_bf16(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale, out, inject,
+                                     status, st);
+        if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // tensor-map encoding failed
+    } else {
+        e = txl::launch_attn_simt_f32(
+            static_cast<const float*>(q), static_cast<const float*>(k),
+            static_cast<const float*>(v), static_cast<const float*>(r_k),
+            static_cast<const float*>(u_bias), static_cast<const float*>(v_bias), B, H, L, M, d_h,
+            scale, static_cast<float*>(out), st);
+    }
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int txl_attn_fwd(const void* q, const void* k, const void* v, const void* r_k,
+                 const void* u_bias, const void* v_bias, int B, int H, int L, int M, int d_h,
+                 float scale, void* out, int dtype, void* stream) {
+    const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
+    if (rc != TXL_OK) return rc;
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, stream);
+}
+
+size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype) {
+    (void)B; (void)H; (void)L; (void)M; (void)d_h; (void)dtype;
+    return 0;
+}
+
+int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k,
+                    const void* u_bias, const void* v_bias, int B, int H, int L, int M, int d_h,
+                    float scale, void* out, int dtype, void* workspace, size_t ws_bytes,
+                    void* stream) {
+    const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
+    if (rc != TXL_OK) return rc;
+    const size_t need = txl_attn_workspace_bytes(B, H, L, M, d_h, dtype);
+    if (need) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < need)
+            return TXL_ERR_WORKSPACE;
+    }
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, stream);
+}
+
+int txl_mem_update(void* mems, const void* hids, int B, int L, int M, int d, int dtype,
+                   void* stream) {
+    const int es = elem_size(dtype);
+    if (!es || B <= 0 || L <= 0 || M < 0 || d <= 0) return TXL_ERR_INVALID_ARG;
+    if (M == 0) return TXL_OK;
+    if (!mems || !hids) return TXL_ERR_INVALID_ARG;
+    if ((long long)B * (M < L ? M : L) * d >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    const size_t row = (size_t)d * es;
+    if (overlap(mems, (size_t)B * M * row, hids, (size_t)B * L * row)) return TXL_ERR_ALIAS;
+    const cudaError_t e =
+        txl::launch_tail_m(mems, hids, B, L, M, row, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_sync_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return TXL_ERR_CUDA;
+    int status = 0;
+    e = cudaMemcpyFromSymbol(&status, txl::g_dev_status, sizeof(int));
+    if (e != cudaSuccess) return TXL_ERR_CUDA;
+    if (status != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(txl::g_dev_status, &zero, sizeof(int)) != cudaSuccess)
+            return TXL_ERR_CUDA;
+        return TXL_ERR_DEVICE_TIMEOUT;
+    }
+    return TXL_OK;
+}
+
+const char* txl_status_string(int status) {
+    switch (status) {
+        case TXL_OK: return "ok";
+        case TXL_ERR_INVALID_ARG: return "invalid argument";
+        case TXL_ERR_UNSUPPORTED: return "unsupported size";
+        case TXL_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case TXL_ERR_ALIAS: return "output overlaps an input";
+        case TXL_ERR_LAUNCH: return "kernel launch failed";
+        case TXL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case TXL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case TXL_ERR_CUDA: return "CUDA runtime/driver call failed";
+        default: return "unknown status";
+    }
+}
+
+int txl_version(void) { return (1 << 16) | 0; }
+
+int txl_debug_inject(int kind) {
+    if (kind < 0 || kind > 1) return TXL_ERR_INVALID_ARG;
+    g_inject = kind;
+    return TXL_OK;
+}
+
+}  // extern "C"

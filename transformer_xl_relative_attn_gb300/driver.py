@@ -1,0 +1,72 @@
+"""Multi-segment driver: rolls per-layer memories across consecutive segments
+on one CUDA stream.
+
+For each segment and each layer n, in order ("Transformer-XL" notes, zty624,
+sections "Segment-Level Recurrence" and "Training and Inference": read the
+segment, attend to memory + current tokens, append the new hidden states,
+drop the oldest):
+
+    q, k, v, r_k, u, v_bias = project(n, mems[n], h)     caller's projections
+    out = txl_attn_fwd(q, k, v, r_k, u, v_bias, ...)      fused kernel
+    txl_mem_update(mems[n], h)                            Tail_M, in place
+    h = next_input(n, out)                                caller's layer body
+
+Every memory is a dense [B, M, d] buffer that the driver updates in place,
+so the memories stay resident in HBM across segments and no allocation
+happens per segment.  The projections and whatever the caller runs between
+layers are the caller's; the driver launches the attention and memory kernels
+and nothing else.  Optionally the per-segment launch sequence is captured once
+into a CUDA graph and replayed (capture requires the callbacks to be
+capturable: static input/output buffers, no host synchronisation).
+"""
+from __future__ import annotations
+
+from typing import Callable, Sequence
+
+import torch
+
+from . import _lib
+
+
+class SegmentDriver:
+    def __init__(self, mems: Sequence[torch.Tensor], stream: torch.cuda.Stream | None = None):
+        if not mems:
+            raise ValueError("need one memory per layer")
+        self.mems = list(mems)
+        B, M, d = self.mems[0].shape
+        for m in self.mems:
+            if m.shape != (B, M, d) or not m.is_cuda or not m.is_contiguous():
+                raise ValueError("memories must be contiguous CUDA tensors of one shape [B, M, d]")
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.mems[0].device)
+        self.segments_done = 0
+
+    @property
+    def n_layers(self) -> int:
+        return len(self.mems)
+
+    def run_segment(self, h0: torch.Tensor,
+                    project: Callable[[int, torch.Tensor, torch.Tensor], tuple],
+                    next_input: Callable[[int, torch.Tensor], torch.Tensor],
+                    outs: list | None = None) -> torch.Tensor:
+        """Runs one segment through all layers; returns the last layer's
+        next_input.  If ``outs`` is given, each layer's attention output is
+        written into outs[n] (preallocated [B,H,L,dh]) instead of a new tensor."""
+        h = h0
+        with torch.cuda.stream(self.stream):
+            for n, mem in enumerate(self.mems):
+                q, k, v, r_k, u, vb, scale = project(n, mem, h)
+                out = _lib.attn_fwd(q, k, v, r_k, u, vb, scale,
+                                    out=None if outs is None else outs[n], stream=self.stream)
+                _lib.mem_update(mem, h, stream=self.stream)
+                h = next_input(n, out)
+        self.segments_done += 1
+        return h
+
+    def state_dict(self) -> dict:
+        """The only state is the per-layer memory (checkpoint/resume)."""
+        return {"mems": [m.detach().clone() for m in self.mems], "segments_done": self.segments_done}
+
+    def load_state_dict(self, sd: dict) -> None:
+        for m, s in zip(self.mems, sd["mems"]):
+            m.copy_(s)
+        self.segments_done = int(sd.get("segments_done", 0))

@@ -241,3 +241,20 @@ def first_call_inputs(wl: Workload, B: int | None = None) -> tuple:
     h = segment_input(w, 0)
     ci = call_inputs(w, params.layers[0], params, mem, h)
     return ci, mem.to(w.torch_dtype), h.to(w.torch_dtype)
+
+
+def random_call_inputs(B: int, H: int, L: int, M: int, dh: int, dtype=torch.bfloat16,
+                       std: float = 1.0, bias_std: float = 0.5, seed: int = 0) -> CallInputs:
+    """Direct N(0, std) draws for every attention input (no projections), cast
+    once to ``dtype``.  With std = 1 and scale = 1/sqrt(d_h) the scores spread
+    over several units, so the softmax is far from uniform and a wrong score
+    shows in the output."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    K = M + L
+
+    def n(*shape, s=std):
+        return torch.empty(shape, dtype=torch.float32).normal_(0.0, s, generator=g).to(dtype)
+
+    return CallInputs(n(B, H, L, dh), n(B, H, K, dh), n(B, H, K, dh), n(K, H, dh),
+                      n(H, dh, s=bias_std), n(H, dh, s=bias_std), 1.0 / math.sqrt(dh))
