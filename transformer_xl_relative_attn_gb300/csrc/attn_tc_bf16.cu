@@ -1,7 +1,7 @@
 // Fused Transformer-XL relative attention, bf16 in / fp32 accumulate, on the
 // sm_103a tensor cores (tcgen05 + TMEM), with TMA-staged K, V and R tiles.
 //
-// What one CTA computes: one (batch row b, head h, query tile of 128 rows
+// Unit of work ("item"): one (batch row b, head h, query tile of 128 rows
 // i0..i0+127) against all visible keys, swept in key tiles of 64:
 //
 //   AC(t)    = (q+u) K_t^T                    content terms a + c (64 keys)
@@ -20,24 +20,41 @@
 //
 // Position band.  For query row i0+ii and key j0+jj the distance is
 // M+i0+ii-j0-jj, i.e. R row (L-i0-128+j0) + (127-ii+jj).  Key tile t (j0 =
-// 64t) therefore needs the 191 R rows base+64t .. base+64t+190 (base =
-// L-i0-128): three 64-row "slots" g = t, t+1, t+2 of the sequence base+64g.
-// Consecutive tiles share two slots, so each tile computes only its newest
-// slot (the first tile all three) into a 4-slot ring of TMEM columns: the
-// position MMA does exactly the algorithmic work.  Row ii of the band, read
-// from band column 127-ii onward, is the shifted position term: the pad /
-// reshape / slice of the pages is never performed and no L x (M+L) score
-// matrix exists.  R rows outside [0, M+L) are zero-filled by TMA and only land
-// on masked entries.
+// 64t) needs the 191 R rows base+64t .. base+64t+190 (base = L-i0-128): three
+// 64-row "slots" g = t, t+1, t+2 of the sequence base+64g.  Consecutive tiles
+// share two slots, so each tile computes only its newest slot (the first tile
+// of an item all three) into a 4-slot ring of TMEM columns: the position MMA
+// does exactly the algorithmic work.  Row ii of the band, read from band
+// column 127-ii onward, is the shifted position term: the pad / reshape /
+// slice of the pages is never performed and no L x (M+L) score matrix exists.
+// R rows outside [0, M+L) are zero-filled by TMA and only land on masked
+// entries.
 //
-// Roles (320 threads, one CTA per SM):
-//   warps 0-3  softmax group 0: key tiles 0, 2, 4, ... (one query row per thread)
-//   warps 4-7  softmax group 1: key tiles 1, 3, 5, ...
-//   warp 8     TMEM allocation; lane 0 issues every MMA
-//   warp 9     lane 0 issues the TMA loads into a 3-stage K/V/R ring
-// Each group keeps its own running max, sum and O accumulator (TMEM); the two
-// partial results are merged at the end.  TMEM columns: AC0 0-63, AC1 64-127,
-// position ring 128-383, O0 384-447, O1 448-511.
+// Persistent schedule.  One CTA per SM walks its items (longest query tiles
+// first, snake order over CTAs).  The TMA producer and the MMA issuer stream
+// across item boundaries; (q+u)c / (q+v)c are double-buffered so the next
+// item's scores can start while the current item is finished and stored.
+//
+// Roles (384 threads; warp w runs on SM sub-partition w % 4):
+//   warps 0-7  two softmax groups of 128 threads (one query row per thread);
+//              group g takes the key tiles whose global index is = g (mod 2),
+//              keeps its own running max, sum and O accumulator, and the two
+//              partial results are merged per item
+//   warp 8     TMEM allocation; issues the score MMAs (AC and position slots)
+//   warp 9     lane 0 issues the TMA loads (128-row boxes: per-SM TMA
+//              throughput grows with the box size) and L2 prefetches
+//   warp 10    issues the P V MMAs
+//   warp 11    idle (keeps every sub-partition at three warps)
+// The score and P V chains are issued from different sub-partitions so that
+// neither waits behind the other or behind the softmax warps' instruction
+// streams.
+//
+// TMEM columns: O0 0-63, O1 64-127, AC0 128-191, AC1 192-255, position ring
+// 256-511.  Shared memory: (q+u)c,(q+v)c x2, P x2, K/V ring, R ring.
+//
+// Ordering facts relied on: tcgen05.mma operations from one thread execute in
+// issue order, and a tcgen05.commit arrives only when every MMA issued before
+// it by the same thread has completed.
 //
 // Every wait is bounded (1 s); on expiry the CTA records a status, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
@@ -51,29 +68,41 @@
 namespace txl {
 
 namespace tc {
-constexpr int BM = 128;        // query rows per CTA (TMEM lanes)
+constexpr int BM = 128;        // query rows per item (TMEM lanes)
 constexpr int BN = 64;         // keys per tile
 constexpr int DH = 64;         // head dim: one 128-byte swizzle row
 constexpr int SLOT = 64;       // R rows per position slot
 constexpr int RING = 4;        // position slots held in TMEM
-constexpr int STAGES = 3;
-constexpr int NTHREADS = 320;
+#ifndef TXL_KV_STAGES
+#define TXL_KV_STAGES 3
+#endif
+#ifndef TXL_R_STAGES
+#define TXL_R_STAGES 2
+#endif
+#ifndef TXL_PREFETCH
+#define TXL_PREFETCH 2
+#endif
+constexpr int KV_STAGES = TXL_KV_STAGES;  // K/V ring: each stage holds two key tiles
+constexpr int R_STAGES = TXL_R_STAGES;    // R ring: each box holds two position slots
+constexpr int PREFETCH = TXL_PREFETCH;    // K/V stages warmed into L2 ahead of their load
+static_assert(KV_STAGES >= 2 && R_STAGES >= 2, "the MMA order needs two stages of each ring");
+constexpr int NTHREADS = 384;
 
+constexpr uint32_t SZ_T = BN * DH * 2;      //  8 KB: one 64-row tile
+constexpr uint32_t SZ_BOX = 2 * SZ_T;       // 16 KB: one 128-row TMA box
 constexpr uint32_t SZ_Q = BM * DH * 2;      // 16 KB
-constexpr uint32_t SZ_T = BN * DH * 2;      //  8 KB: one K, V or R slot tile
-constexpr uint32_t SZ_STAGE = 3 * SZ_T;     // K, V, R slot
-constexpr uint32_t SZ_P = BM * BN * 2;      // 16 KB per group
-constexpr uint32_t OFF_QU = 0;
-constexpr uint32_t OFF_QV = OFF_QU + SZ_Q;
-constexpr uint32_t OFF_STAGE = OFF_QV + SZ_Q;
-constexpr uint32_t OFF_PRO = OFF_STAGE + STAGES * SZ_STAGE;  // R slots 0, 1 of the first tile
-constexpr uint32_t OFF_P = OFF_PRO + 2 * SZ_T;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * SZ_P;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_Q = 0;               // buffer b: (q+u)c at +32K*b, (q+v)c at +32K*b+16K
+constexpr uint32_t OFF_P = OFF_Q + 4 * SZ_Q;          // P of group g at +16K*g; merge exchange
+constexpr uint32_t OFF_KV = OFF_P + 2 * SZ_Q;         // stage s: K box, V box
+constexpr uint32_t OFF_R = OFF_KV + KV_STAGES * 2 * SZ_BOX;
+constexpr uint32_t OFF_ML = OFF_R + R_STAGES * SZ_BOX;  // merge exchange of (m, l)
+constexpr uint32_t OFF_BAR = OFF_ML + BM * 8;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one sm_103a CTA");
 
-constexpr uint32_t COL_AC = 0;      // + 64 * group
-constexpr uint32_t COL_RING = 128;  // + 64 * slot
-constexpr uint32_t COL_O = 384;     // + 64 * group
+constexpr uint32_t COL_O = 0;       // + 64 * group
+constexpr uint32_t COL_AC = 128;    // + 64 * group
+constexpr uint32_t COL_RING = 256;  // + 64 * slot
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0);  // K-major B (K, R)
@@ -89,22 +118,51 @@ struct TcParams {
     __nv_bfloat16* out;
     int B, H, L, M;
     int n_qtiles;
+    int n_items;
     float scale_log2;  // scale * log2(e), folded into q+u and q+v
     int inject;        // 1: withhold the first score-ready signal (timeout test)
     int* status;       // device status word
 };
 
 struct TcShared {
-    uint64_t full[tc::STAGES];
-    uint64_t empty[tc::STAGES];
-    uint64_t q_ready;
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done;
+    uint64_t kv_full[tc::KV_STAGES];
+    uint64_t kv_empty[tc::KV_STAGES];
+    uint64_t r_full[tc::R_STAGES];
+    uint64_t r_empty[tc::R_STAGES];
+    uint64_t q_ready;     // (q+u)c and (q+v)c of the next item are in shared memory
+    uint64_t s_full[2];   // scores of the group's next tile are in TMEM
+    uint64_t s_free[2];   // the group has read them into registers
+    uint64_t p_full[2];   // the group's P tile is in shared memory
+    uint64_t pv_done[2];  // the group's last P V MMA finished
+    uint64_t o_done;      // every MMA of the item finished: O may be read
+    uint64_t o_free;      // the merge has read both O accumulators
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+
+// One work item and the quantities every role derives from it.
+struct Item {
+    int bh, h, i0, ntiles, rbase;
+};
+
+// k-th item of this CTA: items are numbered longest query tile first and dealt
+// to CTAs in snake order (rounds alternate direction) to even out the load.
+__device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long w = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+    if (w >= p.n_items) return false;
+    const int n_bh = p.B * p.H;
+    const int qt = p.n_qtiles - 1 - (int)(w / n_bh);
+    it.bh = (int)(w % n_bh);
+    it.h = it.bh % p.H;
+    it.i0 = qt * tc::BM;
+    const int rows_valid = min(tc::BM, p.L - it.i0);
+    const int kmax = p.M + it.i0 + rows_valid - 1;  // last key any row of the tile sees
+    it.ntiles = kmax / tc::BN + 1;
+    it.rbase = p.L - it.i0 - tc::BM;                // R row of slot 0
+    return true;
+}
 
 // Bounded wait that ignores the abort flag: used to drain in-flight copies and
 // MMAs before the CTA releases its shared and tensor memory.
@@ -116,6 +174,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
             return;
         }
     }
+}
+
+// One arrival per warp: every lane has issued its fences before the
+// __syncwarp, which orders their writes before lane 0's release-arrive.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -139,6 +204,13 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     return *reinterpret_cast<float2*>(&r);
 }
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
 attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmR, const TcParams p) {
@@ -153,34 +225,30 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // Work item: longest query tiles first (they see the most keys).
-    const int n_bh = p.B * p.H;
-    const int item = blockIdx.x;
-    const int qt = p.n_qtiles - 1 - item / n_bh;
-    const int bh = item % n_bh;
-    const int h = bh % p.H;
-    const int i0 = qt * BM;
-    const int rows_valid = min(BM, p.L - i0);
-    const int kmax = p.M + i0 + rows_valid - 1;  // last key any row of the tile sees
-    const int ntiles = kmax / BN + 1;
-    const int rbase = p.L - i0 - BM;             // R row of slot 0, position 0
-
     if (warp == 8) {
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sh->full[s], 1);
-            mbar_init(&sh->empty[s], 1);
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(&sh->kv_full[s], 1);
+            mbar_init(&sh->kv_empty[s], 1);
         }
-        mbar_init(&sh->q_ready, 2 * BM);
+        for (int s = 0; s < R_STAGES; ++s) {
+            mbar_init(&sh->r_full[s], 1);
+            mbar_init(&sh->r_empty[s], 1);
+        }
+        // softmax-side barriers count warps: one elected lane per warp arrives
+        mbar_init(&sh->q_ready, 8);
         for (int g = 0; g < 2; ++g) {
             mbar_init(&sh->s_full[g], 1);
-            mbar_init(&sh->p_full[g], BM);
+            mbar_init(&sh->s_free[g], 4);
+            mbar_init(&sh->p_full[g], 4);
+            mbar_init(&sh->pv_done[g], 1);
         }
         mbar_init(&sh->o_done, 1);
-        mbar_init(&sh->drain, 1);
+        mbar_init(&sh->o_free, 8);
+        mbar_init(&sh->drain, 2);  // one commit from each MMA issuer
         sh->abort = 0;
         fence_mbar_init();
     }
@@ -197,276 +265,477 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
     if (warp < 8) {
         // ------------------------------------------------------ softmax groups
-        const int grp = warp >> 2;          // 0: even key tiles, 1: odd key tiles
+        const int grp = warp >> 2;
         const int wq = warp & 3;            // TMEM lane quarter
-        const int ii = tid & 127;           // query row within the tile
-        const int i = i0 + ii;
+        const int ii = tid & 127;           // query row within the item
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        // Group 0 writes (q+u)*c, group 1 (q+v)*c (c = scale*log2 e), rounded
-        // to bf16, as 128-byte swizzled rows (chunk c of row ii at c ^ (ii&7)).
-        {
-            const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.L + i) * DH);
+        const uint32_t col_ac = COL_AC + 64 * grp;
+        const uint32_t p_tile = s_base + OFF_P + grp * SZ_Q;
+        const float qscale = p.scale_log2;
+
+        // (q+u)c (group 0) or (q+v)c (group 1) of an item, rounded to bf16,
+        // as 128-byte swizzled rows (chunk c of row ii at chunk c ^ (ii & 7)).
+        auto write_q = [&](const Item& it, int kbuf, const uint4 (&q4)[8]) {
             const uint4* brow =
-                reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)h * DH);
-            const uint32_t dst = s_base + (grp == 0 ? OFF_QU : OFF_QV) + ii * 128;
-            const float c = p.scale_log2;
+                reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)it.h * DH);
+            const uint32_t dst = s_base + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q + ii * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
-                uint4 q4 = make_uint4(0, 0, 0, 0);
-                if (i < p.L) q4 = qrow[ch];
                 const uint4 b4 = brow[ch];
-                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&q4);
+                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&q4[ch]);
                 const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b4);
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 qf = __bfloat1622float2(q2[e]);
                     const float2 bf = __bfloat1622float2(b2[e]);
-                    w[e] = pack_bf16x2((qf.x + bf.x) * c, (qf.y + bf.y) * c);
+                    w[e] = pack_bf16x2((qf.x + bf.x) * qscale, (qf.y + bf.y) * qscale);
                 }
                 st_shared_v4(dst + ((ch ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&sh->q_ready);
-        }
+            warp_arrive(&sh->q_ready);
+        };
+        auto load_q = [&](const Item& it, uint4 (&q4)[8]) {
+            const int i = it.i0 + ii;
+            const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)it.bh * p.L + i) * DH);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) q4[ch] = (i < p.L) ? qrow[ch] : make_uint4(0, 0, 0, 0);
+        };
 
-        float m_run = -INFINITY;  // running max (log2 domain), may lag the true max by < 8
-        float l_run = 0.f;
         bool ok = true;
-        int it = 0;
-        const uint32_t p_tile = s_base + OFF_P + grp * SZ_P;
-        for (int t = grp; t < ntiles; t += 2, ++it) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&sh->s_full[grp], it & 1, kDevTimeoutSoftmax, abort, p.status));
-            if (!ok) break;
-            tc_fence_after();
-            const int j0 = t * BN;
-            const bool need_mask = (j0 + BN - 1) > (p.M + i0);
-            const int jlim = p.M + i - j0;  // keys jj > jlim are masked
-            float sc[BN];
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int q2 = 0; q2 < BN / 32; ++q2) {
-                uint32_t ac[32], w0[32], w1[32];
-                tmem_ld32(tmem + lane_off + COL_AC + 64 * grp + 32 * q2, ac);
-                // band columns c0 .. c0+63 of this tile, c0 = 96 - 32*wq + 32*q2
-                const int cA = 96 - 32 * wq + 32 * q2, cB = cA + 32;
-                const uint32_t rA = COL_RING + 64 * ((t + (cA >> 6)) & (RING - 1)) + (cA & 63);
-                const uint32_t rB = COL_RING + 64 * ((t + (cB >> 6)) & (RING - 1)) + (cB & 63);
-                tmem_ld32(tmem + lane_off + rA, w0);
-                tmem_ld32(tmem + lane_off + rB, w1);
-                tmem_wait_ld();
-                float win[64];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    win[x] = __uint_as_float(w0[x]);
-                    win[32 + x] = __uint_as_float(w1[x]);
-                }
-                // per-row shift by o = 31 - lane: win[x] <- win[x + o]
-                const int o = 31 - lane;
-#pragma unroll
-                for (int sb = 16; sb >= 1; sb >>= 1) {
-                    const bool take = (o & sb) != 0;
-#pragma unroll
-                    for (int x = 0; x < 32 + sb - 1; ++x) win[x] = take ? win[x + sb] : win[x];
-                }
-#pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    const float2 s2 = add2(make_float2(__uint_as_float(ac[x]), __uint_as_float(ac[x + 1])),
-                                           make_float2(win[x], win[x + 1]));
-                    sc[32 * q2 + x] = s2.x;
-                    sc[32 * q2 + x + 1] = s2.y;
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        if (32 * q2 + x > jlim) sc[32 * q2 + x] = -INFINITY;
-                }
-#pragma unroll
-                for (int x = 0; x < 32; x += 2) tmax = max3(tmax, sc[32 * q2 + x], sc[32 * q2 + x + 1]);
+        Item cur;
+        int it_g = 0;      // tiles this group has processed (all items)
+        int tbase = 0;     // global index of the current item's first tile
+        int gbase = 0;     // global position-slot counter of the item's slot 0
+        if (item_of(p, 0, cur)) {
+            uint4 qn[8];
+            load_q(cur, qn);
+            write_q(cur, 0, qn);
+        }
+        for (int k = 0; ok && item_of(p, k, cur); ++k) {
+            Item nxt;
+            const bool has_next = item_of(p, k + 1, nxt);
+            // the next item's q row: warmed into L2 now, read when it is
+            // written (after this group's first tile, when registers are free)
+            if (has_next && nxt.i0 + ii < p.L) {
+                const void* qrow = p.q + ((size_t)nxt.bh * p.L + nxt.i0 + ii) * DH;
+                asm volatile("prefetch.L2 [%0];" ::"l"(qrow));
             }
-            // Conditional rescale: keep the running max unless the tile's max
-            // exceeds it by more than the threshold (then p <= 2^threshold).
-            const float m_new = (tmax > m_run + kRescaleThreshold) ? tmax : m_run;
-            // A row may have seen no visible key yet in this group (m_new = -inf):
-            // exponentiate against 0 instead, so every p is exactly 0, not NaN.
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_run - m_use);  // 0 until the first visible key, else 1 or < 1
-            if (it > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+            bool next_written = !has_next;
+            auto write_next_q = [&]() {
+                uint4 qn[8];
+                load_q(nxt, qn);
+                write_q(nxt, (k + 1) & 1, qn);
+                next_written = true;
+            };
+            const int i = cur.i0 + ii;
+            float m_run = -INFINITY;  // running max (log2 domain), may lag the true max by < 8
+            float l_run = 0.f;
+            int seen = 0;             // this group's tiles in this item
+            for (int t = (grp - tbase) & 1; t < cur.ntiles; t += 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh->s_full[grp], it_g & 1,
+                                                       kDevTimeoutSoftmax, abort, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                const int j0 = t * BN;
+                const bool need_mask = (j0 + BN - 1) > (p.M + cur.i0);
+                const int jlim = p.M + i - j0;  // keys jj > jlim are masked
+                float sc[BN];
+                float tmax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int q2 = 0; q2 < BN / 32; ++q2) {
+                    uint32_t ac[32], w0[32], w1[32];
+                    tmem_ld32(tmem + lane_off + col_ac + 32 * q2, ac);
+                    // band columns c0 .. c0+63 of this tile, c0 = 96 - 32*wq + 32*q2;
+                    // band column c lives in ring slot (global slot of t) + c/64
+                    // (item slot t + c/64 is global slot gbase + t + c/64)
+                    const int cA = 96 - 32 * wq + 32 * q2, cB = cA + 32;
+                    const uint32_t rA =
+                        COL_RING + 64 * ((gbase + t + (cA >> 6)) & (RING - 1)) + (cA & 63);
+                    const uint32_t rB =
+                        COL_RING + 64 * ((gbase + t + (cB >> 6)) & (RING - 1)) + (cB & 63);
+                    tmem_ld32(tmem + lane_off + rA, w0);
+                    tmem_ld32(tmem + lane_off + rB, w1);
+                    tmem_wait_ld();
+                    if (q2 == BN / 32 - 1) {
+                        tc_fence_before();
+                        warp_arrive(&sh->s_free[grp]);
+                    }
+                    float win[64];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        win[x] = __uint_as_float(w0[x]);
+                        win[32 + x] = __uint_as_float(w1[x]);
+                    }
+                    // per-row shift by o = 31 - lane: win[x] <- win[x + o]
+                    const int o = 31 - lane;
+#pragma unroll
+                    for (int sb = 16; sb >= 1; sb >>= 1) {
+                        const bool take = (o & sb) != 0;
+#pragma unroll
+                        for (int x = 0; x < 32 + sb - 1; ++x) win[x] = take ? win[x + sb] : win[x];
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        const float2 s2 =
+                            add2(make_float2(__uint_as_float(ac[x]), __uint_as_float(ac[x + 1])),
+                                 make_float2(win[x], win[x + 1]));
+                        sc[32 * q2 + x] = s2.x;
+                        sc[32 * q2 + x + 1] = s2.y;
+                    }
+                    if (need_mask) {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            if (32 * q2 + x > jlim) sc[32 * q2 + x] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2)
+                        tmax = max3(tmax, sc[32 * q2 + x], sc[32 * q2 + x + 1]);
+                }
+                // Conditional rescale: keep the running max unless the tile's max
+                // exceeds it by more than the threshold (then p <= 2^threshold).
+                const float m_new = (tmax > m_run + kRescaleThreshold) ? tmax : m_run;
+                // A row may have seen no visible key yet in this group (m_new =
+                // -inf): exponentiate against 0 instead, so every p is 0, not NaN.
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_run - m_use);
+                if (it_g > 0) {
+                    // the group's previous P V must be done before O is rescaled
+                    // or its P buffer rewritten
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh->pv_done[grp], (it_g - 1) & 1,
+                                                           kDevTimeoutSoftmax, abort, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                if (seen > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o32[32];
+                        tmem_ld32(tmem + lane_off + COL_O + 64 * grp + 32 * c, o32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            o32[x] = __float_as_uint(__uint_as_float(o32[x]) * alpha);
+                        tmem_st32(tmem + lane_off + COL_O + 64 * grp + 32 * c, o32);
+                    }
+                    tmem_wait_st();
+                }
+                const float2 negm = make_float2(-m_use, -m_use);
+                float2 rs = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c8 = 0; c8 < BN / 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x =
+                            add2(make_float2(sc[c8 * 8 + 2 * e], sc[c8 * 8 + 2 * e + 1]), negm);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        rs = add2(rs, make_float2(p0, p1));
+                        w[e] = pack_bf16x2(p0, p1);
+                    }
+                    st_shared_v4(p_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                l_run = l_run * alpha + (rs.x + rs.y);
+                m_run = m_new;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                warp_arrive(&sh->p_full[grp]);
+                ++it_g;
+                ++seen;
+                if (!next_written) write_next_q();
+            }
+            if (ok && !next_written) write_next_q();
+            // ---------------------------------------------- merge + store
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&sh->o_done, k & 1, kDevTimeoutSoftmax, abort, p.status));
+            // group 1's partial (m, l, O) goes through shared memory: O into the
+            // idle P buffers (16-byte chunks swizzled by row), m and l apart.
+            // O is streamed in two 32-column halves to keep registers low.
+            float* ml = reinterpret_cast<float*>(smem + OFF_ML);
+            if (ok && grp == 1) {
+                tc_fence_after();
+                ml[2 * ii] = seen ? m_run : -INFINITY;
+                ml[2 * ii + 1] = seen ? l_run : 0.f;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
                     uint32_t o32[32];
-                    tmem_ld32(tmem + lane_off + COL_O + 64 * grp + 32 * c, o32);
+                    tmem_ld32(tmem + lane_off + COL_O + 64 + 32 * hf, o32);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        o32[x] = __float_as_uint(__uint_as_float(o32[x]) * alpha);
-                    tmem_st32(tmem + lane_off + COL_O + 64 * grp + 32 * c, o32);
-                }
-                tmem_wait_st();
-            }
-            const float2 negm = make_float2(-m_use, -m_use);
-            float2 rs = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c8 = 0; c8 < BN / 8; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = add2(make_float2(sc[c8 * 8 + 2 * e], sc[c8 * 8 + 2 * e + 1]), negm);
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    rs = add2(rs, make_float2(p0, p1));
-                    w[e] = pack_bf16x2(p0, p1);
-                }
-                st_shared_v4(p_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
-            }
-            l_run = l_run * alpha + (rs.x + rs.y);
-            m_run = m_new;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sh->p_full[grp]);
-        }
-        // ------------------------------------------------------ merge + store
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&sh->o_done, 0, kDevTimeoutSoftmax, abort, p.status));
-        // the two groups exchange (m, l, O) through the (now idle) stage buffers
-        float* xch = reinterpret_cast<float*>(smem + OFF_STAGE);  // [128][66] floats
-        if (ok) {
-            tc_fence_after();
-            uint32_t o0[32], o1[32];
-            const bool had = grp < ntiles;  // group 1 has no tile when ntiles == 1
-            tmem_ld32(tmem + lane_off + COL_O + 64 * grp, o0);
-            tmem_ld32(tmem + lane_off + COL_O + 64 * grp + 32, o1);
-            tmem_wait_ld();
-            if (grp == 1) {
-                float* row = xch + ii * 66;
-                row[0] = had ? m_run : -INFINITY;
-                row[1] = had ? l_run : 0.f;
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    row[2 + x] = had ? __uint_as_float(o0[x]) : 0.f;
-                    row[34 + x] = had ? __uint_as_float(o1[x]) : 0.f;
-                }
-            }
-        }
-        // both groups reach this barrier on every path (ok is warp-uniform)
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (ok && grp == 0) {
-            uint32_t o0[32], o1[32];
-            tmem_ld32(tmem + lane_off + COL_O, o0);
-            tmem_ld32(tmem + lane_off + COL_O + 32, o1);
-            tmem_wait_ld();
-            const float* row = xch + ii * 66;
-            const float m1 = row[0], l1 = row[1];
-            const float m = fmaxf(m_run, m1);
-            const float f0 = ex2(m_run - m), f1 = ex2(m1 - m);
-            const float inv = 1.f / (l_run * f0 + l1 * f1);
-            const float a0 = f0 * inv, a1 = f1 * inv;
-            if (i < p.L) {
-                uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.L + i) * DH);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int x = 8 * c + e;
-                        const float mine = __uint_as_float(x < 32 ? o0[x] : o1[x - 32]);
-                        v[e] = mine * a0 + row[2 + x] * a1;
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t a = s_base + OFF_P + ii * 256 + (((8 * hf + c) ^ (ii & 15)) << 4);
+                        // a group without a tile in this item holds stale O: send zeros
+                        if (seen)
+                            st_shared_v4(a, o32[4 * c], o32[4 * c + 1], o32[4 * c + 2], o32[4 * c + 3]);
+                        else
+                            st_shared_v4(a, 0u, 0u, 0u, 0u);
                     }
-                    uint4 w;
-                    w.x = pack_bf16x2(v[0], v[1]);
-                    w.y = pack_bf16x2(v[2], v[3]);
-                    w.z = pack_bf16x2(v[4], v[5]);
-                    w.w = pack_bf16x2(v[6], v[7]);
-                    orow[c] = w;
                 }
+                tc_fence_before();
+                warp_arrive(&sh->o_free);
             }
+            // both groups reach this barrier on every path (ok is warp-uniform)
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (ok && grp == 0) {
+                tc_fence_after();
+                const float m1 = ml[2 * ii], l1 = ml[2 * ii + 1];
+                const float m = fmaxf(m_run, m1);
+                const float f0 = ex2(m_run - m), f1 = ex2(m1 - m);
+                const float inv = 1.f / (l_run * f0 + l1 * f1);
+                const float a0 = seen ? f0 * inv : 0.f, a1 = f1 * inv;
+                uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t o32[32];
+                    tmem_ld32(tmem + lane_off + COL_O + 32 * hf, o32);
+                    tmem_wait_ld();
+                    if (!seen) {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) o32[x] = 0u;  // stale O contributes zero
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float x0[4], x1[4];
+                        const int ch = 8 * hf + 2 * c;
+                        ld_shared_v4(s_base + OFF_P + ii * 256 + ((ch ^ (ii & 15)) << 4), x0);
+                        ld_shared_v4(s_base + OFF_P + ii * 256 + (((ch + 1) ^ (ii & 15)) << 4), x1);
+                        const uint32_t* mine = &o32[8 * c];
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(mine[0]) * a0 + x0[0] * a1,
+                                          __uint_as_float(mine[1]) * a0 + x0[1] * a1);
+                        w.y = pack_bf16x2(__uint_as_float(mine[2]) * a0 + x0[2] * a1,
+                                          __uint_as_float(mine[3]) * a0 + x0[3] * a1);
+                        w.z = pack_bf16x2(__uint_as_float(mine[4]) * a0 + x1[0] * a1,
+                                          __uint_as_float(mine[5]) * a0 + x1[1] * a1);
+                        w.w = pack_bf16x2(__uint_as_float(mine[6]) * a0 + x1[2] * a1,
+                                          __uint_as_float(mine[7]) * a0 + x1[3] * a1);
+                        if (i < p.L) orow[4 * hf + c] = w;
+                    }
+                }
+                tc_fence_before();
+                warp_arrive(&sh->o_free);
+            }
+            // the exchange buffers are the P buffers: read before anyone reuses them
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            // a failed wait anywhere sets the abort flag: both groups leave
+            // together, so neither waits alone at the named barrier
+            if (*abort) ok = false;
+            tbase += cur.ntiles;
+            gbase += cur.ntiles + 2;
         }
         tc_fence_before();
     } else if (warp == 8) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t a_qu = s_base + OFF_QU, a_qv = s_base + OFF_QV;
-            bool ok = mbar_wait(&sh->q_ready, 0, kDevTimeoutMma, abort, p.status);
-            tc_fence_after();
-            // S(t): content MMA into AC[t&1], newest position slot(s) into the ring
-            auto issue_s = [&](int t) -> bool {
-                const int s = t % STAGES;
-                if (!mbar_wait(&sh->full[s], (t / STAGES) & 1, kDevTimeoutMma, abort, p.status))
-                    return false;
-                tc_fence_after();
-                const uint32_t sK = s_base + OFF_STAGE + s * SZ_STAGE;
-                const uint32_t sR = sK + 2 * SZ_T;
-#pragma unroll
-                for (int k = 0; k < DH / 16; ++k)
-                    mma_bf16(tmem + COL_AC + 64 * (t & 1), smem_desc_sw128(a_qu + 32 * k, 16, 1024),
-                             smem_desc_sw128(sK + 32 * k, 16, 1024), IDESC_N64, k > 0);
-                if (t == 0) {
-                    for (int g = 0; g < 2; ++g) {
-                        const uint32_t sRp = s_base + OFF_PRO + g * SZ_T;
-#pragma unroll
-                        for (int k = 0; k < DH / 16; ++k)
-                            mma_bf16(tmem + COL_RING + 64 * g, smem_desc_sw128(a_qv + 32 * k, 16, 1024),
-                                     smem_desc_sw128(sRp + 32 * k, 16, 1024), IDESC_N64, k > 0);
-                    }
-                }
-                const int gslot = t + 2;
-#pragma unroll
-                for (int k = 0; k < DH / 16; ++k)
-                    mma_bf16(tmem + COL_RING + 64 * (gslot & (RING - 1)),
-                             smem_desc_sw128(a_qv + 32 * k, 16, 1024),
-                             smem_desc_sw128(sR + 32 * k, 16, 1024), IDESC_N64, k > 0);
-                if (!(p.inject == 1 && t == 0)) mma_commit(&sh->s_full[t & 1]);
-                return true;
+        // ------------------------------------------------ score MMA issuer
+        // Issues S(0), S(1), ... in order; the P V MMAs go out from warp 10,
+        // so the two chains run on different SM sub-partitions.  The whole
+        // warp waits (bounded mbarrier waits, voted) and one elected lane
+        // issues the MMAs and commits.
+        //
+        // S(T) overwrites AC[T&1], last read by tile T-2, and one position
+        // slot (three for the first tile of an item) whose earlier readers are
+        // tiles <= T-2 (<= T-1 for the first tile of an item).  s_free of each
+        // group completes once per tile of that group, in order; this warp
+        // observes those completions in order and never falls two phases
+        // behind: a group's next completion needs an S not yet issued.
+        const uint32_t leader = elect_one();
+        {
+            bool ok = true;
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                if (ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, kDevTimeoutMma, abort, p.status));
+                return ok;
             };
-            for (int t = 0; ok && t < 2 && t < ntiles; ++t) ok = issue_s(t);
-            for (int t = 0; ok && t < ntiles; ++t) {
-                const int g = t & 1;
-                if (!mbar_wait(&sh->p_full[g], (t >> 1) & 1, kDevTimeoutMma, abort, p.status)) {
-                    ok = false;
-                    break;
+            int seen0 = 0, seen1 = 0;  // s_free completions observed, per group
+            auto s_free_of = [&](int T) {  // tile T (global) has read its scores
+                if (T < 0) return;
+                int& seen = (T & 1) ? seen1 : seen0;
+                while (ok && seen <= (T >> 1)) {
+                    wait(&sh->s_free[T & 1], seen & 1);
+                    ++seen;
                 }
+            };
+            // Shared-memory descriptors of every operand buffer, precomputed;
+            // a k-step of 16 elements (32 bytes) adds 2 to the address field
+            // (16-byte units), a V k-step of 16 rows adds 128.
+            const uint64_t dQ0 = smem_desc_sw128(s_base + OFF_Q, 16, 1024);
+            const uint64_t dK0 = smem_desc_sw128(s_base + OFF_KV, 16, 1024);
+            const uint64_t dR0 = smem_desc_sw128(s_base + OFF_R, 16, 1024);
+            constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
+            // S cursor
+            Item is;
+            bool s_valid = item_of(p, 0, is);
+            int ks = 0, ts = 0, Ts = 0;  // item, local tile, global tile of the next S
+            int kv_s = 0;                // K/V stage counter at the item's first stage
+            int r_s = 0, r_rel = 0;      // R box counter at the item's first box; released boxes
+            int gslot = 0;               // global position-slot counter
+
+            auto issue_s = [&]() {
+                const int stage = kv_s + (ts >> 1);
+                const int nrb = (is.ntiles + 3) >> 1;
+                const int nslots = (ts == 0) ? 3 : 1;
+                if (ts == 0) {
+                    wait(&sh->q_ready, ks & 1);
+                    s_free_of(Ts - 1);
+                }
+                s_free_of(Ts - 2);
+                s_free_of(Ts - 3);
+                // a K/V stage and an R box are waited for by their first reader:
+                // S(ts) reads slots 0..2 (boxes 0, 1) for ts = 0, else slot ts+2
+                // in box (ts+2)/2, which is new when ts is even
+                if (!(ts & 1)) wait(&sh->kv_full[stage % KV_STAGES], (stage / KV_STAGES) & 1);
+                if (ts == 0) {
+                    wait(&sh->r_full[r_s % R_STAGES], (r_s / R_STAGES) & 1);
+                    wait(&sh->r_full[(r_s + 1) % R_STAGES], ((r_s + 1) / R_STAGES) & 1);
+                } else if (!(ts & 1)) {
+                    const int rbox = r_s + ((ts + 2) >> 1);
+                    wait(&sh->r_full[rbox % R_STAGES], (rbox / R_STAGES) & 1);
+                }
+                if (!ok) return;
                 tc_fence_after();
-                const int s = t % STAGES;
-                const uint32_t sV = s_base + OFF_STAGE + s * SZ_STAGE + SZ_T;
-                const uint32_t aP = s_base + OFF_P + g * SZ_P;
+                const uint64_t a_qu = dQ0 + (ks & 1) * 2 * U_Q;
+                const uint64_t a_qv = a_qu + U_Q;
+                const uint64_t b_k = dK0 + (stage % KV_STAGES) * 2 * U_BOX + (ts & 1) * U_T;
+                const uint32_t d_ac = tmem + COL_AC + 64 * (Ts & 1);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                    mma_bf16(tmem + COL_O + 64 * g, smem_desc_sw128(aP + 32 * k, 16, 1024),
-                             smem_desc_sw128(sV + k * 2048, BN * 128, 1024), IDESC_PV,
-                             (t > 1 || k > 0) ? 1u : 0u);
-                mma_commit(&sh->empty[s]);
-                if (t + 2 < ntiles) ok = issue_s(t + 2);
-            }
-            if (ok) mma_commit(&sh->o_done);
-            mma_commit(&sh->drain);
+                for (int k = 0; k < DH / 16; ++k)
+                    mma_ss_elect(d_ac, a_qu + 2 * k, b_k + 2 * k, IDESC_N64, k > 0, leader);
+                // item-local slot g lives at R box r_s + g/2, half g&1
+                for (int j = 0; j < nslots; ++j) {
+                    const int g = (ts == 0) ? j : ts + 2;
+                    const int box = r_s + (g >> 1);
+                    const uint64_t b_r = dR0 + (box % R_STAGES) * U_BOX + (g & 1) * U_T;
+                    const uint32_t d_r = tmem + COL_RING + 64 * ((gslot + j) & (RING - 1));
+#pragma unroll
+                    for (int k = 0; k < DH / 16; ++k)
+                        mma_ss_elect(d_r, a_qv + 2 * k, b_r + 2 * k, IDESC_N64, k > 0, leader);
+                }
+                if (leader && !(p.inject == 1 && Ts == 0)) mma_commit(&sh->s_full[Ts & 1]);
+                // release the R boxes no later S of this item reads:
+                // box v is last read by S(min(max(2v-1, 0), ntiles-1))
+                while (r_rel < nrb && min(max(2 * r_rel - 1, 0), is.ntiles - 1) <= ts) {
+                    if (leader) mma_commit(&sh->r_empty[(r_s + r_rel) % R_STAGES]);
+                    ++r_rel;
+                }
+                gslot += nslots;
+                ++Ts;
+                if (++ts == is.ntiles) {
+                    kv_s += (is.ntiles + 1) >> 1;
+                    r_s += nrb;
+                    r_rel = 0;
+                    ts = 0;
+                    ++ks;
+                    s_valid = item_of(p, ks, is);
+                }
+            };
+
+            while (ok && s_valid) issue_s();
+            if (leader) mma_commit(&sh->drain);
             drain_wait(&sh->drain, 0, p.status);
         }
         __syncwarp();
-    } else {
+    } else if (warp == 10) {
+        // ------------------------------------------------- P V MMA issuer
+        // PV(0), PV(1), ... in order: PV(T) waits for tile T's P; the first
+        // P V of an item also for the merge of the previous item to have
+        // read O.  p_full of a group cannot complete twice before PV(T) is
+        // issued: the group's next P waits for pv_done of this one.
+        const uint32_t leader = elect_one();
+        {
+            bool ok = true;
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                if (ok)
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, kDevTimeoutMma, abort, p.status));
+                return ok;
+            };
+            const uint64_t dP0 = smem_desc_sw128(s_base + OFF_P, 16, 1024);
+            const uint64_t dV0 = smem_desc_sw128(s_base + OFF_KV + SZ_BOX, BN * 128, 1024);
+            constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
+            Item ip;
+            bool p_valid = item_of(p, 0, ip);
+            int kp = 0, tp = 0, Tp = 0, kv_p = 0;
+            while (ok && p_valid) {
+                const int g = Tp & 1;
+                wait(&sh->p_full[g], (Tp >> 1) & 1);
+                if (tp == 0 && kp > 0) wait(&sh->o_free, (kp - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                // K/V stage of tile tp; a stage is free once both of its tiles
+                // went through P V (their S finished before their P existed)
+                const int stage = kv_p + (tp >> 1);
+                const uint64_t b_v = dV0 + (stage % KV_STAGES) * 2 * U_BOX + (tp & 1) * U_T;
+                const uint64_t a_p = dP0 + g * U_Q;
+                const uint32_t d_o = tmem + COL_O + 64 * g;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_ss_elect(d_o, a_p + 2 * k, b_v + 128 * k, IDESC_PV,
+                                 (tp > 1 || k > 0) ? 1u : 0u, leader);
+                if (leader) {
+                    mma_commit(&sh->pv_done[g]);
+                    if ((tp & 1) || tp == ip.ntiles - 1) mma_commit(&sh->kv_empty[stage % KV_STAGES]);
+                    if (tp + 1 == ip.ntiles) mma_commit(&sh->o_done);
+                }
+                ++Tp;
+                if (++tp == ip.ntiles) {
+                    kv_p += (ip.ntiles + 1) >> 1;
+                    tp = 0;
+                    ++kp;
+                    p_valid = item_of(p, kp, ip);
+                }
+            }
+            if (leader) mma_commit(&sh->drain);
+            drain_wait(&sh->drain, 0, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % STAGES;
-                if (t >= STAGES && !mbar_wait(&sh->empty[s], ((t / STAGES) & 1) ^ 1,
-                                              kDevTimeoutProducer, abort, p.status))
-                    break;
-                uint8_t* st = smem + OFF_STAGE + s * SZ_STAGE;
-                mbar_expect_tx(&sh->full[s], SZ_STAGE + (t == 0 ? 2 * SZ_T : 0));
-                const int j0 = t * BN;
-                tma_load_3d(st, &tmK, &sh->full[s], 0, j0, bh);
-                tma_load_3d(st + SZ_T, &tmV, &sh->full[s], 0, j0, bh);
-                tma_load_2d(st + 2 * SZ_T, &tmR, &sh->full[s], h * DH, rbase + SLOT * (t + 2));
-                if (t == 0) {
-                    tma_load_2d(smem + OFF_PRO, &tmR, &sh->full[s], h * DH, rbase);
-                    tma_load_2d(smem + OFF_PRO + SZ_T, &tmR, &sh->full[s], h * DH, rbase + SLOT);
+            int kvc = 0, rc = 0;  // loads issued into each ring
+            bool ok = true;
+            Item it;
+            for (int k = 0; ok && item_of(p, k, it); ++k) {
+                const int nkv = (it.ntiles + 1) >> 1;  // K/V stages of this item
+                const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
+                int rb = 0;
+                for (int u = 0; ok && u < nkv; ++u) {
+                    // R boxes that S(2u) and S(2u+1) read, then the K/V stage
+                    for (; rb <= u + 1 && rb < nrb; ++rb, ++rc) {
+                        const int s = rc % R_STAGES;
+                        if (rc >= R_STAGES && !mbar_wait(&sh->r_empty[s], ((rc / R_STAGES) & 1) ^ 1,
+                                                         kDevTimeoutProducer, abort, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&sh->r_full[s], SZ_BOX);
+                        tma_load_2d(smem + OFF_R + s * SZ_BOX, &tmR, &sh->r_full[s], it.h * DH,
+                                    it.rbase + SLOT * 2 * rb);
+                    }
+                    if (!ok) break;
+                    const int s = kvc % KV_STAGES;
+                    if (kvc >= KV_STAGES && !mbar_wait(&sh->kv_empty[s], ((kvc / KV_STAGES) & 1) ^ 1,
+                                                       kDevTimeoutProducer, abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    // warm L2 PREFETCH stages ahead (the first ones at the item start)
+                    for (int w = (u == 0 ? 1 : u + PREFETCH); w <= u + PREFETCH && w < nkv; ++w) {
+                        tma_prefetch_l2_3d(&tmK, 0, w * 2 * BN, it.bh);
+                        tma_prefetch_l2_3d(&tmV, 0, w * 2 * BN, it.bh);
+                        tma_prefetch_l2_2d(&tmR, it.h * DH, it.rbase + SLOT * 2 * (w + 1));
+                    }
+                    mbar_expect_tx(&sh->kv_full[s], 2 * SZ_BOX);
+                    uint8_t* st = smem + OFF_KV + s * 2 * SZ_BOX;
+                    tma_load_3d(st, &tmK, &sh->kv_full[s], 0, u * 2 * BN, it.bh);
+                    tma_load_3d(st + SZ_BOX, &tmV, &sh->kv_full[s], 0, u * 2 * BN, it.bh);
+                    ++kvc;
                 }
-                issued = t + 1;
             }
-            // drain: the last load of each stage has landed
-            for (int t = issued - STAGES; t < issued; ++t)
-                if (t >= 0) drain_wait(&sh->full[t % STAGES], (t / STAGES) & 1, p.status);
+            // drain: the last load into each ring slot has landed
+            for (int c = kvc - KV_STAGES; c < kvc; ++c)
+                if (c >= 0) drain_wait(&sh->kv_full[c % KV_STAGES], (c / KV_STAGES) & 1, p.status);
+            for (int c = rc - R_STAGES; c < rc; ++c)
+                if (c >= 0) drain_wait(&sh->r_full[c % R_STAGES], (c / R_STAGES) & 1, p.status);
         }
         __syncwarp();
     }
@@ -510,6 +779,17 @@ static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const cuui
     return r == CUDA_SUCCESS;
 }
 
+static int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
                                 const void* ub, const void* vb, int B, int H, int L, int M,
@@ -528,14 +808,14 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     {
         cuuint64_t dims[3] = {(cuuint64_t)DH, (cuuint64_t)K, (cuuint64_t)B * H};
         cuuint64_t strides[2] = {(cuuint64_t)DH * 2, (cuuint64_t)K * DH * 2};
-        cuuint32_t box[3] = {DH, BN, 1};
+        cuuint32_t box[3] = {DH, 2 * BN, 1};
         if (!encode_bf16(&mK, k, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!encode_bf16(&mV, v, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[2] = {(cuuint64_t)H * DH, (cuuint64_t)K};
         cuuint64_t strides[1] = {(cuuint64_t)H * DH * 2};
-        cuuint32_t box[2] = {DH, SLOT};
+        cuuint32_t box[2] = {DH, 2 * SLOT};
         if (!encode_bf16(&mR, r, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     TcParams p;
@@ -548,12 +828,14 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.L = L;
     p.M = M;
     p.n_qtiles = (L + BM - 1) / BM;
+    const long long n_items = (long long)B * H * p.n_qtiles;
+    if (n_items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    p.n_items = (int)n_items;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.inject = inject;
     p.status = status;
-    const long long grid = (long long)B * H * p.n_qtiles;
-    if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    attn_tc_bf16_kernel<<<(unsigned)grid, NTHREADS, SMEM_BYTES, stream>>>(mK, mV, mR, p);
+    const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
+    attn_tc_bf16_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mK, mV, mR, p);
     return cudaGetLastError();
 }
 
