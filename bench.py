@@ -305,7 +305,7 @@ def run_ours(args, wl: W.Workload):
             "peak": peak_tf,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4),
-            "traffic": None,
+            "traffic": measured_traffic(wl.name),
             "peak_source": f"bf16_tflops_sustained ({peak_src})",
             "flops_per_launch": flops_call,
             "avg_launch_ms": round(attn_avg_ms, 5),
@@ -325,6 +325,32 @@ def run_ours(args, wl: W.Workload):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
+# launch, from an ncu capture summarised under profiles/; reported only while
+# the kernel sources still hash to what was captured.
+_TRAFFIC_CAPTURES = {
+    "base512_bf16": {
+        "sha256_prefix": {"attn_tc_bf16.cu": "39e4e4e8243f1a1e", "txl_device.cuh": "8b9b396a7f9d2a8b"},
+        "bytes_per_launch": 61122560,
+        "summary": "profiles/attn_tc_bf16_base512_ncu_full.md",
+    },
+}
+
+
+def measured_traffic(workload):
+    import hashlib
+
+    cap = _TRAFFIC_CAPTURES.get(workload)
+    if cap is None:
+        return None
+    csrc = os.path.join(ROOT, "transformer_xl_relative_attn_gb300", "csrc")
+    for name, prefix in cap["sha256_prefix"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != prefix:
+                return None
+    return cap["bytes_per_launch"]
 
 
 def measure_e2e(args, wl, calls, graph, stream, flops_step, ws):

@@ -550,10 +550,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             int seen0 = 0, seen1 = 0;  // s_free completions observed, per group
             auto s_free_of = [&](int T) {  // tile T (global) has read its scores
                 if (T < 0) return;
-                int& seen = (T & 1) ? seen1 : seen0;
-                while (ok && seen <= (T >> 1)) {
-                    wait(&sh->s_free[T & 1], seen & 1);
-                    ++seen;
+                const int n = T >> 1;
+                if (T & 1) {
+                    for (; ok && seen1 <= n; ++seen1) wait(&sh->s_free[1], seen1 & 1);
+                } else {
+                    for (; ok && seen0 <= n; ++seen0) wait(&sh->s_free[0], seen0 & 1);
                 }
             };
             // Shared-memory descriptors of every operand buffer, precomputed;
