@@ -71,6 +71,14 @@ def reduce_max(x: float, ws: int) -> float:
     return float(t.item())
 
 
+def whole_job_rate(elapsed_ms_local: float, ws: int, work_per_step: float, steps: int):
+    """Whole-job throughput over ``ws`` replicas that each did ``work_per_step``
+    per step: the slowest rank's time (max over ranks) divides the work of all
+    ranks.  Returns (rate per second, max elapsed ms)."""
+    elapsed_max = reduce_max(elapsed_ms_local, ws)
+    return ws * work_per_step * steps / (elapsed_max * 1e-3), elapsed_max
+
+
 def barrier(ws: int):
     if ws > 1:
         import torch.distributed as dist
@@ -261,12 +269,11 @@ def run_ours(args, wl: W.Workload):
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
     txl.check_status()
-    elapsed_max = reduce_max(elapsed_ms, ws)
-
     flops_call = wl.attn_flops()
     flops_step = flops_call * n_calls
     tokens_step = wl.B * wl.L * wl.segments
-    value = ws * flops_step * args.steps / (elapsed_max * 1e-3) / 1e12
+    rate, elapsed_max = whole_job_rate(elapsed_ms, ws, flops_step, args.steps)
+    value = rate / 1e12
     ms_per_step = elapsed_max / args.steps
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = flops_call / (attn_avg_ms * 1e-3) / 1e12
