@@ -22,9 +22,10 @@
 // M+i0+ii-j0-jj, i.e. R row (L-i0-128+j0) + (127-ii+jj).  Key tile t (j0 =
 // 64t) needs the 191 R rows base+64t .. base+64t+190 (base = L-i0-128): three
 // 64-row "slots" g = t, t+1, t+2 of the sequence base+64g.  Consecutive tiles
-// share two slots, so each tile computes only its newest slot (the first tile
-// of an item all three) into a 4-slot ring of TMEM columns: the position MMA
-// does exactly the algorithmic work.  Row ii of the band, read from band
+// share two slots, so the key tiles go out in pairs (2p, 2p+1) and each pair
+// computes only its two newest slots 2p+2, 2p+3 (the first pair slots 0-3),
+// one 128-row R box, into a 4-slot ring of TMEM columns: the position MMA does
+// the algorithmic work plus at most one slot per item.  Row ii of the band, read from band
 // column 127-ii onward, is the shifted position term: the pad / reshape /
 // slice of the pages is never performed and no L x (M+L) score matrix exists.
 // R rows outside [0, M+L) are zero-filled by TMA and only land on masked
@@ -37,7 +38,7 @@
 //
 // Roles (384 threads; warp w runs on SM sub-partition w % 4):
 //   warps 0-7  two softmax groups of 128 threads (one query row per thread);
-//              group g takes the key tiles whose global index is = g (mod 2),
+//              group g takes the item's key tiles t = g (mod 2),
 //              keeps its own running max, sum and O accumulator, and the two
 //              partial results are merged per item
 //   warp 8     TMEM allocation; issues the score MMAs (AC and position slots)
@@ -105,7 +106,8 @@ constexpr uint32_t COL_AC = 128;    // + 64 * group
 constexpr uint32_t COL_RING = 256;  // + 64 * slot
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0);  // K-major B (K, R)
+constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0);    // K-major B: one key tile
+constexpr uint32_t IDESC_N128 = idesc_bf16_f32(128, 128, 0);  // K-major B: a K or R box
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DH, 1);   // MN-major B (V)
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
@@ -163,6 +165,11 @@ __device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
     it.rbase = p.L - it.i0 - tc::BM;                // R row of slot 0
     return true;
 }
+
+// Position slots an item occupies in the ring: slots 0 .. ntiles+1 are read,
+// rounded up to an even count so that every item starts on an even global
+// slot and each score MMA writes two adjacent slots (one R box of 128 rows).
+__device__ __forceinline__ int slots_of(int ntiles) { return 2 * (((ntiles + 1) >> 1) + 1); }
 
 // Bounded wait that ignores the abort flag: used to drain in-flight copies and
 // MMAs before the CTA releases its shared and tensor memory.
@@ -306,8 +313,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         bool ok = true;
         Item cur;
         int it_g = 0;      // tiles this group has processed (all items)
-        int tbase = 0;     // global index of the current item's first tile
-        int gbase = 0;     // global position-slot counter of the item's slot 0
+        int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
         if (item_of(p, 0, cur)) {
             uint4 qn[8];
             load_q(cur, qn);
@@ -333,7 +339,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             float m_run = -INFINITY;  // running max (log2 domain), may lag the true max by < 8
             float l_run = 0.f;
             int seen = 0;             // this group's tiles in this item
-            for (int t = (grp - tbase) & 1; t < cur.ntiles; t += 2) {
+            for (int t = grp; t < cur.ntiles; t += 2) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&sh->s_full[grp], it_g & 1,
                                                        kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
@@ -522,23 +528,24 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             // a failed wait anywhere sets the abort flag: both groups leave
             // together, so neither waits alone at the named barrier
             if (*abort) ok = false;
-            tbase += cur.ntiles;
-            gbase += cur.ntiles + 2;
+            gbase += slots_of(cur.ntiles);
         }
         tc_fence_before();
     } else if (warp == 8) {
         // ------------------------------------------------ score MMA issuer
-        // Issues S(0), S(1), ... in order; the P V MMAs go out from warp 10,
-        // so the two chains run on different SM sub-partitions.  The whole
-        // warp waits (bounded mbarrier waits, voted) and one elected lane
-        // issues the MMAs and commits.
+        // Key tiles go out in pairs (2p, 2p+1) of one item, one per softmax
+        // group (group g takes the item's tiles t = g mod 2): one N=128 MMA
+        // chain computes both tiles' AC into AC0|AC1 against the 128-key K box
+        // of stage p, and one N=128 chain computes the two new position slots
+        // 2p+2, 2p+3 (slots 0-3 for the first pair) against one R box.  The
+        // pages' relative shift needs slots t, t+1, t+2 for tile t.
         //
-        // S(T) overwrites AC[T&1], last read by tile T-2, and one position
-        // slot (three for the first tile of an item) whose earlier readers are
-        // tiles <= T-2 (<= T-1 for the first tile of an item).  s_free of each
-        // group completes once per tile of that group, in order; this warp
-        // observes those completions in order and never falls two phases
-        // behind: a group's next completion needs an S not yet issued.
+        // Pair p overwrites both AC buffers and one slot pair (for p = 0 both)
+        // whose earlier readers are tiles already issued, so it waits until
+        // every issued tile has read its scores.  s_free of each group
+        // completes once per tile of that group, in order, and cannot run two
+        // phases ahead of these waits: its next phase needs the next pair.
+        // The whole warp waits (bounded, voted); one elected lane issues.
         const uint32_t leader = elect_one();
         {
             bool ok = true;
@@ -547,101 +554,82 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, kDevTimeoutMma, abort, p.status));
                 return ok;
             };
-            int seen0 = 0, seen1 = 0;  // s_free completions observed, per group
-            auto s_free_of = [&](int T) {  // tile T (global) has read its scores
-                if (T < 0) return;
-                const int n = T >> 1;
-                if (T & 1) {
-                    for (; ok && seen1 <= n; ++seen1) wait(&sh->s_free[1], seen1 & 1);
-                } else {
-                    for (; ok && seen0 <= n; ++seen0) wait(&sh->s_free[0], seen0 & 1);
-                }
-            };
             // Shared-memory descriptors of every operand buffer, precomputed;
             // a k-step of 16 elements (32 bytes) adds 2 to the address field
-            // (16-byte units), a V k-step of 16 rows adds 128.
+            // (16-byte units).
             const uint64_t dQ0 = smem_desc_sw128(s_base + OFF_Q, 16, 1024);
             const uint64_t dK0 = smem_desc_sw128(s_base + OFF_KV, 16, 1024);
             const uint64_t dR0 = smem_desc_sw128(s_base + OFF_R, 16, 1024);
-            constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
-            // S cursor
+            constexpr uint32_t U_Q = SZ_Q >> 4, U_BOX = SZ_BOX >> 4;
+            int seen0 = 0, seen1 = 0;  // s_free completions observed, per group
+            int iss0 = 0, iss1 = 0;    // tiles issued, per group
+            int kv_s = 0, r_s = 0;     // K/V stage and R box counters at the item start
+            int gbase = 0;             // global position-slot counter at the item start
             Item is;
-            bool s_valid = item_of(p, 0, is);
-            int ks = 0, ts = 0, Ts = 0;  // item, local tile, global tile of the next S
-            int kv_s = 0;                // K/V stage counter at the item's first stage
-            int r_s = 0, r_rel = 0;      // R box counter at the item's first box; released boxes
-            int gslot = 0;               // global position-slot counter
-
-            auto issue_s = [&]() {
-                const int stage = kv_s + (ts >> 1);
-                const int nrb = (is.ntiles + 3) >> 1;
-                const int nslots = (ts == 0) ? 3 : 1;
-                if (ts == 0) {
-                    wait(&sh->q_ready, ks & 1);
-                    s_free_of(Ts - 1);
-                }
-                s_free_of(Ts - 2);
-                s_free_of(Ts - 3);
-                // a K/V stage and an R box are waited for by their first reader:
-                // S(ts) reads slots 0..2 (boxes 0, 1) for ts = 0, else slot ts+2
-                // in box (ts+2)/2, which is new when ts is even
-                if (!(ts & 1)) wait(&sh->kv_full[stage % KV_STAGES], (stage / KV_STAGES) & 1);
-                if (ts == 0) {
-                    wait(&sh->r_full[r_s % R_STAGES], (r_s / R_STAGES) & 1);
-                    wait(&sh->r_full[(r_s + 1) % R_STAGES], ((r_s + 1) / R_STAGES) & 1);
-                } else if (!(ts & 1)) {
-                    const int rbox = r_s + ((ts + 2) >> 1);
-                    wait(&sh->r_full[rbox % R_STAGES], (rbox / R_STAGES) & 1);
-                }
-                if (!ok) return;
-                tc_fence_after();
+            for (int ks = 0; ok && item_of(p, ks, is); ++ks) {
+                const int npairs = (is.ntiles + 1) >> 1;
+                const int nrb = npairs + 1;  // R boxes of the item (slots 0 .. 2*npairs+1)
+                wait(&sh->q_ready, ks & 1);
                 const uint64_t a_qu = dQ0 + (ks & 1) * 2 * U_Q;
                 const uint64_t a_qv = a_qu + U_Q;
-                const uint64_t b_k = dK0 + (stage % KV_STAGES) * 2 * U_BOX + (ts & 1) * U_T;
-                const uint32_t d_ac = tmem + COL_AC + 64 * (Ts & 1);
-#pragma unroll
-                for (int k = 0; k < DH / 16; ++k)
-                    mma_ss_elect(d_ac, a_qu + 2 * k, b_k + 2 * k, IDESC_N64, k > 0, leader);
-                // item-local slot g lives at R box r_s + g/2, half g&1
-                for (int j = 0; j < nslots; ++j) {
-                    const int g = (ts == 0) ? j : ts + 2;
-                    const int box = r_s + (g >> 1);
-                    const uint64_t b_r = dR0 + (box % R_STAGES) * U_BOX + (g & 1) * U_T;
-                    const uint32_t d_r = tmem + COL_RING + 64 * ((gslot + j) & (RING - 1));
+                int r_rel = 0;  // R boxes of this item released
+                for (int pp = 0; ok && pp < npairs; ++pp) {
+                    for (; ok && seen0 < iss0; ++seen0) wait(&sh->s_free[0], seen0 & 1);
+                    for (; ok && seen1 < iss1; ++seen1) wait(&sh->s_free[1], seen1 & 1);
+                    const int stage = kv_s + pp;
+                    wait(&sh->kv_full[stage % KV_STAGES], (stage / KV_STAGES) & 1);
+                    if (pp == 0) {
+                        wait(&sh->r_full[r_s % R_STAGES], (r_s / R_STAGES) & 1);
+                        wait(&sh->r_full[(r_s + 1) % R_STAGES], ((r_s + 1) / R_STAGES) & 1);
+                    } else {
+                        const int rb = r_s + pp + 1;
+                        wait(&sh->r_full[rb % R_STAGES], (rb / R_STAGES) & 1);
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    const bool two = 2 * pp + 1 < is.ntiles;
+                    // AC of tiles 2p (AC0) and 2p+1 (AC1): the stage's K box
+                    const uint64_t b_k = dK0 + (stage % KV_STAGES) * 2 * U_BOX;
+                    const uint32_t idesc_ac = two ? IDESC_N128 : IDESC_N64;
 #pragma unroll
                     for (int k = 0; k < DH / 16; ++k)
-                        mma_ss_elect(d_r, a_qv + 2 * k, b_r + 2 * k, IDESC_N64, k > 0, leader);
+                        mma_ss_elect(tmem + COL_AC, a_qu + 2 * k, b_k + 2 * k, idesc_ac, k > 0, leader);
+                    // position slots: R box b holds item slots 2b, 2b+1, which
+                    // live in ring slot pair ((gbase / 2) + b) & 1
+                    const int b_first = (pp == 0) ? 0 : pp + 1;
+                    for (int b = b_first; b <= pp + 1; ++b) {
+                        const uint64_t b_r = dR0 + ((r_s + b) % R_STAGES) * U_BOX;
+                        const uint32_t d_r = tmem + COL_RING + 128 * (((gbase >> 1) + b) & 1);
+#pragma unroll
+                        for (int k = 0; k < DH / 16; ++k)
+                            mma_ss_elect(d_r, a_qv + 2 * k, b_r + 2 * k, IDESC_N128, k > 0, leader);
+                    }
+                    if (leader) {
+                        if (!(p.inject == 1 && ks == 0 && pp == 0)) mma_commit(&sh->s_full[0]);
+                        if (two) mma_commit(&sh->s_full[1]);
+                        // R boxes 0 .. pp+1 are not read again
+                        for (int b = r_rel; b <= pp + 1 && b < nrb; ++b)
+                            mma_commit(&sh->r_empty[(r_s + b) % R_STAGES]);
+                    }
+                    r_rel = min(pp + 2, nrb);
+                    ++iss0;
+                    if (two) ++iss1;
                 }
-                if (leader && !(p.inject == 1 && Ts == 0)) mma_commit(&sh->s_full[Ts & 1]);
-                // release the R boxes no later S of this item reads:
-                // box v is last read by S(min(max(2v-1, 0), ntiles-1))
-                while (r_rel < nrb && min(max(2 * r_rel - 1, 0), is.ntiles - 1) <= ts) {
-                    if (leader) mma_commit(&sh->r_empty[(r_s + r_rel) % R_STAGES]);
-                    ++r_rel;
-                }
-                gslot += nslots;
-                ++Ts;
-                if (++ts == is.ntiles) {
-                    kv_s += (is.ntiles + 1) >> 1;
-                    r_s += nrb;
-                    r_rel = 0;
-                    ts = 0;
-                    ++ks;
-                    s_valid = item_of(p, ks, is);
-                }
-            };
-
-            while (ok && s_valid) issue_s();
+                kv_s += npairs;
+                r_s += nrb;
+                gbase += slots_of(is.ntiles);
+            }
             if (leader) mma_commit(&sh->drain);
             drain_wait(&sh->drain, 0, p.status);
         }
         __syncwarp();
     } else if (warp == 10) {
         // ------------------------------------------------- P V MMA issuer
-        // PV(0), PV(1), ... in order: PV(T) waits for tile T's P; the first
-        // P V of an item also for the merge of the previous item to have
-        // read O.  p_full of a group cannot complete twice before PV(T) is
-        // issued: the group's next P waits for pv_done of this one.
+        // The tiles of each item in order; tile t belongs to group t mod 2.
+        // PV(t) waits for the tile's P; the first P V of an item also for the
+        // merge of the previous item to have read O.  p_full of a group cannot
+        // complete twice before its P V is issued: the group's next P waits
+        // for pv_done of this one.
         const uint32_t leader = elect_one();
         {
             bool ok = true;
@@ -655,10 +643,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
             Item ip;
             bool p_valid = item_of(p, 0, ip);
-            int kp = 0, tp = 0, Tp = 0, kv_p = 0;
+            int kp = 0, tp = 0, kv_p = 0;
+            int pc0 = 0, pc1 = 0;  // P tiles consumed, per group
             while (ok && p_valid) {
-                const int g = Tp & 1;
-                wait(&sh->p_full[g], (Tp >> 1) & 1);
+                const int g = tp & 1;
+                wait(&sh->p_full[g], (g ? pc1 : pc0) & 1);
                 if (tp == 0 && kp > 0) wait(&sh->o_free, (kp - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
@@ -677,7 +666,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     if ((tp & 1) || tp == ip.ntiles - 1) mma_commit(&sh->kv_empty[stage % KV_STAGES]);
                     if (tp + 1 == ip.ntiles) mma_commit(&sh->o_done);
                 }
-                ++Tp;
+                if (g) ++pc1; else ++pc0;
                 if (++tp == ip.ntiles) {
                     kv_p += (ip.ntiles + 1) >> 1;
                     tp = 0;
