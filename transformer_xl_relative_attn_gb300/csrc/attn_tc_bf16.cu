@@ -96,8 +96,7 @@ constexpr uint32_t OFF_Q = 0;               // buffer b: (q+u)c at +32K*b, (q+v)
 constexpr uint32_t OFF_P = OFF_Q + 4 * SZ_Q;          // P of group g at +16K*g; merge exchange
 constexpr uint32_t OFF_KV = OFF_P + 2 * SZ_Q;         // stage s: K box, V box
 constexpr uint32_t OFF_R = OFF_KV + KV_STAGES * 2 * SZ_BOX;
-constexpr uint32_t OFF_ML = OFF_R + R_STAGES * SZ_BOX;  // merge exchange of (m, l)
-constexpr uint32_t OFF_BAR = OFF_ML + BM * 8;
+constexpr uint32_t OFF_BAR = OFF_R + R_STAGES * SZ_BOX;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one sm_103a CTA");
 
@@ -456,78 +455,65 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (ok)
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&sh->o_done, k & 1, kDevTimeoutSoftmax, abort, p.status));
-            // group 1's partial (m, l, O) goes through shared memory: O into the
-            // idle P buffers (16-byte chunks swizzled by row), m and l apart.
-            // O is streamed in two 32-column halves to keep registers low.
-            float* ml = reinterpret_cast<float*>(smem + OFF_ML);
-            if (ok && grp == 1) {
-                tc_fence_after();
-                ml[2 * ii] = seen ? m_run : -INFINITY;
-                ml[2 * ii + 1] = seen ? l_run : 0.f;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t o32[32];
-                    tmem_ld32(tmem + lane_off + COL_O + 64 + 32 * hf, o32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t a = s_base + OFF_P + ii * 256 + (((8 * hf + c) ^ (ii & 15)) << 4);
-                        // a group without a tile in this item holds stale O: send zeros
-                        if (seen)
-                            st_shared_v4(a, o32[4 * c], o32[4 * c + 1], o32[4 * c + 2], o32[4 * c + 3]);
-                        else
-                            st_shared_v4(a, 0u, 0u, 0u, 0u);
-                    }
-                }
-                tc_fence_before();
-                warp_arrive(&sh->o_free);
+            // Each group finishes half of the output columns (group g: 32g ..
+            // 32g+31) from both accumulators, which its warps read straight from
+            // TMEM; only the per-row (m, l) cross between the groups, through
+            // the other group's P buffer (idle until that group's next tile, so
+            // one barrier suffices).  l = -1 marks a group without a tile in
+            // this item: its O is stale and is not read.  The second barrier
+            // keeps every P write of the next tiles behind all (m, l) reads.
+            {
+                float* ml_out = reinterpret_cast<float*>(smem + OFF_P + (grp ^ 1) * SZ_Q);
+                ml_out[2 * ii] = seen ? m_run : -INFINITY;
+                ml_out[2 * ii + 1] = seen ? l_run : -1.f;
             }
-            // both groups reach this barrier on every path (ok is warp-uniform)
+            // both groups reach these barriers on every path (ok is warp-uniform)
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (ok && grp == 0) {
-                tc_fence_after();
-                const float m1 = ml[2 * ii], l1 = ml[2 * ii + 1];
-                const float m = fmaxf(m_run, m1);
-                const float f0 = ex2(m_run - m), f1 = ex2(m1 - m);
-                const float inv = 1.f / (l_run * f0 + l1 * f1);
-                const float a0 = seen ? f0 * inv : 0.f, a1 = f1 * inv;
-                uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t o32[32];
-                    tmem_ld32(tmem + lane_off + COL_O + 32 * hf, o32);
-                    tmem_wait_ld();
-                    if (!seen) {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) o32[x] = 0u;  // stale O contributes zero
-                    }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float x0[4], x1[4];
-                        const int ch = 8 * hf + 2 * c;
-                        ld_shared_v4(s_base + OFF_P + ii * 256 + ((ch ^ (ii & 15)) << 4), x0);
-                        ld_shared_v4(s_base + OFF_P + ii * 256 + (((ch + 1) ^ (ii & 15)) << 4), x1);
-                        const uint32_t* mine = &o32[8 * c];
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(mine[0]) * a0 + x0[0] * a1,
-                                          __uint_as_float(mine[1]) * a0 + x0[1] * a1);
-                        w.y = pack_bf16x2(__uint_as_float(mine[2]) * a0 + x0[2] * a1,
-                                          __uint_as_float(mine[3]) * a0 + x0[3] * a1);
-                        w.z = pack_bf16x2(__uint_as_float(mine[4]) * a0 + x1[0] * a1,
-                                          __uint_as_float(mine[5]) * a0 + x1[1] * a1);
-                        w.w = pack_bf16x2(__uint_as_float(mine[6]) * a0 + x1[2] * a1,
-                                          __uint_as_float(mine[7]) * a0 + x1[3] * a1);
-                        if (i < p.L) orow[4 * hf + c] = w;
-                    }
-                }
-                tc_fence_before();
-                warp_arrive(&sh->o_free);
+            float mo, lo;
+            {
+                const float* ml_in = reinterpret_cast<const float*>(smem + OFF_P + grp * SZ_Q);
+                mo = ml_in[2 * ii];
+                lo = ml_in[2 * ii + 1];
             }
-            // the exchange buffers are the P buffers: read before anyone reuses them
             asm volatile("bar.sync 1, 256;" ::: "memory");
             // a failed wait anywhere sets the abort flag: both groups leave
-            // together, so neither waits alone at the named barrier
+            // together, so neither waits alone at a later named barrier
             if (*abort) ok = false;
+            if (ok) {
+                tc_fence_after();
+                // (m, l) of group 0 and group 1
+                const float m0 = grp ? mo : (seen ? m_run : -INFINITY);
+                const float l0 = grp ? lo : (seen ? l_run : -1.f);
+                const float m1 = grp ? (seen ? m_run : -INFINITY) : mo;
+                const float l1 = grp ? (seen ? l_run : -1.f) : lo;
+                const bool has0 = l0 >= 0.f, has1 = l1 >= 0.f;
+                const float m = fmaxf(m0, m1);
+                const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
+                const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
+                const float a0 = f0 * inv, a1 = f1 * inv;
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tmem + lane_off + COL_O + 32 * grp, o0);
+                tmem_ld32(tmem + lane_off + COL_O + 64 + 32 * grp, o1);
+                tmem_wait_ld();
+                tc_fence_before();
+                warp_arrive(&sh->o_free);
+                uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH) + 4 * grp;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
+                        y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
+                    }
+                    uint4 w;
+                    w.x = pack_bf16x2(y[0], y[1]);
+                    w.y = pack_bf16x2(y[2], y[3]);
+                    w.z = pack_bf16x2(y[4], y[5]);
+                    w.w = pack_bf16x2(y[6], y[7]);
+                    if (i < p.L) orow[c] = w;
+                }
+            }
             gbase += slots_of(cur.ntiles);
         }
         tc_fence_before();
