@@ -51,7 +51,8 @@
 // streams.
 //
 // TMEM columns: O0 0-63, O1 64-127, AC0 128-191, AC1 192-255, position ring
-// 256-511.  Shared memory: (q+u)c,(q+v)c x2, P x2, K/V ring, R ring.
+// 256-511.  Shared memory: (q+u)c,(q+v)c x2 (each first filled with the raw q
+// tile by TMA, then rewritten in place), P x2, K/V ring, R ring.
 //
 // Ordering facts relied on: tcgen05.mma operations from one thread execute in
 // issue order, and a tcgen05.commit arrives only when every MMA issued before
@@ -131,6 +132,7 @@ struct TcShared {
     uint64_t r_full[tc::R_STAGES];
     uint64_t r_empty[tc::R_STAGES];
     uint64_t q_ready;     // (q+u)c and (q+v)c of the next item are in shared memory
+    uint64_t q_full[2];   // the raw q tile of the next item landed in group g's slot
     uint64_t s_full[2];   // scores of the group's next tile are in TMEM
     uint64_t s_free[2];   // the group has read them into registers
     uint64_t p_full[2];   // the group's P tile is in shared memory
@@ -218,8 +220,9 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
 }
 
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
-attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmR, const TcParams p) {
+attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
+                    const TcParams p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -247,6 +250,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         // softmax-side barriers count warps: one elected lane per warp arrives
         mbar_init(&sh->q_ready, 8);
         for (int g = 0; g < 2; ++g) {
+            mbar_init(&sh->q_full[g], 1);
             mbar_init(&sh->s_full[g], 1);
             mbar_init(&sh->s_free[g], 4);
             mbar_init(&sh->p_full[g], 4);
@@ -259,6 +263,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         fence_mbar_init();
     }
     if (warp == 9 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmR);
@@ -279,16 +284,38 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const uint32_t p_tile = s_base + OFF_P + grp * SZ_Q;
         const float qscale = p.scale_log2;
 
-        // (q+u)c (group 0) or (q+v)c (group 1) of an item, rounded to bf16,
-        // as 128-byte swizzled rows (chunk c of row ii at chunk c ^ (ii & 7)).
-        auto write_q = [&](const Item& it, int kbuf, const uint4 (&q4)[8]) {
+        // (q+u)c (group 0) or (q+v)c (group 1) of an item, rounded to bf16, in
+        // the group's slot of Q buffer kbuf.  One thread of the group loads the
+        // raw q tile there by TMA (128B swizzle: chunk c of row ii at chunk
+        // c ^ (ii & 7); rows past L arrive as zeros); later each thread turns
+        // its own row into (q+bias)c in place.  The buffer is free when the
+        // load is issued: its last readers were the score MMAs of the item
+        // before the current one, which completed before the current item's
+        // first scores.
+        bool ok = true;
+        auto issue_q = [&](const Item& it, int kbuf) {
+            if (ii == 0) {
+                mbar_expect_tx(&sh->q_full[grp], SZ_Q);
+                tma_load_3d(smem + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q, &tmQ, &sh->q_full[grp], 0,
+                            it.i0, it.bh);
+            }
+            const void* brow = (grp == 0 ? p.ub : p.vb) + (size_t)it.h * DH;
+            if ((ii & 31) == 0) asm volatile("prefetch.global.L1 [%0];" ::"l"(brow));
+        };
+        auto write_q = [&](const Item& it, int kbuf, int kq) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full[grp], kq & 1, kDevTimeoutSoftmax,
+                                                   abort, p.status));
+            if (!ok) return;
             const uint4* brow =
                 reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)it.h * DH);
-            const uint32_t dst = s_base + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q + ii * 128;
+            const uint32_t row = s_base + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q + ii * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
-                const uint4 b4 = brow[ch];
-                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&q4[ch]);
+                const uint32_t a = row + ((ch ^ (ii & 7)) << 4);
+                float raw[4];
+                ld_shared_v4(a, raw);
+                const uint4 b4 = __ldg(brow + ch);
+                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
                 const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b4);
                 uint32_t w[4];
 #pragma unroll
@@ -297,41 +324,31 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const float2 bf = __bfloat1622float2(b2[e]);
                     w[e] = pack_bf16x2((qf.x + bf.x) * qscale, (qf.y + bf.y) * qscale);
                 }
-                st_shared_v4(dst + ((ch ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
+                st_shared_v4(a, w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             warp_arrive(&sh->q_ready);
         };
-        auto load_q = [&](const Item& it, uint4 (&q4)[8]) {
-            const int i = it.i0 + ii;
-            const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)it.bh * p.L + i) * DH);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) q4[ch] = (i < p.L) ? qrow[ch] : make_uint4(0, 0, 0, 0);
-        };
 
-        bool ok = true;
         Item cur;
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
-        if (item_of(p, 0, cur)) {
-            uint4 qn[8];
-            load_q(cur, qn);
-            write_q(cur, 0, qn);
-        }
         for (int k = 0; ok && item_of(p, k, cur); ++k) {
+            // the first item's q tile; a failed wait leaves ok false, and the
+            // group still reaches this item's merge barriers below
+            if (k == 0) {
+                issue_q(cur, 0);
+                write_q(cur, 0, 0);
+            }
             Item nxt;
             const bool has_next = item_of(p, k + 1, nxt);
-            // the next item's q row: warmed into L2 now, read when it is
-            // written (after this group's first tile, when registers are free)
-            if (has_next && nxt.i0 + ii < p.L) {
-                const void* qrow = p.q + ((size_t)nxt.bh * p.L + nxt.i0 + ii) * DH;
-                asm volatile("prefetch.L2 [%0];" ::"l"(qrow));
-            }
-            bool next_written = !has_next;
+            // the next item's q tile: loaded once this group holds the current
+            // item's first scores, turned into (q+bias)c after that tile
+            bool next_issued = !has_next, next_written = !has_next;
             auto write_next_q = [&]() {
-                uint4 qn[8];
-                load_q(nxt, qn);
-                write_q(nxt, (k + 1) & 1, qn);
+                if (!next_issued) issue_q(nxt, (k + 1) & 1);
+                next_issued = true;
+                write_q(nxt, (k + 1) & 1, k + 1);
                 next_written = true;
             };
             const int i = cur.i0 + ii;
@@ -343,6 +360,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                                                        kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
                 tc_fence_after();
+                if (!next_issued) {
+                    issue_q(nxt, (k + 1) & 1);
+                    next_issued = true;
+                }
                 const int j0 = t * BN;
                 const bool need_mask = (j0 + BN - 1) > (p.M + cur.i0);
                 const int jlim = p.M + i - j0;  // keys jj > jlim are masked
@@ -780,7 +801,14 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
         attr_set = true;
     }
     const int K = M + L;
-    CUtensorMap mK, mV, mR;
+    CUtensorMap mQ, mK, mV, mR;
+    {
+        // q tile of an item: 128 rows of one (b, h); rows past L read as zeros
+        cuuint64_t dims[3] = {(cuuint64_t)DH, (cuuint64_t)L, (cuuint64_t)B * H};
+        cuuint64_t strides[2] = {(cuuint64_t)DH * 2, (cuuint64_t)L * DH * 2};
+        cuuint32_t box[3] = {DH, BM, 1};
+        if (!encode_bf16(&mQ, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
     {
         cuuint64_t dims[3] = {(cuuint64_t)DH, (cuuint64_t)K, (cuuint64_t)B * H};
         cuuint64_t strides[2] = {(cuuint64_t)DH * 2, (cuuint64_t)K * DH * 2};
@@ -811,7 +839,7 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.inject = inject;
     p.status = status;
     const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
-    attn_tc_bf16_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mK, mV, mR, p);
+    attn_tc_bf16_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
     return cudaGetLastError();
 }
 
