@@ -84,9 +84,13 @@ constexpr int RING = 4;        // position slots held in TMEM
 #ifndef TXL_PREFETCH
 #define TXL_PREFETCH 2
 #endif
+#ifndef TXL_FMA_STAGES
+#define TXL_FMA_STAGES 1
+#endif
 constexpr int KV_STAGES = TXL_KV_STAGES;  // K/V ring: each stage holds two key tiles
 constexpr int R_STAGES = TXL_R_STAGES;    // R ring: each box holds two position slots
 constexpr int PREFETCH = TXL_PREFETCH;    // K/V stages warmed into L2 ahead of their load
+constexpr int FMA_STAGES = TXL_FMA_STAGES;  // relative-shift stages done on the FMA pipe
 static_assert(KV_STAGES >= 2 && R_STAGES >= 2, "the MMA order needs two stages of each ring");
 constexpr int NTHREADS = 384;
 
@@ -394,13 +398,23 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         win[x] = __uint_as_float(w0[x]);
                         win[32 + x] = __uint_as_float(w1[x]);
                     }
-                    // per-row shift by o = 31 - lane: win[x] <- win[x + o]
+                    // per-row shift by o = 31 - lane: win[x] <- win[x + o], as a
+                    // barrel of selects.  The last FMA_STAGES stages run on the FMA pipe
+                    // (a*t + b*(1-t) with t in {0, 1} is exact for finite a, b),
+                    // which is otherwise idle while the selects fill the ALU.
                     const int o = 31 - lane;
 #pragma unroll
-                    for (int sb = 16; sb >= 1; sb >>= 1) {
+                    for (int sb = 16; sb >= (1 << FMA_STAGES); sb >>= 1) {
                         const bool take = (o & sb) != 0;
 #pragma unroll
                         for (int x = 0; x < 32 + sb - 1; ++x) win[x] = take ? win[x + sb] : win[x];
+                    }
+#pragma unroll
+                    for (int sb = (1 << FMA_STAGES) >> 1; sb >= 1; sb >>= 1) {
+                        const float tk = (o & sb) ? 1.f : 0.f, nt = 1.f - tk;
+#pragma unroll
+                        for (int x = 0; x < 32 + sb - 1; ++x)
+                            win[x] = __fmaf_rn(win[x + sb], tk, __fmul_rn(win[x], nt));
                     }
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
