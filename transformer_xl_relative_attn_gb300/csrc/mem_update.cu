@@ -5,41 +5,56 @@
 // of [M_tau; H_tau]).  With L >= M every new row comes from h.  With L < M
 // row r takes mem[r+L] while r+L < M, else h[r+L-M].
 //
-// In place without a workspace: rows r congruent to c modulo L form a chain
-// c, c+L, c+2L, ...; row r reads row r+L, which belongs to the same chain, so
-// chains are disjoint.  One thread walks one chain (for one 16-byte column of
-// one batch row) in ascending order, loading a block of up to kChain sources
-// into registers before it stores them, so every source is read before the
-// store that overwrites it and the loads of a block are all in flight at once.
-// Adjacent threads own adjacent 16-byte columns of the same row: every warp
-// access is a contiguous 512-byte segment.
+// In place without a workspace (details at each kernel).  Adjacent threads
+// own adjacent vectors of a row, so every warp access is contiguous.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace txl {
 
-constexpr int kChain = 8;
+constexpr int kChain = 8;   // sources of one chain in flight per thread
+constexpr int kCopyUnroll = 4;  // vectors in flight per thread in the plain copy
 
-template <typename V>
-__global__ void __launch_bounds__(256) tail_m_kernel(V* __restrict__ mem, const V* __restrict__ hid,
-                                                     int B, int L, int M, int rowv) {
-    // rowv = row length in units of V; chains = min(L, M)
-    const int chains = L < M ? L : M;
-    const long long total = (long long)B * chains * rowv;
-    long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= total) return;
-    const int col = (int)(t % rowv);
-    const long long cb = t / rowv;
-    const int c = (int)(cb % chains);
-    const int b = (int)(cb / chains);
-    V* mrow = mem + (size_t)b * M * rowv + col;
-    const V* hrow = hid + (size_t)b * L * rowv + col;
-    if (L >= M) {
-        // one row per chain: new[c] = h[L - M + c]
-        mrow[(size_t)c * rowv] = hrow[(size_t)(L - M + c) * rowv];
-        return;
+// L >= M: every new row comes from h, and memory row r of batch b takes h row
+// L-M+r, so the roll is one contiguous copy of M rows per batch row: element
+// e of the flattened memory [B, M, row] is element (e / seg) * hstride + hoff
+// + e % seg of h.  Each thread moves kCopyUnroll vectors spaced one block
+// apart (coalesced per warp), all loads issued before the stores.
+template <typename V, typename I>
+__global__ void __launch_bounds__(256) tail_copy_kernel(V* __restrict__ mem, const V* __restrict__ hid,
+                                                        I total, I seg, I hstride, I hoff) {
+    const I base = (I)blockIdx.x * (256 * kCopyUnroll) + threadIdx.x;
+    V buf[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const I e = base + (I)u * 256;
+        if (e < total) {
+            const I b = e / seg;
+            buf[u] = hid[b * hstride + hoff + (e - b * seg)];
+        }
     }
-    // chain rows r = c, c+L, ... < M
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const I e = base + (I)u * 256;
+        if (e < total) mem[e] = buf[u];
+    }
+}
+
+// L < M: rows r congruent to c modulo L form a chain c, c+L, c+2L, ...; row
+// r reads row r+L of the same chain, so chains are disjoint and one thread
+// walks one chain (for one vector column of one batch row) upwards, loading a
+// block of kChain sources before storing them.
+template <typename V, typename I>
+__global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, const V* __restrict__ hid,
+                                                         int L, int M, I rowv, I total) {
+    const I t = (I)blockIdx.x * 256 + threadIdx.x;
+    if (t >= total) return;
+    const I col = t % rowv;
+    const I cb = t / rowv;
+    const int c = (int)(cb % (I)L);
+    const I b = cb / (I)L;
+    V* mrow = mem + b * (I)M * rowv + col;
+    const V* hrow = hid + b * (I)L * rowv + col;
     for (int r0 = c; r0 < M; r0 += kChain * L) {
         V buf[kChain];
 #pragma unroll
@@ -47,30 +62,49 @@ __global__ void __launch_bounds__(256) tail_m_kernel(V* __restrict__ mem, const 
             const int r = r0 + s * L;
             if (r < M) {
                 const int src = r + L;
-                buf[s] = src < M ? mrow[(size_t)src * rowv] : hrow[(size_t)(src - M) * rowv];
+                buf[s] = src < M ? mrow[(I)src * rowv] : hrow[(I)(src - M) * rowv];
             }
         }
 #pragma unroll
         for (int s = 0; s < kChain; ++s) {
             const int r = r0 + s * L;
-            if (r < M) mrow[(size_t)r * rowv] = buf[s];
+            if (r < M) mrow[(I)r * rowv] = buf[s];
         }
     }
 }
 
-// Launches the roll with the widest unit the alignment allows.
+// Launches the roll with the widest vector the alignment allows and 32-bit
+// index arithmetic whenever the element counts fit.
 cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int M, size_t row_bytes,
                           cudaStream_t stream) {
-    const int chains = L < M ? L : M;
     auto go = [&](auto tag) -> cudaError_t {
         using V = decltype(tag);
-        const int rowv = (int)(row_bytes / sizeof(V));
-        const long long total = (long long)B * chains * rowv;
-        const int threads = 256;
-        const long long blocks = (total + threads - 1) / threads;
-        if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-        tail_m_kernel<V><<<(unsigned)blocks, threads, 0, stream>>>(
-            static_cast<V*>(mem), static_cast<const V*>(hid), B, L, M, rowv);
+        const long long rowv = (long long)(row_bytes / sizeof(V));
+        if (L >= M) {
+            const long long seg = (long long)M * rowv, total = (long long)B * seg;
+            const long long hsz = (long long)B * L * rowv;
+            const long long blocks = (total + 256 * kCopyUnroll - 1) / (256 * kCopyUnroll);
+            if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+            if (hsz < 0x7FFFFFFFll - 256 * kCopyUnroll)
+                tail_copy_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
+                    static_cast<V*>(mem), static_cast<const V*>(hid), (int)total, (int)seg,
+                    (int)(L * rowv), (int)((L - M) * rowv));
+            else
+                tail_copy_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
+                    static_cast<V*>(mem), static_cast<const V*>(hid), total, seg, L * rowv,
+                    (L - M) * rowv);
+        } else {
+            const long long total = (long long)B * L * rowv;
+            const long long msz = (long long)B * M * rowv;
+            const long long blocks = (total + 255) / 256;
+            if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+            if (msz < 0x7FFFFFFFll - 256)
+                tail_chain_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
+                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, (int)rowv, (int)total);
+            else
+                tail_chain_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
+                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, rowv, total);
+        }
         return cudaGetLastError();
     };
     const uintptr_t a = reinterpret_cast<uintptr_t>(mem) | reinterpret_cast<uintptr_t>(hid);
