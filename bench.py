@@ -226,14 +226,37 @@ def run_ours(args, wl: W.Workload):
     ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in calls]
     ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in calls]
 
+    side = torch.cuda.Stream(device=dev)
+
     def step(timed_events: bool):
+        # Attention calls in order on the current stream; each Tail_M roll on a
+        # side stream, after the point where its layer's inputs were projected
+        # (just before that layer's attention) and before the next segment's
+        # layer of the same memory starts (the projection reads the rolled
+        # memory).  The rolls (HBM-bound) thus overlap later attention calls
+        # (tensor/ALU-bound), with every data dependency of the segment
+        # recurrence kept.
+        cur = torch.cuda.current_stream()
+        rolled = {}
         for c, ea, eb in zip(calls, ev_a, ev_b):
+            n = c["n"]
+            if n in rolled:
+                cur.wait_event(rolled[n])
+            inputs_ready = torch.cuda.Event()
+            inputs_ready.record(cur)
             if timed_events:
                 ea.record()
-            txl.attn_fwd(c["q"], c["k"], c["v"], rks[c["n"]], u, vb, wl.scale, out=c["out"])
+            txl.attn_fwd(c["q"], c["k"], c["v"], rks[n], u, vb, wl.scale, out=c["out"])
             if timed_events:
                 eb.record()
-            txl.mem_update(mems[c["n"]], c["h"])
+            side.wait_event(inputs_ready)
+            with torch.cuda.stream(side):
+                txl.mem_update(mems[n], c["h"], stream=side)
+            rolled[n] = torch.cuda.Event()
+            rolled[n].record(side)
+        joined = torch.cuda.Event()
+        joined.record(side)
+        cur.wait_event(joined)
 
     # capture one step as a CUDA graph (warm the launch path first)
     with torch.cuda.stream(stream):

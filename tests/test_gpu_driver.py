@@ -19,12 +19,12 @@ def bits(t):
     return t.contiguous().cpu().view(torch.int16).numpy()
 
 
-def make_driver(record):
+def make_driver(record, overlap=False):
     dev = torch.device("cuda")
     params = W.make_params(WL)
     mems = [m.to(dev, WL.torch_dtype) for m in W.initial_memories(WL)]
     rks = [W.project_r(lw, WL.M, WL.L, WL.H, device=dev) for lw in params.layers]
-    drv = txl.SegmentDriver(mems)
+    drv = txl.SegmentDriver(mems, mem_stream=torch.cuda.Stream() if overlap else None)
 
     def project(n, mem, h):
         ci = W.call_inputs(WL, params.layers[n], params, mem, h, r_k32=rks[n])
@@ -40,9 +40,11 @@ def make_driver(record):
     return drv, project, next_input
 
 
-def test_driver_calls_and_memories_match_oracle():
+@pytest.mark.parametrize("overlap", [False, True])
+def test_driver_calls_and_memories_match_oracle(overlap):
+    """overlap=True runs the rolls on a second stream."""
     rec = []
-    drv, project, next_input = make_driver(rec)
+    drv, project, next_input = make_driver(rec, overlap)
     ref_mem = [bits(m) for m in drv.mems]
     for s in range(WL.segments):
         h0 = W.segment_input(WL, s).cuda().to(WL.torch_dtype)
@@ -65,8 +67,9 @@ def test_driver_calls_and_memories_match_oracle():
         assert np.array_equal(bits(m), ref_mem[n])
 
 
-def test_driver_checkpoint_resume_is_identical():
-    drv, project, next_input = make_driver(None)
+@pytest.mark.parametrize("overlap", [False, True])
+def test_driver_checkpoint_resume_is_identical(overlap):
+    drv, project, next_input = make_driver(None, overlap)
     h = [W.segment_input(WL, s).cuda().to(WL.torch_dtype) for s in range(3)]
     drv.run_segment(h[0], project, next_input)
     sd = drv.state_dict()
