@@ -91,9 +91,16 @@ size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype);
 /*
  * txl_attn_fwd with caller-provided scratch: `workspace` (device, 256-byte
  * aligned, at least txl_attn_workspace_bytes(...) bytes) holds the partial
- * results of the split-key path.  The library then allocates nothing.
- * TXL_ERR_WORKSPACE if the buffer is missing, misaligned or too small.
- * Concurrent calls must use distinct workspaces.
+ * results of the split-key path, which the bf16 kernel takes when the call has
+ * fewer (b, h, 128-row query tile) items than the GPU has SMs: each item's key
+ * tiles are split over several CTAs, each writes its unnormalised partial O
+ * and (max, sum) per row, and a combine pass merges them (the online-softmax
+ * merge).  Nothing in the workspace needs to start at zero; every value read
+ * is written earlier in the same call.  With a size of 0 the workspace is not
+ * touched and may be null.  The library allocates nothing.
+ * TXL_ERR_WORKSPACE if the buffer is missing, misaligned or too small;
+ * TXL_ERR_ALIAS if it overlaps q, k, v or out.  Concurrent calls must use
+ * distinct workspaces.
  */
 int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k,
                     const void* u_bias, const void* v_bias,

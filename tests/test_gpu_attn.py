@@ -164,3 +164,71 @@ def test_bf16_timeout_injection_then_recovery():
     assert txl.sync_status() == -6
     assert txl.sync_status() == 0  # cleared
     check_bf16(ci)
+
+
+# ------------------------------------------------------- split-key workspace path
+@pytest.mark.parametrize("B,H,L,M", [
+    (1, 2, 128, 3000),    # two items, long memory: many splits
+    (2, 3, 200, 1500),    # ragged query tail, two query tiles per (b, h)
+    (1, 1, 64, 700),      # one item, short query tile
+    (2, 2, 128, 1000),    # memory not a tile multiple
+])
+def test_bf16_split_keys_with_workspace(B, H, L, M):
+    ci = W.random_call_inputs(B, H, L, M, 64, seed=B * 7 + M)
+    need = txl.attn_workspace_bytes(B, H, L, M, 64)
+    assert need > 0  # fewer items than SMs: the call splits the keys
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dev = [t.cuda() for t in (ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb)]
+    got = txl.attn_fwd_ws(*dev, ws, scale=ci.scale)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    got = got.float().cpu().double().numpy()
+    ref = oracle.attn(ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb, ci.scale)
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= bf16_tol(ref)
+    # the unsplit entry point agrees within the same tolerance
+    plain = run_gpu(ci)
+    assert np.abs(plain - ref).max() <= bf16_tol(ref)
+
+
+def test_bf16_workspace_entry_full_size_long_memory():
+    """The long-memory workload (B=8, H=16, L=128, M=3200: 128 items) through
+    the workspace entry point, with whatever split the launch picks; the
+    oracle checks a seeded sample of (b, h)."""
+    wl = W.WORKLOADS["longmem3200_bf16"]
+    ci, _, _ = W.first_call_inputs(wl)
+    need = txl.attn_workspace_bytes(wl.B, wl.H, wl.L, wl.M, wl.dh)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+    dev = [t.cuda() for t in (ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb)]
+    got = txl.attn_fwd_ws(*dev, ws, scale=ci.scale)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    got = got.float().cpu().double().numpy()
+    n = wl.B * wl.H
+    pairs = sorted({0, n - 1, *np.random.default_rng(9).choice(n, size=4, replace=False).tolist()})
+    ref = oracle.attn(ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb, ci.scale, pairs=pairs)
+    g = np.stack([got[p // wl.H, p % wl.H] for p in pairs])
+    r = np.stack([ref[p // wl.H, p % wl.H] for p in pairs])
+    assert np.abs(g - r).max() <= bf16_tol(r)
+
+
+def test_bf16_workspace_errors():
+    B, H, L, M = 1, 2, 128, 3000
+    ci = W.random_call_inputs(B, H, L, M, 64, seed=5)
+    dev = [t.cuda() for t in (ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb)]
+    need = txl.attn_workspace_bytes(B, H, L, M, 64)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(txl.TxlError) as e:
+        txl.attn_fwd_ws(*dev, small, scale=ci.scale)
+    assert e.value.code == -7
+    big = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(txl.TxlError) as e:
+        txl.attn_fwd_ws(*dev, big[16:], scale=ci.scale)  # not 256-byte aligned
+    assert e.value.code == -7
+    # a workspace overlapping the output
+    nout = dev[0].numel() * 2
+    buf = torch.empty(need + nout, dtype=torch.uint8, device="cuda")
+    out = buf[need - 256: need - 256 + nout].view(torch.bfloat16).view(dev[0].shape)
+    with pytest.raises(txl.TxlError) as e:
+        txl.attn_fwd_ws(*dev, buf[:need], scale=ci.scale, out=out)
+    assert e.value.code == -4

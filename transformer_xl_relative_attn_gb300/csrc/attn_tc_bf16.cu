@@ -124,7 +124,11 @@ struct TcParams {
     __nv_bfloat16* out;
     int B, H, L, M;
     int n_qtiles;
-    int n_items;
+    int n_items;       // (b, h, query tile) items
+    int nsplit;        // key splits per item (1: the kernel writes the output)
+    int n_units;       // n_items * nsplit work units
+    float* ws_o;       // nsplit > 1: unnormalised O of each unit, [unit][128][64]
+    float2* ws_ml;     // nsplit > 1: (m, l) of each unit's rows, [unit][128]
     float scale_log2;  // scale * log2(e), folded into q+u and q+v
     int inject;        // 1: withhold the first score-ready signal (timeout test)
     int* status;       // device status word
@@ -148,26 +152,46 @@ struct TcShared {
     int abort;
 };
 
-// One work item and the quantities every role derives from it.
+// One work unit and the quantities every role derives from it: the key tiles
+// t0 .. t0+ntiles-1 of one (b, h, query tile) item (all of them unless the
+// item is split over several units).
 struct Item {
-    int bh, h, i0, ntiles, rbase;
+    int bh, h, i0, t0, ntiles, rbase, unit;
 };
 
-// k-th item of this CTA: items are numbered longest query tile first and dealt
-// to CTAs in snake order (rounds alternate direction) to even out the load.
+// k-th unit of this CTA: items are numbered longest query tile first, the
+// splits of an item are adjacent, and units are dealt to CTAs in snake order
+// (rounds alternate direction) to even out the load.  A split takes a
+// contiguous range of tile pairs, so t0 is even.
+template <bool SPLIT>
 __device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
     const int G = gridDim.x, c = blockIdx.x;
-    const long long w = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
-    if (w >= p.n_items) return false;
+    const int w = k * G + ((k & 1) ? (G - 1 - c) : c);  // below 2^31: checked at launch
+    if (w >= p.n_units) return false;
+    int witem = w, sp = 0;
+    if constexpr (SPLIT) {
+        witem = w / p.nsplit;
+        sp = w - witem * p.nsplit;
+    }
     const int n_bh = p.B * p.H;
-    const int qt = p.n_qtiles - 1 - (int)(w / n_bh);
-    it.bh = (int)(w % n_bh);
+    const int qq = witem / n_bh;
+    const int qt = p.n_qtiles - 1 - qq;
+    it.bh = witem - qq * n_bh;
     it.h = it.bh % p.H;
     it.i0 = qt * tc::BM;
     const int rows_valid = min(tc::BM, p.L - it.i0);
     const int kmax = p.M + it.i0 + rows_valid - 1;  // last key any row of the tile sees
-    it.ntiles = kmax / tc::BN + 1;
-    it.rbase = p.L - it.i0 - tc::BM;                // R row of slot 0
+    const int all = kmax / tc::BN + 1;
+    it.t0 = 0;
+    it.ntiles = all;
+    if constexpr (SPLIT) {
+        const int pairs = (all + 1) >> 1;
+        const int lo = pairs * sp / p.nsplit, hi = pairs * (sp + 1) / p.nsplit;
+        it.t0 = 2 * lo;
+        it.ntiles = min(2 * hi, all) - it.t0;
+    }
+    it.rbase = p.L - it.i0 - tc::BM + tc::SLOT * it.t0;  // R row of the unit's slot 0
+    it.unit = w;
     return true;
 }
 
@@ -223,6 +247,9 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
                  : "memory");
 }
 
+// SPLIT: the units are key splits of items and write partial results (see
+// attn_combine_kernel); otherwise every unit is a whole item.
+template <bool SPLIT>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
 attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
@@ -337,7 +364,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         Item cur;
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
-        for (int k = 0; ok && item_of(p, k, cur); ++k) {
+        for (int k = 0; ok && item_of<SPLIT>(p, k, cur); ++k) {
             // the first item's q tile; a failed wait leaves ok false, and the
             // group still reaches this item's merge barriers below
             if (k == 0) {
@@ -345,7 +372,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 write_q(cur, 0, 0);
             }
             Item nxt;
-            const bool has_next = item_of(p, k + 1, nxt);
+            const bool has_next = item_of<SPLIT>(p, k + 1, nxt);
             // the next item's q tile: loaded once this group holds the current
             // item's first scores, turned into (q+bias)c after that tile
             bool next_issued = !has_next, next_written = !has_next;
@@ -368,7 +395,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     issue_q(nxt, (k + 1) & 1);
                     next_issued = true;
                 }
-                const int j0 = t * BN;
+                const int j0 = (cur.t0 + t) * BN;
                 const bool need_mask = (j0 + BN - 1) > (p.M + cur.i0);
                 const int jlim = p.M + i - j0;  // keys jj > jlim are masked
                 float sc[BN];
@@ -523,30 +550,55 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const float l1 = grp ? (seen ? l_run : -1.f) : lo;
                 const bool has0 = l0 >= 0.f, has1 = l1 >= 0.f;
                 const float m = fmaxf(m0, m1);
-                const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
-                const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
-                const float a0 = f0 * inv, a1 = f1 * inv;
                 uint32_t o0[32], o1[32];
                 tmem_ld32(tmem + lane_off + COL_O + 32 * grp, o0);
                 tmem_ld32(tmem + lane_off + COL_O + 64 + 32 * grp, o1);
                 tmem_wait_ld();
                 tc_fence_before();
                 warp_arrive(&sh->o_free);
-                uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH) + 4 * grp;
+                if constexpr (!SPLIT) {
+                    const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
+                    const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
+                    const float a0 = f0 * inv, a1 = f1 * inv;
+                    uint4* orow =
+                        reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH) + 4 * grp;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float y[8];
+                    for (int c = 0; c < 4; ++c) {
+                        float y[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
-                        y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
+                        for (int e = 0; e < 8; ++e) {
+                            const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
+                            y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
+                        }
+                        uint4 w;
+                        w.x = pack_bf16x2(y[0], y[1]);
+                        w.y = pack_bf16x2(y[2], y[3]);
+                        w.z = pack_bf16x2(y[4], y[5]);
+                        w.w = pack_bf16x2(y[6], y[7]);
+                        if (i < p.L) orow[c] = w;
                     }
-                    uint4 w;
-                    w.x = pack_bf16x2(y[0], y[1]);
-                    w.y = pack_bf16x2(y[2], y[3]);
-                    w.z = pack_bf16x2(y[4], y[5]);
-                    w.w = pack_bf16x2(y[6], y[7]);
-                    if (i < p.L) orow[c] = w;
+                } else {
+                    // this unit's share: O relative to the row max m, and
+                    // (m, l); a split unit may hold no visible key of a row
+                    // (all its keys past the row's diagonal): zeros, l = 0
+                    const bool live = m > -INFINITY;
+                    const float f0 = (has0 && live) ? ex2(m0 - m) : 0.f;
+                    const float f1 = (has1 && live) ? ex2(m1 - m) : 0.f;
+                    float4* orow = reinterpret_cast<float4*>(
+                        p.ws_o + ((size_t)cur.unit * BM + ii) * DH + 32 * grp);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float y[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = has0 ? __uint_as_float(o0[4 * c + e]) * f0 : 0.f;
+                            y[e] = has1 ? fmaf(__uint_as_float(o1[4 * c + e]), f1, x0) : x0;
+                        }
+                        orow[c] = make_float4(y[0], y[1], y[2], y[3]);
+                    }
+                    if (grp == 0)
+                        p.ws_ml[(size_t)cur.unit * BM + ii] =
+                            make_float2(m, (has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
                 }
             }
             gbase += slots_of(cur.ntiles);
@@ -587,7 +639,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             int kv_s = 0, r_s = 0;     // K/V stage and R box counters at the item start
             int gbase = 0;             // global position-slot counter at the item start
             Item is;
-            for (int ks = 0; ok && item_of(p, ks, is); ++ks) {
+            for (int ks = 0; ok && item_of<SPLIT>(p, ks, is); ++ks) {
                 const int npairs = (is.ntiles + 1) >> 1;
                 const int nrb = npairs + 1;  // R boxes of the item (slots 0 .. 2*npairs+1)
                 wait(&sh->q_ready, ks & 1);
@@ -663,7 +715,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dV0 = smem_desc_sw128(s_base + OFF_KV + SZ_BOX, BN * 128, 1024);
             constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
             Item ip;
-            bool p_valid = item_of(p, 0, ip);
+            bool p_valid = item_of<SPLIT>(p, 0, ip);
             int kp = 0, tp = 0, kv_p = 0;
             int pc0 = 0, pc1 = 0;  // P tiles consumed, per group
             while (ok && p_valid) {
@@ -692,7 +744,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     kv_p += (ip.ntiles + 1) >> 1;
                     tp = 0;
                     ++kp;
-                    p_valid = item_of(p, kp, ip);
+                    p_valid = item_of<SPLIT>(p, kp, ip);
                 }
             }
             if (leader) mma_commit(&sh->drain);
@@ -705,7 +757,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             int kvc = 0, rc = 0;  // loads issued into each ring
             bool ok = true;
             Item it;
-            for (int k = 0; ok && item_of(p, k, it); ++k) {
+            for (int k = 0; ok && item_of<SPLIT>(p, k, it); ++k) {
                 const int nkv = (it.ntiles + 1) >> 1;  // K/V stages of this item
                 const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
                 int rb = 0;
@@ -731,14 +783,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                     // warm L2 PREFETCH stages ahead (the first ones at the item start)
                     for (int w = (u == 0 ? 1 : u + PREFETCH); w <= u + PREFETCH && w < nkv; ++w) {
-                        tma_prefetch_l2_3d(&tmK, 0, w * 2 * BN, it.bh);
-                        tma_prefetch_l2_3d(&tmV, 0, w * 2 * BN, it.bh);
+                        tma_prefetch_l2_3d(&tmK, 0, (it.t0 + 2 * w) * BN, it.bh);
+                        tma_prefetch_l2_3d(&tmV, 0, (it.t0 + 2 * w) * BN, it.bh);
                         tma_prefetch_l2_2d(&tmR, it.h * DH, it.rbase + SLOT * 2 * (w + 1));
                     }
                     mbar_expect_tx(&sh->kv_full[s], 2 * SZ_BOX);
                     uint8_t* st = smem + OFF_KV + s * 2 * SZ_BOX;
-                    tma_load_3d(st, &tmK, &sh->kv_full[s], 0, u * 2 * BN, it.bh);
-                    tma_load_3d(st + SZ_BOX, &tmV, &sh->kv_full[s], 0, u * 2 * BN, it.bh);
+                    tma_load_3d(st, &tmK, &sh->kv_full[s], 0, (it.t0 + 2 * u) * BN, it.bh);
+                    tma_load_3d(st + SZ_BOX, &tmV, &sh->kv_full[s], 0, (it.t0 + 2 * u) * BN, it.bh);
                     ++kvc;
                 }
             }
@@ -757,6 +809,45 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// Combines the key splits of every query row: with m* the largest split max
+// of the row, out = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s (the
+// online-softmax merge of partial results).  One thread per 8 output columns.
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
+                    __nv_bfloat16* __restrict__ out, int n_bh, int L, int n_qtiles, int nsplit) {
+    using namespace tc;
+    const int t = blockIdx.x * 256 + threadIdx.x;
+    if (t >= n_bh * L * 8) return;
+    const int ch = t & 7, row = t >> 3;
+    const int i = row % L, bh = row / L;
+    const int qt = i / BM, ii = i % BM;
+    const int witem = (n_qtiles - 1 - qt) * n_bh + bh;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) {
+        const float2 ml = ws_ml[(size_t)(witem * nsplit + sp) * BM + ii];
+        if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, den = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+        const size_t unit = (size_t)witem * nsplit + sp;
+        const float2 ml = ws_ml[unit * BM + ii];
+        if (!(ml.y > 0.f)) continue;
+        const float w = exp2f(ml.x - mx);
+        den += w * ml.y;
+        const float4* o = reinterpret_cast<const float4*>(ws_o + (unit * BM + ii) * DH + 8 * ch);
+        const float4 a = o[0], b = o[1];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+    const float inv = 1.f / den;
+    uint4 r;
+    r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    r.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    r.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    r.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    reinterpret_cast<uint4*>(out + ((size_t)bh * L + i) * DH)[ch] = r;
 }
 
 // ---------------------------------------------------------------- host side
@@ -802,15 +893,59 @@ static int num_sms() {
 }
 
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+// Key splits per item when a workspace is available.  With fewer items than
+// SMs, whole items leave SMs idle; splitting each item's key tiles over
+// several units fills them, at the price of per-unit work (the q tile, the
+// first pair's extra position slots, the partial result) and a combine pass.
+// The count minimises a makespan estimate in key tiles: rounds of units per
+// CTA times (tiles per unit + kUnitCost), plus kCombineCost when split.
+// Every split keeps at least two tile pairs.
+int attn_tc_bf16_splits(int B, int H, int L, int M) {
+    using namespace tc;
+    constexpr double kUnitCost = 3.0, kCombineCost = 4.0;  // in key tiles, measured on GB300
+    const long long n_items = (long long)B * H * ((L + BM - 1) / BM);
+    const int sms = num_sms();
+    if (n_items >= sms || n_items <= 0) return 1;
+    const int tiles_max = (M + L - 1) / BN + 1;                 // longest item
+    const int tiles0 = (M + (L < BM ? L : BM) - 1) / BN + 1;   // shortest item
+    const int max_split = ((tiles0 + 1) / 2) / 2;
+    int best = 1;
+    double best_cost = 1e300;
+    for (int ns = 1; ns <= max_split || ns == 1; ++ns) {
+        const long long units = n_items * ns;
+        const double rounds = (double)((units + sms - 1) / sms);
+        const double cost = rounds * ((double)tiles_max / ns + kUnitCost) + (ns > 1 ? kCombineCost : 0.0);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = ns;
+        }
+        if (ns >= 64) break;
+    }
+    return best;
+}
+
+// Workspace bytes of a split launch (0 when the launch does not split):
+// per unit, O [128][64] and (m, l) [128] in fp32.
+size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M) {
+    using namespace tc;
+    const int ns = attn_tc_bf16_splits(B, H, L, M);
+    if (ns <= 1) return 0;
+    const size_t units = (size_t)B * H * ((L + BM - 1) / BM) * ns;
+    return units * BM * (DH * sizeof(float) + sizeof(float2));
+}
+
 cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
                                 const void* ub, const void* vb, int B, int H, int L, int M,
-                                float scale, void* out, int inject, int* status,
+                                float scale, void* out, void* workspace, int inject, int* status,
                                 cudaStream_t stream) {
     using namespace tc;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_bf16_kernel,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -849,11 +984,27 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     const long long n_items = (long long)B * H * p.n_qtiles;
     if (n_items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_items = (int)n_items;
+    p.nsplit = workspace ? attn_tc_bf16_splits(B, H, L, M) : 1;
+    if ((long long)p.n_items * p.nsplit + 2ll * num_sms() >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    p.n_units = p.n_items * p.nsplit;
+    const size_t units = (size_t)p.n_units;
+    p.ws_o = p.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+    p.ws_ml = p.nsplit > 1 ? reinterpret_cast<float2*>(static_cast<float*>(workspace) + units * BM * DH)
+                           : nullptr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.inject = inject;
     p.status = status;
-    const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
-    attn_tc_bf16_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+    const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
+    if (p.nsplit > 1)
+        attn_tc_bf16_kernel<true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+    else
+        attn_tc_bf16_kernel<false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.nsplit == 1) return e;
+    const long long threads = (long long)B * H * L * 8;
+    if (threads >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    attn_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
+        p.ws_o, p.ws_ml, p.out, B * H, L, p.n_qtiles, p.nsplit);
     return cudaGetLastError();
 }
 

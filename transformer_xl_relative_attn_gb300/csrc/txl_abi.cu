@@ -18,8 +18,9 @@ cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v,
                                  int dh, float scale, float* out, cudaStream_t stream);
 cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
                                 const void* ub, const void* vb, int B, int H, int L, int M,
-                                float scale, void* out, int inject, int* status,
+                                float scale, void* out, void* workspace, int inject, int* status,
                                 cudaStream_t stream);
+size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
 }  // namespace txl
 
 namespace {
@@ -70,7 +71,7 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* r_k
 
 int launch_attn(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
                 const void* v_bias, int B, int H, int L, int M, int d_h, float scale, void* out,
-                int dtype, void* stream) {
+                int dtype, void* workspace, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == TXL_BF16) {
@@ -78,8 +79,8 @@ int launch_attn(const void* q, const void* k, const void* v, const void* r_k, co
         if (!status) return TXL_ERR_CUDA;
         const int inject = g_inject;
         g_inject = 0;
-        e = txl::launch_attn_tc_bf16(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale, out, inject,
-                                     status, st);
+        e = txl::launch_attn_tc_bf16(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale, out,
+                                     workspace, inject, status, st);
         if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // tensor-map encoding failed
     } else {
         e = txl::launch_attn_simt_f32(
@@ -100,12 +101,15 @@ int txl_attn_fwd(const void* q, const void* k, const void* v, const void* r_k,
                  float scale, void* out, int dtype, void* stream) {
     const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
     if (rc != TXL_OK) return rc;
-    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, stream);
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, nullptr,
+                       stream);
 }
 
 size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype) {
-    (void)B; (void)H; (void)L; (void)M; (void)d_h; (void)dtype;
-    return 0;
+    // only the bf16 kernel splits; sizes a call would reject need nothing
+    if (dtype != TXL_BF16 || d_h != 64 || B <= 0 || H <= 0 || L <= 0 || M < 0) return 0;
+    if ((long long)M + L >= (1ll << 30) || (long long)B * H >= (1ll << 30)) return 0;
+    return txl::attn_tc_bf16_workspace_bytes(B, H, L, M);
 }
 
 int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k,
@@ -118,8 +122,14 @@ int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k
     if (need) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < need)
             return TXL_ERR_WORKSPACE;
+        const int es = elem_size(dtype);
+        const size_t nq = (size_t)B * H * L * d_h * es, nkv = (size_t)B * H * ((size_t)M + L) * d_h * es;
+        if (overlap(workspace, need, out, nq) || overlap(workspace, need, q, nq) ||
+            overlap(workspace, need, k, nkv) || overlap(workspace, need, v, nkv))
+            return TXL_ERR_ALIAS;
     }
-    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, stream);
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype,
+                       need ? workspace : nullptr, stream);
 }
 
 int txl_mem_update(void* mems, const void* hids, int B, int L, int M, int d, int dtype,
