@@ -50,7 +50,8 @@ enum txl_status {
     TXL_ERR_LAUNCH = -5,         /* the CUDA launch itself failed */
     TXL_ERR_DEVICE_TIMEOUT = -6, /* a bounded device-side wait expired (reported by txl_sync_status) */
     TXL_ERR_WORKSPACE = -7,      /* workspace pointer null/misaligned or smaller than required */
-    TXL_ERR_CUDA = -8            /* a CUDA runtime/driver call failed (e.g. tensor-map encoding) */
+    TXL_ERR_CUDA = -8,           /* a CUDA runtime/driver call failed (e.g. tensor-map encoding) */
+    TXL_ERR_SCRATCH_LIMIT = -9   /* the call needs more scratch than txl_attn_fwd_noalloc holds */
 };
 
 /*
@@ -106,6 +107,37 @@ int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k
                     const void* u_bias, const void* v_bias,
                     int B, int H, int L, int M, int d_h, float scale, void* out,
                     int dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of the static device scratch that txl_attn_fwd_noalloc uses.
+ */
+#define TXL_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * txl_attn_fwd_ws without a caller workspace and without any allocation: the
+ * split-key path (see txl_attn_fwd_ws) takes its partial results from one
+ * file-scope static device buffer of TXL_NOALLOC_SCRATCH_BYTES (16 MiB) per
+ * device, whose address the library looks up once per device on the first
+ * call.  The pages have no counterpart of this entry point: it exists for
+ * callers that cannot hand out a workspace (for example a fixed launch
+ * sequence).
+ *
+ *   - Same arguments, results and errors as txl_attn_fwd_ws; a call whose
+ *     txl_attn_workspace_bytes(...) exceeds TXL_NOALLOC_SCRATCH_BYTES returns
+ *     TXL_ERR_SCRATCH_LIMIT and launches nothing.
+ *   - Nothing in the scratch needs to start at zero: every value read is
+ *     written earlier in the same call.
+ *   - The first call on each device must not be inside a stream capture (it
+ *     looks the buffer up with cudaGetSymbolAddress).
+ *   - Calls that overlap in time on one device (different streams, or
+ *     threads) share the buffer and race: order them, e.g. on one stream.
+ *   - Calls that need no scratch (txl_attn_workspace_bytes(...) == 0) do not
+ *     touch it.
+ */
+int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* r_k,
+                         const void* u_bias, const void* v_bias,
+                         int B, int H, int L, int M, int d_h, float scale, void* out,
+                         int dtype, void* stream);
 
 /*
  * Tail_M memory roll, in place ("Transformer-XL" notes, section

@@ -3,15 +3,18 @@ recurrence memory.
 
 Public API (all computation runs in libtxl.so's CUDA kernels):
     attn_fwd, attn_fwd_ws, attn_workspace_bytes   relative attention forward
+    attn_fwd_noalloc                              the same with the library's static scratch
     mem_update                                    Tail_M memory roll, in place
     sync_status, check_status                     device status word
     SegmentDriver                                 multi-segment, multi-layer driver
 """
-from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_ws, attn_workspace_bytes,
+from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
+                   attn_workspace_bytes,
                    check_status, debug_inject, header_functions, load, mem_update, status_string,
                    sync_status, version, LIB_PATH)
 from .driver import SegmentDriver
 
-__all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_ws", "attn_workspace_bytes",
+__all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
+           "attn_workspace_bytes",
            "check_status", "debug_inject", "header_functions", "load", "mem_update",
            "status_string", "sync_status", "version", "SegmentDriver", "LIB_PATH"]

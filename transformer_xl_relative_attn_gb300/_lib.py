@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_fwd.restype = i
         lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
         lib.txl_attn_fwd_ws.restype = i
+        lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
+        lib.txl_attn_fwd_noalloc.restype = i
         lib.txl_attn_workspace_bytes.argtypes = [i] * 6
         lib.txl_attn_workspace_bytes.restype = sz
         lib.txl_mem_update.argtypes = [vp, vp] + [i] * 5 + [vp]
@@ -168,6 +170,19 @@ def attn_fwd_ws(q, k, v, r_k, u, vb, workspace, scale=None, out=None, stream=Non
                                 _dtype_code(q), wp, wn, _stream(stream, q.device))
     if rc != 0:
         raise TxlError(rc, "txl_attn_fwd_ws")
+    return out
+
+
+def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
+    """txl_attn_fwd_noalloc: like attn_fwd_ws, with the library's static
+    device scratch instead of a caller workspace (calls on one device must not
+    overlap in time; the first call on a device must not be captured)."""
+    B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    rc = load().txl_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                                     u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale,
+                                     out.data_ptr(), _dtype_code(q), _stream(stream, q.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_attn_fwd_noalloc")
     return out
 
 

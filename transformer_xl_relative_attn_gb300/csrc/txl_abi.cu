@@ -3,6 +3,7 @@
 // caller's stream.  Nothing here allocates device memory.
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "txl_attn.h"
@@ -24,6 +25,27 @@ size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
 }  // namespace txl
 
 namespace {
+
+// Scratch of txl_attn_fwd_noalloc: one static buffer per device (a module
+// global exists once per device context).
+__device__ __align__(256) unsigned char g_noalloc_scratch[TXL_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Address of the static scratch on the current device, looked up once.
+void* noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    return g_scratch_addr[dev];
+}
 
 int g_inject = 0;
 
@@ -161,6 +183,22 @@ int txl_sync_status(void* stream) {
     return TXL_OK;
 }
 
+int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* r_k,
+                         const void* u_bias, const void* v_bias, int B, int H, int L, int M,
+                         int d_h, float scale, void* out, int dtype, void* stream) {
+    const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
+    if (rc != TXL_OK) return rc;
+    const size_t need = txl_attn_workspace_bytes(B, H, L, M, d_h, dtype);
+    if (need > TXL_NOALLOC_SCRATCH_BYTES) return TXL_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if (need) {
+        scratch = noalloc_scratch();
+        if (!scratch) return TXL_ERR_CUDA;
+    }
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, scratch,
+                       stream);
+}
+
 const char* txl_status_string(int status) {
     switch (status) {
         case TXL_OK: return "ok";
@@ -172,6 +210,7 @@ const char* txl_status_string(int status) {
         case TXL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case TXL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case TXL_ERR_CUDA: return "CUDA runtime/driver call failed";
+        case TXL_ERR_SCRATCH_LIMIT: return "call needs more scratch than the static no-alloc buffer";
         default: return "unknown status";
     }
 }
