@@ -356,7 +356,8 @@ def run_ours(args, wl: W.Workload):
     }
 
     if not args.no_e2e:
-        result["e2e"] = measure_e2e(args, wl, calls, graph, stream, flops_step, ws)
+        result["e2e"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch,
+                                    flops_step, ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"], result["parity"] = cpu_baseline_and_parity(wl, calls, rks, u, vb)
     if rank == 0:
@@ -392,22 +393,59 @@ def measured_traffic(workload):
     return cap["bytes_per_launch"]
 
 
-def measure_e2e(args, wl, calls, graph, stream, flops_step, ws):
-    """Same metric end to end: each step copies every input of the step from
-    pinned host memory, replays the step and reads every output back."""
-    ins = [(c[x], c[x].cpu().pin_memory()) for c in calls for x in ("q", "k", "v", "h")]
+def measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch, flops_step, ws):
+    """Same metric end to end through the public API: each step copies every
+    input of the step from pinned host memory (q, k, v and the layer input h
+    of every call) and reads every attention output back.  Copies run on
+    their own streams and overlap the calls: call i starts once its inputs
+    arrived, its output leaves once it is written; the next step's copies
+    into a buffer wait until this step is done with it."""
+    import transformer_xl_relative_attn_gb300 as txl
+
+    ins = [[(c[x], c[x].cpu().pin_memory()) for x in ("q", "k", "v", "h")] for c in calls]
     outs = [(c["out"], torch.empty(c["out"].shape, dtype=c["out"].dtype).pin_memory()) for c in calls]
-    h2d = sum(d.numel() * d.element_size() for d, _ in ins)
+    h2d = sum(d.numel() * d.element_size() for call in ins for d, _ in call)
     d2h = sum(d.numel() * d.element_size() for d, _ in outs)
     steps = max(3, min(args.steps, 10))
+    dev = stream.device
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_calls = len(calls)
 
     def one():
-        with torch.cuda.stream(stream):
-            for d, hbuf in ins:
-                d.copy_(hbuf, non_blocking=True)
-            graph.replay()
-            for d, hbuf in outs:
-                hbuf.copy_(d, non_blocking=True)
+        arrived = [torch.cuda.Event() for _ in range(n_calls)]
+        written = [torch.cuda.Event() for _ in range(n_calls)]
+        rolled = {}
+        with torch.cuda.stream(up):
+            for i in range(n_calls):
+                for d, hbuf in ins[i]:
+                    d.copy_(hbuf, non_blocking=True)
+                arrived[i].record(up)
+        for i, c in enumerate(calls):
+            n = c["n"]
+            stream.wait_event(arrived[i])
+            if n in rolled:
+                stream.wait_event(rolled[n])
+            ready = torch.cuda.Event()
+            ready.record(stream)
+            if scratch is None:
+                txl.attn_fwd(c["q"], c["k"], c["v"], rks[n], u, vb, wl.scale, out=c["out"], stream=stream)
+            else:
+                txl.attn_fwd_ws(c["q"], c["k"], c["v"], rks[n], u, vb, scratch, wl.scale,
+                                out=c["out"], stream=stream)
+            written[i].record(stream)
+            side.wait_event(ready)
+            txl.mem_update(mems[n], c["h"], stream=side)
+            rolled[n] = torch.cuda.Event()
+            rolled[n].record(side)
+            down.wait_event(written[i])
+            with torch.cuda.stream(down):
+                outs[i][1].copy_(outs[i][0], non_blocking=True)
+        # the next step's copies overwrite these inputs and outputs
+        for st in (stream, side, down):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            up.wait_event(ev)
+            stream.wait_event(ev)
 
     one()
     torch.cuda.synchronize()
