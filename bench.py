@@ -299,6 +299,7 @@ def run_ours(args, wl: W.Workload):
     sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
+    roll_ms = time_rolls(calls, mems, stream)
     txl.check_status()
     flops_call = wl.attn_flops()
     flops_step = flops_call * n_calls
@@ -351,6 +352,21 @@ def run_ours(args, wl: W.Workload):
             "attn_share_of_step": round(sum(attn_ms) / ms_per_step, 4),
         },
         # per call: the attention kernel (+ the split combine pass) and Tail_M
+        # the Tail_M roll timed alone after the timed region (in the step it
+        # runs on a second stream in the gaps between attention kernels)
+        "roofline_mem_update": {
+            "kernel": "tail_copy_kernel" if wl.L >= wl.M else "tail_chain_kernel",
+            "bound": "hbm",
+            "achieved": round(wl.mem_update_bytes() / (sum(roll_ms) / len(roll_ms) * 1e-3) / 1e9, 1),
+            "peak": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+            "unit": "GB/s",
+            "frac": round(wl.mem_update_bytes() / (sum(roll_ms) / len(roll_ms) * 1e-3) / 1e9
+                          / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), 4),
+            "bytes_per_launch": wl.mem_update_bytes(),
+            "avg_launch_ms": round(sum(roll_ms) / len(roll_ms), 5),
+            "measured": "each call's roll once, in step order, alone on one stream, as a CUDA graph "
+                        "with CUDA events between the rolls",
+        },
         "gpu_launches": (3 if scratch is not None else 2) * n_calls * args.steps,
         "clocks": sampler.summary(),
     }
@@ -391,6 +407,27 @@ def measured_traffic(workload):
             if hashlib.sha256(f.read()).hexdigest()[:16] != prefix:
                 return None
     return cap["bytes_per_launch"]
+
+
+def time_rolls(calls, mems, stream):
+    """Durations (ms) of every call's Tail_M roll, each alone on `stream`, in
+    step order (so consecutive rolls touch different layers' memories).  The
+    rolls and their events are captured in a CUDA graph first, so the events
+    time the device, not the host's launch path."""
+    import transformer_xl_relative_attn_gb300 as txl
+
+    evs = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in calls]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c, (a, b) in zip(calls, evs):
+            a.record()
+            txl.mem_update(mems[c["n"]], c["h"])
+            b.record()
+    g.replay()
+    torch.cuda.synchronize()
+    txl.check_status()
+    return [a.elapsed_time(b) for a, b in evs]
 
 
 def measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch, flops_step, ws):
