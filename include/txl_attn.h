@@ -140,6 +140,35 @@ int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
                          int dtype, void* stream);
 
 /*
+ * Projections feeding txl_attn_fwd, bf16 in and out, fp32 accumulation, on
+ * the tensor cores ("Transformer-XL模型 核心源码阅读笔记",
+ * RelPartialLearnableMultiHeadAttn.forward: qkv_net over the concatenation of
+ * memory and current hidden states, r_net over the position embedding).
+ *
+ * txl_qkv_proj:
+ *   h     [B, L, d]     current hidden states (layer input), d = H * d_h
+ *   mem   [B, M, d]     the layer's memory (may be null when M = 0)
+ *   w_qkv [3d, d]       stacked weights, rows [0,d) W_q, [d,2d) W_k, [2d,3d) W_v
+ *                       (output = input x W^T, the nn.Linear layout)
+ *   q     [B, H, L, d_h]      q = h W_q^T, split into heads
+ *   k, v  [B, H, M+L, d_h]    rows 0..M-1 from mem, rows M.. from h, split into
+ *                             heads (no [mem; h] concatenation is formed)
+ * txl_r_proj:
+ *   emb   [K, d]   position embedding rows (the sinusoid of distances K-1..0)
+ *   w_r   [d, d]   W_r (nn.Linear layout)
+ *   r_k   [K, H, d_h] = emb W_r^T (row-major [K, d])
+ *
+ * Supported sizes (TXL_ERR_UNSUPPORTED otherwise): d_h = 64, H a multiple of
+ * 4, L, M and K multiples of 128 (M may be 0).  Pointers 16-byte aligned
+ * (TXL_ERR_MISALIGNED); outputs must not overlap inputs (TXL_ERR_ALIAS).
+ * Asynchronous on `stream`; nothing is allocated.  Bounded device waits
+ * report TXL_ERR_DEVICE_TIMEOUT through txl_sync_status.
+ */
+int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L, int M, int H,
+                 int d_h, void* q, void* k, void* v, void* stream);
+int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream);
+
+/*
  * Tail_M memory roll, in place ("Transformer-XL" notes, section
  * "Segment-Level Recurrence": M_{tau+1} = Tail_M([M_tau; H_tau]); source notes
  * MemTransformerLM._update_mems with ext_len = 0 and a full memory).

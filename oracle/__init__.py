@@ -20,6 +20,14 @@ mem_update(mem, hid, mem_len, ext_len=0)
     source-reading notes (end = mlen + max(0, qlen - ext_len),
     beg = max(0, end - mem_len)) and the batch-major layout of the
     "Transformer-XL" notes, section "Batched Tensor Contract".
+qkv_proj(h, mem, w_qkv, n_head), r_proj(emb, w_r, n_head)
+    The projections that feed the attention, as the source-reading notes
+    write them (RelPartialLearnableMultiHeadAttn.forward: qkv_net applied to
+    the concatenation cat = [mems; w] along the sequence axis, its output
+    chunked into q, k, v and viewed as heads; r_net applied to the position
+    embedding): here literally a concatenation, an fp64 matrix product with
+    the nn.Linear convention (output = input W^T) and a reshape into heads,
+    batch-major as in the "Transformer-XL" notes' "Batched Tensor Contract".
 sinusoid(pos, demb)
     Is NOT here: the sinusoid is input preparation and lives in the seeded
     workload module.
@@ -143,3 +151,30 @@ def mem_update(mem, hid, mem_len: int, ext_len: int = 0) -> np.ndarray:
     beg = max(0, end - mem_len)
     cat = np.concatenate([mem, hid], axis=1)
     return np.ascontiguousarray(cat[:, beg:end])
+
+
+def _heads(x: np.ndarray, n_head: int) -> np.ndarray:
+    """[B, T, n_head*d_head] -> [B, n_head, T, d_head]."""
+    B, T, d = x.shape
+    return x.reshape(B, T, n_head, d // n_head).transpose(0, 2, 1, 3).copy()
+
+
+def qkv_proj(h, mem, w_qkv, n_head: int):
+    """q from the current segment only, k and v from [mem; h]; w_qkv [3d, d]
+    stacks W_q, W_k, W_v (output = input W^T).  Returns fp64 q [B,H,L,dh],
+    k, v [B,H,M+L,dh]."""
+    h64, m64, w64 = _f64(h), _f64(mem), _f64(w_qkv)
+    d = h64.shape[2]
+    cat = np.concatenate([m64, h64], axis=1)
+    wq, wk, wv = w64[:d], w64[d:2 * d], w64[2 * d:]
+    q = _heads(h64 @ wq.T, n_head)
+    k = _heads(cat @ wk.T, n_head)
+    v = _heads(cat @ wv.T, n_head)
+    return q, k, v
+
+
+def r_proj(emb, w_r, n_head: int):
+    """r_k [K, H, dh] = emb [K, d] W_r^T (fp64)."""
+    e64, w64 = _f64(emb), _f64(w_r)
+    K, d = e64.shape
+    return (e64 @ w64.T).reshape(K, n_head, d // n_head)

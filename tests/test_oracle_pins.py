@@ -331,3 +331,42 @@ def test_workload_flop_and_byte_counts():
     assert wl.visible_pairs() == 393472
     assert wl.attn_flops() == 6 * 64 * 22 * 8 * 393472
     assert wl.mem_update_bytes() == 2 * 22 * 512 * 512 * 2
+
+
+# --------------------------------------------------------------------------
+# projections feeding the attention (qkv_net over [mem; h], r_net)
+# --------------------------------------------------------------------------
+def test_qkv_proj_identity_and_permutation_weights():
+    """W_q = I gives q = h split into heads; W_k a cyclic column shift and
+    W_v = 2I pin the output = input W^T convention, the head split and the
+    memory-rows-first order of k and v."""
+    B, L, M, H, dh = 2, 3, 2, 2, 4
+    d = H * dh
+    h = np.arange(B * L * d, dtype=np.float64).reshape(B, L, d)
+    mem = -np.arange(B * M * d, dtype=np.float64).reshape(B, M, d) - 1
+    shift = np.roll(np.eye(d), 1, axis=1)       # (x shift^T)[:, c] = x[:, c + 1 mod d]
+    w = np.concatenate([np.eye(d), shift, 2 * np.eye(d)])
+    q, k, v = oracle.qkv_proj(h, mem, w, H)
+    for b in range(B):
+        for hh in range(H):
+            cols = slice(hh * dh, (hh + 1) * dh)
+            np.testing.assert_array_equal(q[b, hh], h[b, :, cols])
+            cat = np.concatenate([mem[b], h[b]])
+            np.testing.assert_array_equal(v[b, hh], 2 * cat[:, cols])
+            rolled = np.roll(cat, -1, axis=1)
+            np.testing.assert_array_equal(k[b, hh], rolled[:, cols])
+    assert k.shape == (B, H, M + L, dh) and q.shape == (B, H, L, dh)
+
+
+def test_r_proj_is_rowwise_product_split_into_heads():
+    K, H, dh = 5, 2, 3
+    d = H * dh
+    rng = np.random.default_rng(3)
+    emb = rng.normal(size=(K, d))
+    w = rng.normal(size=(d, d))
+    r = oracle.r_proj(emb, w, H)
+    for t in range(K):
+        for hh in range(H):
+            for e in range(dh):
+                ref = sum(emb[t, c] * w[hh * dh + e, c] for c in range(d))
+                assert abs(r[t, hh, e] - ref) < 1e-12

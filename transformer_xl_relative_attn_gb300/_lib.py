@@ -58,6 +58,10 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_fwd_ws.restype = i
         lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
         lib.txl_attn_fwd_noalloc.restype = i
+        lib.txl_qkv_proj.argtypes = [vp] * 3 + [i] * 5 + [vp] * 4
+        lib.txl_qkv_proj.restype = i
+        lib.txl_r_proj.argtypes = [vp, vp] + [i] * 3 + [vp, vp]
+        lib.txl_r_proj.restype = i
         lib.txl_attn_workspace_bytes.argtypes = [i] * 6
         lib.txl_attn_workspace_bytes.restype = sz
         lib.txl_mem_update.argtypes = [vp, vp] + [i] * 5 + [vp]
@@ -183,6 +187,50 @@ def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
                                      out.data_ptr(), _dtype_code(q), _stream(stream, q.device))
     if rc != 0:
         raise TxlError(rc, "txl_attn_fwd_noalloc")
+    return out
+
+
+def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
+    """txl_qkv_proj: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
+    h [B, L, d], mem [B, M, d] (M may be 0), w_qkv [3d, d]; bf16 CUDA tensors.
+    Returns (q [B, H, L, d_h], k, v [B, H, M+L, d_h])."""
+    if h.dim() != 3 or mem.dim() != 3:
+        raise ValueError("h must be [B, L, d] and mem [B, M, d]")
+    B, L, d = h.shape
+    M = mem.shape[1]
+    dh = d // H
+    _need(h, "h", (B, L, d), torch.bfloat16)
+    if M > 0:
+        _need(mem, "mem", (B, M, d), torch.bfloat16)
+    _need(w_qkv, "w_qkv", (3 * d, d), torch.bfloat16)
+    if q is None:
+        q = torch.empty((B, H, L, dh), dtype=torch.bfloat16, device=h.device)
+    if k is None:
+        k = torch.empty((B, H, M + L, dh), dtype=torch.bfloat16, device=h.device)
+    if v is None:
+        v = torch.empty((B, H, M + L, dh), dtype=torch.bfloat16, device=h.device)
+    _need(q, "q", (B, H, L, dh), torch.bfloat16)
+    _need(k, "k", (B, H, M + L, dh), torch.bfloat16)
+    _need(v, "v", (B, H, M + L, dh), torch.bfloat16)
+    rc = load().txl_qkv_proj(h.data_ptr(), mem.data_ptr() if M > 0 else 0, w_qkv.data_ptr(), B, L, M, H,
+                             dh, q.data_ptr(), k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_qkv_proj")
+    return q, k, v
+
+
+def r_proj(emb, w_r, H, out=None, stream=None):
+    """txl_r_proj: r_k [K, H, d_h] = emb [K, d] W_r^T; bf16 CUDA tensors."""
+    K, d = emb.shape
+    dh = d // H
+    _need(emb, "emb", (K, d), torch.bfloat16)
+    _need(w_r, "w_r", (d, d), torch.bfloat16)
+    if out is None:
+        out = torch.empty((K, H, dh), dtype=torch.bfloat16, device=emb.device)
+    _need(out, "r_k", (K, H, dh), torch.bfloat16)
+    rc = load().txl_r_proj(emb.data_ptr(), w_r.data_ptr(), K, H, dh, out.data_ptr(), _stream(stream, emb.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_r_proj")
     return out
 
 

@@ -22,6 +22,9 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, void* out, void* workspace, int inject, int* status,
                                 cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
+cudaError_t launch_proj_gemm(const void* a_src, int Ta, const void* b_src, int Tb, int B,
+                             const void* w, int N, int K, int d, int H, int dh, int T_out, int plain,
+                             void* out0, void* out1, void* out2, int* status, cudaStream_t stream);
 }  // namespace txl
 
 namespace {
@@ -197,6 +200,57 @@ int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
     }
     return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, scratch,
                        stream);
+}
+
+int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L, int M, int H,
+                 int d_h, void* q, void* k, void* v, void* stream) {
+    if (!h || !w_qkv || !q || !k || !v || (M > 0 && !mem)) return TXL_ERR_INVALID_ARG;
+    if (B <= 0 || L <= 0 || M < 0 || H <= 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
+    if (d_h != 64 || H % 4 != 0 || L % 128 != 0 || M % 128 != 0) return TXL_ERR_UNSUPPORTED;
+    const long long d = (long long)H * d_h;
+    if ((long long)B * (M + L) * d >= (1ll << 31) || (long long)(M + L) >= (1ll << 20))
+        return TXL_ERR_UNSUPPORTED;
+    if (!aligned16(h) || !aligned16(w_qkv) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        (M > 0 && !aligned16(mem)))
+        return TXL_ERR_MISALIGNED;
+    const size_t nh = (size_t)B * L * d * 2, nm = (size_t)B * M * d * 2, nw = (size_t)3 * d * d * 2;
+    const size_t nq = nh, nkv = (size_t)B * (M + L) * d * 2;
+    const void* outs[3] = {q, k, v};
+    const size_t nout[3] = {nq, nkv, nkv};
+    for (int o = 0; o < 3; ++o) {
+        if (overlap(outs[o], nout[o], h, nh) || overlap(outs[o], nout[o], w_qkv, nw) ||
+            (M > 0 && overlap(outs[o], nout[o], mem, nm)))
+            return TXL_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlap(outs[o], nout[o], outs[o2], nout[o2])) return TXL_ERR_ALIAS;
+    }
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const unsigned char* w = static_cast<const unsigned char*>(w_qkv);
+    cudaError_t e = txl::launch_proj_gemm(h, 0, h, L, B, w, (int)d, (int)d, (int)d, H, d_h, L, 0, q,
+                                          nullptr, nullptr, status, st);
+    if (e == cudaSuccess)
+        e = txl::launch_proj_gemm(mem, M, h, L, B, w + (size_t)d * d * 2, (int)(2 * d), (int)d, (int)d,
+                                  H, d_h, M + L, 0, k, v, nullptr, status, st);
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream) {
+    if (!emb || !w_r || !r_k || K <= 0 || H <= 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
+    if (d_h != 64 || H % 4 != 0 || K % 128 != 0) return TXL_ERR_UNSUPPORTED;
+    const long long d = (long long)H * d_h;
+    if ((long long)K * d >= (1ll << 31)) return TXL_ERR_UNSUPPORTED;
+    if (!aligned16(emb) || !aligned16(w_r) || !aligned16(r_k)) return TXL_ERR_MISALIGNED;
+    const size_t nr = (size_t)K * d * 2;
+    if (overlap(r_k, nr, emb, nr) || overlap(r_k, nr, w_r, (size_t)d * d * 2)) return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    cudaError_t e = txl::launch_proj_gemm(emb, 0, emb, K, 1, w_r, (int)d, (int)d, (int)d, H, d_h, K, 1,
+                                          r_k, nullptr, nullptr, status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 
 const char* txl_status_string(int status) {
