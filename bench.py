@@ -300,6 +300,7 @@ def run_ours(args, wl: W.Workload):
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
     roll_ms = time_rolls(calls, mems, stream)
+    proj = time_projections(wl, dev, stream, peaks)
     txl.check_status()
     flops_call = wl.attn_flops()
     flops_step = flops_call * n_calls
@@ -354,6 +355,7 @@ def run_ours(args, wl: W.Workload):
         # per call: the attention kernel (+ the split combine pass) and Tail_M
         # the Tail_M roll timed alone after the timed region (in the step it
         # runs on a second stream in the gaps between attention kernels)
+        "projections": proj,
         "roofline_mem_update": {
             "kernel": "tail_copy_kernel" if wl.L >= wl.M else "tail_chain_kernel",
             "bound": "hbm",
@@ -407,6 +409,61 @@ def measured_traffic(workload):
             if hashlib.sha256(f.read()).hexdigest()[:16] != prefix:
                 return None
     return cap["bytes_per_launch"]
+
+
+def time_projections(wl, dev, stream, peaks):
+    """The layer projections that produce the attention's inputs (txl_qkv_proj:
+    q from h, k/v from memory and h; txl_r_proj), timed alone for one layer of
+    the workload in a captured graph (kernel time, not the host launch path).
+    They are not part of the timed step: the step starts from projected
+    inputs.  None when the sizes are outside the projection kernel's range."""
+    import transformer_xl_relative_attn_gb300 as txl
+
+    B, L, M, H, dh = wl.B, wl.L, wl.M, wl.H, wl.dh
+    d = H * dh
+    if dh != 64 or H % 4 or L % 128 or M % 128 or wl.dtype != "bf16":
+        return None
+    g = torch.Generator(device="cpu").manual_seed(17)
+    h = torch.randn(B, L, d, generator=g).to(device=dev, dtype=torch.bfloat16)
+    mem = torch.randn(B, M, d, generator=g).to(device=dev, dtype=torch.bfloat16)
+    w = (0.02 * torch.randn(3 * d, d, generator=g)).to(device=dev, dtype=torch.bfloat16)
+    emb = torch.randn(M + L, d, generator=g).to(device=dev, dtype=torch.bfloat16)
+    wr = (0.02 * torch.randn(d, d, generator=g)).to(device=dev, dtype=torch.bfloat16)
+    q = torch.empty(B, H, L, dh, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(B, H, M + L, dh, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    r = torch.empty(M + L, H, dh, dtype=torch.bfloat16, device=dev)
+    reps = 10
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        txl.qkv_proj(h, mem, w, H, q, k, v)
+        txl.r_proj(emb, wr, H, r)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ev[0].record()
+        for _ in range(reps):
+            txl.qkv_proj(h, mem, w, H, q, k, v)
+        ev[1].record()
+        for _ in range(reps):
+            txl.r_proj(emb, wr, H, r)
+        ev[2].record()
+    graph.replay()
+    torch.cuda.synchronize()
+    txl.check_status()
+    qkv_ms = ev[0].elapsed_time(ev[1]) / reps
+    r_ms = ev[1].elapsed_time(ev[2]) / reps
+    f_qkv = 2.0 * B * L * d * d + 2.0 * B * (M + L) * 2 * d * d
+    f_r = 2.0 * (M + L) * d * d
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {
+        "qkv_proj": {"ms": round(qkv_ms, 5), "tflops": round(f_qkv / (qkv_ms * 1e-3) / 1e12, 2),
+                     "frac": round(f_qkv / (qkv_ms * 1e-3) / 1e12 / peak, 4), "flops": f_qkv},
+        "r_proj": {"ms": round(r_ms, 5), "tflops": round(f_r / (r_ms * 1e-3) / 1e12, 2),
+                   "frac": round(f_r / (r_ms * 1e-3) / 1e12 / peak, 4), "flops": f_r},
+        "peak": peak, "peak_source": "bf16_tflops (burst: kernels timed alone)",
+        "measured": "one layer's projections, 10 back-to-back repeats in a CUDA graph",
+    }
 
 
 def time_rolls(calls, mems, stream):
