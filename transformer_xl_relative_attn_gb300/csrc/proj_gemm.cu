@@ -45,17 +45,35 @@ constexpr uint32_t TMEM_COLS = 512;     // two accumulators of BN columns
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0);
 }  // namespace pg
 
+// One GEMM of the launch: per batch row, Ta rows of source a (the memory)
+// then Tb rows of source b (current), times the problem's weights.
+struct PgProblem {
+    int Ta, Tb;     // rows per batch from source a, then source b (Ta a multiple of BM)
+    int N;          // output columns (a multiple of BN)
+    int T_out;      // rows per (batch, head) of the outputs
+    int n_rt, n_nt, tiles;
+    __nv_bfloat16* out[3];  // output column c -> tensor c / d
+};
+
 struct PgParams {
     int B;          // batch rows
-    int Ta, Tb;     // rows per batch from source a (memory) then source b (current)
     int K;          // reduction length (= d)
-    int N;          // output columns (a multiple of BN)
-    int d, H, dh;   // output column c -> tensor c / d, head (c % d) / dh, element c % dh
-    int T_out;      // rows per (batch, head) of the outputs
+    int d, H, dh;   // output column c -> head (c % d) / dh, element c % dh
     int plain;      // 1: outputs are [rows, d] row-major (no head split)
-    int n_rt, n_nt, n_tiles;
-    __nv_bfloat16* out[3];
+    int n_tiles;    // tiles of problem 0, then of problem 1
+    PgProblem pr[2];
     int* status;
+};
+
+// Host description of one projection GEMM of a launch.
+struct ProjGemm {
+    const void* a_src;  // [B, Ta, K] (memory rows) or null when Ta = 0
+    const void* b_src;  // [B, Tb, K]
+    int Ta, Tb;
+    const void* w;      // [N, K]
+    int N;
+    int T_out;
+    void* out[3];
 };
 
 struct PgShared {
@@ -68,17 +86,24 @@ struct PgShared {
     int abort;
 };
 
-// Tile w of the launch: column tile fastest, then row tile, then batch row.
-__device__ __forceinline__ void pg_tile(const PgParams& p, int w, int& b, int& t0, int& n0) {
-    const int nt = w % p.n_nt, rest = w / p.n_nt;
+// Tile w of the launch: problem 0's tiles, then problem 1's; within a
+// problem the column tile runs fastest, then the row tile, then the batch row.
+__device__ __forceinline__ int pg_tile(const PgParams& p, int w, int& b, int& t0, int& n0) {
+    const int g = w < p.pr[0].tiles ? 0 : 1;
+    const PgProblem& pr = p.pr[g];
+    if (g) w -= p.pr[0].tiles;
+    const int nt = w % pr.n_nt, rest = w / pr.n_nt;
     n0 = nt * pg::BN;
-    t0 = (rest % p.n_rt) * pg::BM;
-    b = rest / p.n_rt;
+    t0 = (rest % pr.n_rt) * pg::BM;
+    b = rest / pr.n_rt;
+    return g;
 }
 
 __global__ void __launch_bounds__(pg::NTHREADS, 1)
-proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAb,
-                 const __grid_constant__ CUtensorMap tmW, const PgParams p) {
+proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                 const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmA1,
+                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmW1,
+                 const PgParams p) {
     using namespace pg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -104,9 +129,12 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         mbar_init(&sh->drain, 1);
         sh->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmAb);
-        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmB0);
+        tma_prefetch_desc(&tmW0);
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB1);
+        tma_prefetch_desc(&tmW1);
     }
     tc_fence_before();
     __syncthreads();
@@ -121,9 +149,12 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int c = 0;  // loads issued into the ring
             for (int w = blockIdx.x; ok && w < p.n_tiles; w += gridDim.x) {
                 int b, t0, n0;
-                pg_tile(p, w, b, t0, n0);
+                const int g = pg_tile(p, w, b, t0, n0);
+                const int Ta = p.pr[g].Ta;
                 // a row tile lies wholly in one source (Ta is a multiple of BM)
-                const bool from_a = t0 < p.Ta;
+                const CUtensorMap* mA = t0 < Ta ? (g ? &tmA1 : &tmA0) : (g ? &tmB1 : &tmB0);
+                const int ta = t0 < Ta ? t0 : t0 - Ta;
+                const CUtensorMap* mW = g ? &tmW1 : &tmW0;
                 for (int k = 0; k < ksteps; ++k, ++c) {
                     const int s = c % STAGES;
                     if (c >= STAGES && !mbar_wait(&sh->empty[s], ((c / STAGES) & 1) ^ 1,
@@ -132,11 +163,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         break;
                     }
                     mbar_expect_tx(&sh->full[s], SZ_A + SZ_B);
-                    if (from_a)
-                        tma_load_3d(smem + OFF_A + s * SZ_A, &tmA, &sh->full[s], k * BK, t0, b);
-                    else
-                        tma_load_3d(smem + OFF_A + s * SZ_A, &tmAb, &sh->full[s], k * BK, t0 - p.Ta, b);
-                    tma_load_2d(smem + OFF_B + s * SZ_B, &tmW, &sh->full[s], k * BK, n0);
+                    tma_load_3d(smem + OFF_A + s * SZ_A, mA, &sh->full[s], k * BK, ta, b);
+                    tma_load_2d(smem + OFF_B + s * SZ_B, mW, &sh->full[s], k * BK, n0);
                 }
             }
             // drain: the last load into each ring slot has landed
@@ -205,7 +233,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!ok) break;
             tc_fence_after();
             int b, t0, n0;
-            pg_tile(p, w, b, t0, n0);
+            const int g = pg_tile(p, w, b, t0, n0);
+            const PgProblem& pr = p.pr[g];
             const int t = t0 + row;
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
@@ -219,13 +248,13 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 const int n = n0 + 32 * cc;
                 const int o = n / p.d, nd = n - o * p.d;
-                __nv_bfloat16* const base = o == 0 ? p.out[0] : (o == 1 ? p.out[1] : p.out[2]);
+                __nv_bfloat16* const base = o == 0 ? pr.out[0] : (o == 1 ? pr.out[1] : pr.out[2]);
                 __nv_bfloat16* dst;
                 if (p.plain) {
-                    dst = base + ((size_t)b * p.T_out + t) * p.d + nd;
+                    dst = base + ((size_t)b * pr.T_out + t) * p.d + nd;
                 } else {
                     const int head = nd / p.dh, e = nd - head * p.dh;
-                    dst = base + (((size_t)b * p.H + head) * p.T_out + t) * p.dh + e;
+                    dst = base + (((size_t)b * p.H + head) * pr.T_out + t) * p.dh + e;
                 }
                 uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -289,13 +318,13 @@ static int pg_num_sms() {
     return n;
 }
 
-// out[c / d] <- rows of [a_src; b_src] (per batch row: Ta rows of a_src, then Tb
-// rows of b_src, each row K bf16) times w^T (w: N rows of K, row-major).
-// Requires Ta, Tb multiples of 128 (Ta may be 0), K a multiple of 64, N a
-// multiple of 256, N / d <= 3.
-cudaError_t launch_proj_gemm(const void* a_src, int Ta, const void* b_src, int Tb, int B,
-                             const void* w, int N, int K, int d, int H, int dh, int T_out, int plain,
-                             void* out0, void* out1, void* out2, int* status, cudaStream_t stream) {
+// One launch of up to two projection GEMMs (ProjGemm each): out[c / d] <-
+// rows of [a_src; b_src] (per batch row: Ta rows of a_src, then Tb rows of
+// b_src, each row K bf16) times w^T (w: N rows of K, row-major).  Requires Ta,
+// Tb multiples of 128 (Ta may be 0), K a multiple of 64, N a multiple of 256,
+// N / d <= 3.
+cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
+                             int plain, int* status, cudaStream_t stream) {
     using namespace pg;
     static bool attr_set = false;
     if (!attr_set) {
@@ -304,48 +333,55 @@ cudaError_t launch_proj_gemm(const void* a_src, int Ta, const void* b_src, int T
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    CUtensorMap mA, mB, mW;
-    const cuuint32_t boxA[3] = {BK, BM, 1};
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Tb, (cuuint64_t)B};
-        const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)Tb * K * 2};
-        if (!pg_encode(&mB, b_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
-    }
-    if (Ta > 0) {
-        const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Ta, (cuuint64_t)B};
-        const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)Ta * K * 2};
-        if (!pg_encode(&mA, a_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
-    } else {
-        mA = mB;  // no memory rows: every row tile comes from b_src
-    }
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {BK, BN};
-        if (!pg_encode(&mW, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
+    if (n_gemm < 1 || n_gemm > 2) return cudaErrorInvalidValue;
+    CUtensorMap maps[2][3];  // per problem: source a, source b, weights
     PgParams p;
     p.B = B;
-    p.Ta = Ta;
-    p.Tb = Tb;
     p.K = K;
-    p.N = N;
     p.d = d;
     p.H = H;
     p.dh = dh;
-    p.T_out = T_out;
     p.plain = plain;
-    p.n_rt = (Ta + Tb) / BM;
-    p.n_nt = N / BN;
-    const long long tiles = (long long)B * p.n_rt * p.n_nt;
-    if (tiles <= 0 || tiles > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    p.n_tiles = (int)tiles;
-    p.out[0] = static_cast<__nv_bfloat16*>(out0);
-    p.out[1] = static_cast<__nv_bfloat16*>(out1);
-    p.out[2] = static_cast<__nv_bfloat16*>(out2);
     p.status = status;
+    const cuuint32_t boxA[3] = {BK, BM, 1};
+    long long total = 0;
+    for (int g = 0; g < 2; ++g) {
+        const ProjGemm& q = gm[g < n_gemm ? g : 0];
+        {
+            const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)q.Tb, (cuuint64_t)B};
+            const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)q.Tb * K * 2};
+            if (!pg_encode(&maps[g][1], q.b_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
+        }
+        if (q.Ta > 0) {
+            const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)q.Ta, (cuuint64_t)B};
+            const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)q.Ta * K * 2};
+            if (!pg_encode(&maps[g][0], q.a_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
+        } else {
+            maps[g][0] = maps[g][1];  // no memory rows: every row tile comes from b_src
+        }
+        {
+            const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)q.N};
+            const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+            const cuuint32_t box[2] = {BK, BN};
+            if (!pg_encode(&maps[g][2], q.w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        }
+        PgProblem& pr = p.pr[g];
+        pr.Ta = q.Ta;
+        pr.Tb = q.Tb;
+        pr.N = q.N;
+        pr.T_out = q.T_out;
+        pr.n_rt = (q.Ta + q.Tb) / BM;
+        pr.n_nt = q.N / BN;
+        const long long tiles = g < n_gemm ? (long long)B * pr.n_rt * pr.n_nt : 0;
+        pr.tiles = (int)(tiles > 0x7FFFFFFFll ? 0 : tiles);
+        total += tiles;
+        for (int o = 0; o < 3; ++o) pr.out[o] = static_cast<__nv_bfloat16*>(q.out[o]);
+    }
+    if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    p.n_tiles = (int)total;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(mA, mB, mW, p);
+    proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(maps[0][0], maps[0][1], maps[0][2], maps[1][0],
+                                                            maps[1][1], maps[1][2], p);
     return cudaGetLastError();
 }
 

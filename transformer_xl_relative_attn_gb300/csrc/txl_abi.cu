@@ -22,9 +22,17 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, void* out, void* workspace, int inject, int* status,
                                 cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
-cudaError_t launch_proj_gemm(const void* a_src, int Ta, const void* b_src, int Tb, int B,
-                             const void* w, int N, int K, int d, int H, int dh, int T_out, int plain,
-                             void* out0, void* out1, void* out2, int* status, cudaStream_t stream);
+struct ProjGemm {
+    const void* a_src;
+    const void* b_src;
+    int Ta, Tb;
+    const void* w;
+    int N;
+    int T_out;
+    void* out[3];
+};
+cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
+                             int plain, int* status, cudaStream_t stream);
 }  // namespace txl
 
 namespace {
@@ -228,11 +236,11 @@ int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L
     if (!status) return TXL_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned char* w = static_cast<const unsigned char*>(w_qkv);
-    cudaError_t e = txl::launch_proj_gemm(h, 0, h, L, B, w, (int)d, (int)d, (int)d, H, d_h, L, 0, q,
-                                          nullptr, nullptr, status, st);
-    if (e == cudaSuccess)
-        e = txl::launch_proj_gemm(mem, M, h, L, B, w + (size_t)d * d * 2, (int)(2 * d), (int)d, (int)d,
-                                  H, d_h, M + L, 0, k, v, nullptr, status, st);
+    // one launch: q from h and W_q; k, v from [mem; h] and the W_k, W_v rows
+    const txl::ProjGemm gm[2] = {
+        {nullptr, h, 0, L, w, (int)d, L, {q, nullptr, nullptr}},
+        {M > 0 ? mem : nullptr, h, M, L, w + (size_t)d * d * 2, (int)(2 * d), M + L, {k, v, nullptr}}};
+    cudaError_t e = txl::launch_proj_gemm(gm, 2, B, (int)d, (int)d, H, d_h, 0, status, st);
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
@@ -247,8 +255,9 @@ int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_
     if (overlap(r_k, nr, emb, nr) || overlap(r_k, nr, w_r, (size_t)d * d * 2)) return TXL_ERR_ALIAS;
     int* status = dev_status_ptr();
     if (!status) return TXL_ERR_CUDA;
-    cudaError_t e = txl::launch_proj_gemm(emb, 0, emb, K, 1, w_r, (int)d, (int)d, (int)d, H, d_h, K, 1,
-                                          r_k, nullptr, nullptr, status, static_cast<cudaStream_t>(stream));
+    const txl::ProjGemm gm = {nullptr, emb, 0, K, w_r, (int)d, K, {r_k, nullptr, nullptr}};
+    cudaError_t e = txl::launch_proj_gemm(&gm, 1, 1, (int)d, (int)d, H, d_h, 1, status,
+                                          static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
