@@ -11,6 +11,8 @@
 // GEMM, so no [mem; h] concatenation is formed, and the epilogue writes each
 // 64-column head slice straight into the head-split layout.
 //
+// One launch may carry two GEMMs (q from h, and k|v from [mem; h]) dealt from
+// one tile list, so the smaller one does not leave a partial round of its own.
 // One CTA per SM walks output tiles of 128 rows x 256 columns; K (= d) is
 // streamed in 64-element steps through a 4-stage TMA ring (A tile 16 KB, B tile
 // 32 KB, 128B swizzle).  Roles (256 threads): warp 0 lane 0 issues the TMA
