@@ -52,7 +52,10 @@
 //
 // TMEM columns: O0 0-63, O1 64-127, AC0 128-191, AC1 192-255, position ring
 // 256-511.  Shared memory: (q+u)c,(q+v)c x2 (each first filled with the raw q
-// tile by TMA, then rewritten in place), P x2, K/V ring, R ring.
+// tile by TMA, then rewritten in place), P x2, K/V ring, R ring.  A group's P
+// buffer is also the scratch of its per-row shift: after the group's previous
+// P V finished and before the new P is written, each warp moves its rows'
+// band windows through its 4 KB quarter of it.
 //
 // Ordering facts relied on: tcgen05.mma operations from one thread execute in
 // issue order, and a tcgen05.commit arrives only when every MMA issued before
@@ -84,13 +87,9 @@ constexpr int RING = 4;        // position slots held in TMEM
 #ifndef TXL_PREFETCH
 #define TXL_PREFETCH 2
 #endif
-#ifndef TXL_FMA_STAGES
-#define TXL_FMA_STAGES 1
-#endif
 constexpr int KV_STAGES = TXL_KV_STAGES;  // K/V ring: each stage holds two key tiles
 constexpr int R_STAGES = TXL_R_STAGES;    // R ring: each box holds two position slots
 constexpr int PREFETCH = TXL_PREFETCH;    // K/V stages warmed into L2 ahead of their load
-constexpr int FMA_STAGES = TXL_FMA_STAGES;  // relative-shift stages done on the FMA pipe
 static_assert(KV_STAGES >= 2 && R_STAGES >= 2, "the MMA order needs two stages of each ring");
 constexpr int NTHREADS = 384;
 
@@ -240,6 +239,47 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     return *reinterpret_cast<float2*>(&r);
 }
 
+// Per-row shift through shared memory.  A thread holds 64 consecutive band
+// columns w0[0..31] | w1[0..31] of its row and needs window columns o .. o+31
+// (o = 31 - lane).  It writes window column k to position k - o when k >= o
+// and window column 32 + k to position k + 32 - o otherwise (for each k
+// exactly one of the two lands in 0..31), then reads positions 0..31 back in
+// order.  Position x of lane l is word 32 x + l of the warp's 4 KB scratch:
+// each store and load of the warp touches 32 distinct banks, and a lane only
+// ever touches its own words.  `base` is the lane's word of position 0 minus
+// 128 o bytes.
+template <int K>
+__device__ __forceinline__ void st_shift_pair(int o, uint32_t base, uint32_t w0k, uint32_t w1k) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.le.s32 q, %0, %1;\n\t"
+        "@q st.shared.b32 [%2+%3], %4;\n\t"
+        "@!q st.shared.b32 [%2+%5], %6;\n\t}"
+        ::"r"(o), "n"(K), "r"(base), "n"(128 * K), "r"(w0k), "n"(4096 + 128 * K), "r"(w1k)
+        : "memory");
+}
+template <int K>
+__device__ __forceinline__ float ld_shift(uint32_t base) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(base), "n"(128 * K) : "memory");
+    return v;
+}
+template <int K>
+__device__ __forceinline__ void st_shift_all(int o, uint32_t base, const uint32_t (&w0)[32],
+                                             const uint32_t (&w1)[32]) {
+    if constexpr (K < 32) {
+        st_shift_pair<K>(o, base, w0[K], w1[K]);
+        st_shift_all<K + 1>(o, base, w0, w1);
+    }
+}
+template <int K>
+__device__ __forceinline__ void ld_shift_all(uint32_t base, float (&win)[32]) {
+    if constexpr (K < 32) {
+        win[K] = ld_shift<K>(base);
+        ld_shift_all<K + 1>(base, win);
+    }
+}
+
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
@@ -313,6 +353,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t col_ac = COL_AC + 64 * grp;
         const uint32_t p_tile = s_base + OFF_P + grp * SZ_Q;
+        // this warp's quarter of the group's P buffer doubles as the row-shift
+        // scratch T[pos][lane] (word pos * 32 + lane) before P is written
+        const uint32_t t_ld = p_tile + wq * 4096 + 4 * lane;
+        const uint32_t t_st = t_ld - 128u * (uint32_t)(31 - lane);
         const float qscale = p.scale_log2;
 
         // (q+u)c (group 0) or (q+v)c (group 1) of an item, rounded to bf16, in
@@ -395,6 +439,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     issue_q(nxt, (k + 1) & 1);
                     next_issued = true;
                 }
+                if (it_g > 0) {
+                    // the group's previous P V must be done before its P buffer
+                    // is reused (shift scratch, then P) or O is rescaled
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh->pv_done[grp], (it_g - 1) & 1,
+                                                           kDevTimeoutSoftmax, abort, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
                 const int j0 = (cur.t0 + t) * BN;
                 const bool need_mask = (j0 + BN - 1) > (p.M + cur.i0);
                 const int jlim = p.M + i - j0;  // keys jj > jlim are masked
@@ -419,30 +471,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         tc_fence_before();
                         warp_arrive(&sh->s_free[grp]);
                     }
-                    float win[64];
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        win[x] = __uint_as_float(w0[x]);
-                        win[32 + x] = __uint_as_float(w1[x]);
-                    }
-                    // per-row shift by o = 31 - lane: win[x] <- win[x + o], as a
-                    // barrel of selects.  The last FMA_STAGES stages run on the FMA pipe
-                    // (a*t + b*(1-t) with t in {0, 1} is exact for finite a, b),
-                    // which is otherwise idle while the selects fill the ALU.
-                    const int o = 31 - lane;
-#pragma unroll
-                    for (int sb = 16; sb >= (1 << FMA_STAGES); sb >>= 1) {
-                        const bool take = (o & sb) != 0;
-#pragma unroll
-                        for (int x = 0; x < 32 + sb - 1; ++x) win[x] = take ? win[x + sb] : win[x];
-                    }
-#pragma unroll
-                    for (int sb = (1 << FMA_STAGES) >> 1; sb >= 1; sb >>= 1) {
-                        const float tk = (o & sb) ? 1.f : 0.f, nt = 1.f - tk;
-#pragma unroll
-                        for (int x = 0; x < 32 + sb - 1; ++x)
-                            win[x] = __fmaf_rn(win[x + sb], tk, __fmul_rn(win[x], nt));
-                    }
+                    float win[32];
+                    st_shift_all<0>(31 - lane, t_st, w0, w1);
+                    ld_shift_all<0>(t_ld, win);
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
                         const float2 s2 =
@@ -467,14 +498,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 // -inf): exponentiate against 0 instead, so every p is 0, not NaN.
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 const float alpha = ex2(m_run - m_use);
-                if (it_g > 0) {
-                    // the group's previous P V must be done before O is rescaled
-                    // or its P buffer rewritten
-                    ok = __all_sync(0xffffffffu, mbar_wait(&sh->pv_done[grp], (it_g - 1) & 1,
-                                                           kDevTimeoutSoftmax, abort, p.status));
-                    if (!ok) break;
-                    tc_fence_after();
-                }
                 if (seen > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -488,6 +511,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                     tmem_wait_st();
                 }
+                __syncwarp();  // every lane's scratch reads precede the P rows
                 const float2 negm = make_float2(-m_use, -m_use);
                 float2 rs = make_float2(0.f, 0.f);
 #pragma unroll
