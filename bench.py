@@ -374,8 +374,15 @@ def run_ours(args, wl: W.Workload):
     }
 
     if not args.no_e2e:
-        result["e2e"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch,
-                                    flops_step, ws)
+        if wl.dh == 64 and wl.dtype == "bf16" and wl.H % 4 == 0 and wl.L % 128 == 0 and wl.M % 128 == 0:
+            result["e2e"] = measure_e2e_stack(args, wl, dev, flops_step, ws)
+            # the attention calls alone through the host: q, k, v, h of every
+            # call copied in, every output copied out
+            result["e2e_attn_calls"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb,
+                                                   scratch, flops_step, ws)
+        else:
+            result["e2e"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch,
+                                        flops_step, ws)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"], result["parity"] = cpu_baseline_and_parity(wl, calls, rks, u, vb)
     if rank == 0:
@@ -552,6 +559,90 @@ def measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch, flops_
     return {"value": round(ws * flops_step * steps / el / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1e3 * el / steps, 3)}
+
+
+def build_stack(wl, dev, stream):
+    """An AttnStack of the workload's layers with the library's own
+    projections: W_q, W_k, W_v stacked in the nn.Linear layout, r_k of every
+    layer projected once by txl_r_proj from the sinusoid of distances
+    M+L-1 .. 0, layer 0's memory in rows, the others in heads."""
+    import transformer_xl_relative_attn_gb300 as txl
+    bf = torch.bfloat16
+    p = W.make_params(wl)
+    H = wl.H
+    with torch.cuda.stream(stream):
+        w_qkv = [torch.cat([lw.W_q.t(), lw.W_k.t(), lw.W_v.t()]).contiguous().to(dev, bf) for lw in p.layers]
+        emb = W.sinusoid(torch.arange(wl.M + wl.L - 1, -1, -1), wl.d).to(dev, bf)
+        r_k = [txl.r_proj(emb, lw.W_r.t().contiguous().to(dev, bf), H, stream=stream) for lw in p.layers]
+        u = [p.u.to(dev, bf)] * wl.layers
+        vb = [p.v.to(dev, bf)] * wl.layers
+        m0 = W.initial_memories(wl)
+        mems = [m0[0].to(dev, bf)] + [W._split_heads(m, H).to(dev, bf) for m in m0[1:]]
+    stream.synchronize()
+    return txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, wl.L, stream=stream)
+
+
+def measure_e2e_stack(args, wl, dev, flops_step, ws):
+    """The metric end to end through the segment-level public API
+    (AttnStack.run_segment: projections, Tail_M rolls and attention of every
+    layer in libtxl.so).  Each step copies every segment's layer-0 hidden
+    states [B, L, d] from pinned host memory and reads every segment's last
+    attention output back; segment s+1's upload overlaps segment s's layers
+    and segment s's download overlaps segment s+1's.  The step's work is the
+    bench step's 36 attention calls and rolls plus the 36 projections; the
+    value counts the attention FLOPs only."""
+    import transformer_xl_relative_attn_gb300 as txl
+    stream = torch.cuda.Stream(device=dev)
+    stack = build_stack(wl, dev, stream)
+    bf = torch.bfloat16
+    S = wl.segments
+    h_host = [W.segment_input(wl, s).to(bf).pin_memory() for s in range(S)]
+    h_dev = [torch.empty(h.shape, dtype=bf, device=dev) for h in h_host]
+    o_shape = (wl.B, wl.H, wl.L, wl.dh)
+    o_dev = [torch.empty(o_shape, dtype=bf, device=dev) for _ in range(S)]
+    o_host = [torch.empty(o_shape, dtype=bf).pin_memory() for _ in range(S)]
+    h2d = sum(h.numel() * h.element_size() for h in h_host)
+    d2h = sum(o.numel() * o.element_size() for o in o_host)
+    steps = max(3, min(args.steps, 10))
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def one():
+        arrived = [torch.cuda.Event() for _ in range(S)]
+        with torch.cuda.stream(up):
+            for s in range(S):
+                h_dev[s].copy_(h_host[s], non_blocking=True)
+                arrived[s].record(up)
+        for s in range(S):
+            stream.wait_event(arrived[s])
+            stack.run_segment(h_dev[s], out=o_dev[s])
+            written = torch.cuda.Event()
+            written.record(stream)
+            down.wait_event(written)
+            with torch.cuda.stream(down):
+                o_host[s].copy_(o_dev[s], non_blocking=True)
+        # the next step's copies overwrite these buffers
+        for st in (stream, down):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            up.wait_event(ev)
+            stream.wait_event(ev)
+
+    one()
+    torch.cuda.synchronize()
+    txl.check_status()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = reduce_max(time.perf_counter() - t0, ws)
+    txl.check_status()
+    return {"value": round(ws * flops_step * steps / el / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(1e3 * el / steps, 3),
+            "tokens_per_s": round(ws * wl.B * wl.L * S * steps / el, 1),
+            "api": "AttnStack.run_segment per segment (txl_qkv_proj_ex, txl_mem_update, txl_attn_fwd "
+                   "per layer); host hidden states in, last layer's attention output out"}
 
 
 def cpu_baseline_and_parity(wl, calls, rks, u, vb):

@@ -166,6 +166,21 @@ int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
  */
 int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L, int M, int H,
                  int d_h, void* q, void* k, void* v, void* stream);
+
+/*
+ * txl_qkv_proj_ex: txl_qkv_proj with the layout of h and mem chosen per
+ * argument.  TXL_LAYOUT_ROWS: [B, T, d] as above.  TXL_LAYOUT_HEADS:
+ * [B, H, T, d_h], the layout txl_attn_fwd writes its output in, so a stack of
+ * layers feeds one layer's attention output (and the memory rolled from it)
+ * straight into the next layer's projections; row t of head h is columns
+ * h*d_h .. h*d_h+d_h-1 of the row-major view.  Other layouts return
+ * TXL_ERR_INVALID_ARG; sizes, alignment and aliasing as for txl_qkv_proj.
+ */
+#define TXL_LAYOUT_ROWS 0
+#define TXL_LAYOUT_HEADS 1
+int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout,
+                    const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
+                    void* v, void* stream);
 int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream);
 
 /*

@@ -7,16 +7,17 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
     mem_update                                    Tail_M memory roll, in place
     qkv_proj, r_proj                              head-split input projections (tensor cores)
     sync_status, check_status                     device status word
-    SegmentDriver                                 multi-segment, multi-layer driver
+    SegmentDriver                                 multi-segment, multi-layer driver (caller's projections)
+    AttnStack                                     the same with the library's projections
 """
 from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
                    attn_workspace_bytes,
                    check_status, debug_inject, header_functions, load, mem_update, qkv_proj, r_proj,
                    status_string,
                    sync_status, version, LIB_PATH)
-from .driver import SegmentDriver
+from .driver import AttnStack, SegmentDriver
 
 __all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
            "attn_workspace_bytes",
            "check_status", "debug_inject", "header_functions", "load", "mem_update", "qkv_proj", "r_proj",
-           "status_string", "sync_status", "version", "SegmentDriver", "LIB_PATH"]
+           "status_string", "sync_status", "version", "SegmentDriver", "AttnStack", "LIB_PATH"]

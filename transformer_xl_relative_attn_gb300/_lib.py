@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_fwd_noalloc.restype = i
         lib.txl_qkv_proj.argtypes = [vp] * 3 + [i] * 5 + [vp] * 4
         lib.txl_qkv_proj.restype = i
+        lib.txl_qkv_proj_ex.argtypes = [vp, i, vp, i, vp] + [i] * 5 + [vp] * 4
+        lib.txl_qkv_proj_ex.restype = i
         lib.txl_r_proj.argtypes = [vp, vp] + [i] * 3 + [vp, vp]
         lib.txl_r_proj.restype = i
         lib.txl_attn_workspace_bytes.argtypes = [i] * 6
@@ -191,17 +193,33 @@ def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
 
 
 def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
-    """txl_qkv_proj: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
-    h [B, L, d], mem [B, M, d] (M may be 0), w_qkv [3d, d]; bf16 CUDA tensors.
-    Returns (q [B, H, L, d_h], k, v [B, H, M+L, d_h])."""
-    if h.dim() != 3 or mem.dim() != 3:
-        raise ValueError("h must be [B, L, d] and mem [B, M, d]")
-    B, L, d = h.shape
-    M = mem.shape[1]
+    """txl_qkv_proj_ex: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
+    h is [B, L, d] (rows) or [B, H, L, d_h] (heads: an attention output),
+    mem likewise [B, M, d] or [B, H, M, d_h] (M may be 0); w_qkv [3d, d]; bf16
+    CUDA tensors.  Returns (q [B, H, L, d_h], k, v [B, H, M+L, d_h])."""
+    if h.dim() == 3:
+        B, L, d = h.shape
+        h_layout = 0
+    elif h.dim() == 4:
+        B, Hh, L, dh_ = h.shape
+        if Hh != H:
+            raise ValueError("h in the heads layout must have H heads")
+        d = H * dh_
+        h_layout = 1
+    else:
+        raise ValueError("h must be [B, L, d] or [B, H, L, d_h]")
     dh = d // H
-    _need(h, "h", (B, L, d), torch.bfloat16)
+    if mem.dim() == 3:
+        M = mem.shape[1]
+        mem_layout, mem_shape = 0, (B, M, d)
+    elif mem.dim() == 4:
+        M = mem.shape[2]
+        mem_layout, mem_shape = 1, (B, H, M, dh)
+    else:
+        raise ValueError("mem must be [B, M, d] or [B, H, M, d_h]")
+    _need(h, "h", (B, L, d) if h_layout == 0 else (B, H, L, dh), torch.bfloat16)
     if M > 0:
-        _need(mem, "mem", (B, M, d), torch.bfloat16)
+        _need(mem, "mem", mem_shape, torch.bfloat16)
     _need(w_qkv, "w_qkv", (3 * d, d), torch.bfloat16)
     if q is None:
         q = torch.empty((B, H, L, dh), dtype=torch.bfloat16, device=h.device)
@@ -212,10 +230,11 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
     _need(q, "q", (B, H, L, dh), torch.bfloat16)
     _need(k, "k", (B, H, M + L, dh), torch.bfloat16)
     _need(v, "v", (B, H, M + L, dh), torch.bfloat16)
-    rc = load().txl_qkv_proj(h.data_ptr(), mem.data_ptr() if M > 0 else 0, w_qkv.data_ptr(), B, L, M, H,
-                             dh, q.data_ptr(), k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
+    rc = load().txl_qkv_proj_ex(h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
+                                w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                _stream(stream, h.device))
     if rc != 0:
-        raise TxlError(rc, "txl_qkv_proj")
+        raise TxlError(rc, "txl_qkv_proj_ex")
     return q, k, v
 
 

@@ -26,9 +26,19 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "proj_gemm.h"
 #include "txl_device.cuh"
 
 namespace txl {
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 
 namespace pg {
 constexpr int BM = 128;     // rows per tile (TMEM lanes)
@@ -65,17 +75,6 @@ struct PgParams {
     int n_tiles;    // tiles of problem 0, then of problem 1
     PgProblem pr[2];
     int* status;
-};
-
-// Host description of one projection GEMM of a launch.
-struct ProjGemm {
-    const void* a_src;  // [B, Ta, K] (memory rows) or null when Ta = 0
-    const void* b_src;  // [B, Tb, K]
-    int Ta, Tb;
-    const void* w;      // [N, K]
-    int N;
-    int T_out;
-    void* out[3];
 };
 
 struct PgShared {
@@ -165,7 +164,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                         break;
                     }
                     mbar_expect_tx(&sh->full[s], SZ_A + SZ_B);
-                    tma_load_3d(smem + OFF_A + s * SZ_A, mA, &sh->full[s], k * BK, ta, b);
+                    tma_load_4d(smem + OFF_A + s * SZ_A, mA, &sh->full[s], 0, ta, k, b);
                     tma_load_2d(smem + OFF_B + s * SZ_B, mW, &sh->full[s], k * BK, n0);
                 }
             }
@@ -303,7 +302,7 @@ static bool pg_encode(CUtensorMap* map, const void* base, int rank, const cuuint
                       const cuuint64_t* strides, const cuuint32_t* box) {
     PgEncodeFn fn = pg_encode_fn();
     if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -320,11 +319,7 @@ static int pg_num_sms() {
     return n;
 }
 
-// One launch of up to two projection GEMMs (ProjGemm each): out[c / d] <-
-// rows of [a_src; b_src] (per batch row: Ta rows of a_src, then Tb rows of
-// b_src, each row K bf16) times w^T (w: N rows of K, row-major).  Requires Ta,
-// Tb multiples of 128 (Ta may be 0), K a multiple of 64, N a multiple of 256,
-// N / d <= 3.
+// (declared in proj_gemm.h)
 cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
                              int plain, int* status, cudaStream_t stream) {
     using namespace pg;
@@ -345,19 +340,23 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     p.dh = dh;
     p.plain = plain;
     p.status = status;
-    const cuuint32_t boxA[3] = {BK, BM, 1};
+    // Both layouts as one 4-D view (element, row t, 64-column chunk k, batch
+    // row b), so the kernel loads chunk k of rows t0.. with coordinates
+    // (0, t0, k, b) either way.
+    auto encode_src = [&](CUtensorMap* map, const void* src, int T, int heads) {
+        const cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)(K / BK), (cuuint64_t)B};
+        const cuuint64_t row = heads ? (cuuint64_t)BK * 2 : (cuuint64_t)K * 2;
+        const cuuint64_t chunk = heads ? (cuuint64_t)T * BK * 2 : (cuuint64_t)BK * 2;
+        const cuuint64_t strides[3] = {row, chunk, (cuuint64_t)T * K * 2};
+        const cuuint32_t box[4] = {BK, BM, 1, 1};
+        return pg_encode(map, src, 4, dims, strides, box);
+    };
     long long total = 0;
     for (int g = 0; g < 2; ++g) {
         const ProjGemm& q = gm[g < n_gemm ? g : 0];
-        {
-            const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)q.Tb, (cuuint64_t)B};
-            const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)q.Tb * K * 2};
-            if (!pg_encode(&maps[g][1], q.b_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
-        }
+        if (!encode_src(&maps[g][1], q.b_src, q.Tb, q.b_heads)) return cudaErrorInvalidValue;
         if (q.Ta > 0) {
-            const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)q.Ta, (cuuint64_t)B};
-            const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)q.Ta * K * 2};
-            if (!pg_encode(&maps[g][0], q.a_src, 3, dims, strides, boxA)) return cudaErrorInvalidValue;
+            if (!encode_src(&maps[g][0], q.a_src, q.Ta, q.a_heads)) return cudaErrorInvalidValue;
         } else {
             maps[g][0] = maps[g][1];  // no memory rows: every row tile comes from b_src
         }

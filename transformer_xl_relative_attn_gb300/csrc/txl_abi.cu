@@ -6,6 +6,7 @@
 #include <mutex>
 #include <cuda_runtime.h>
 
+#include "proj_gemm.h"
 #include "txl_attn.h"
 #include "txl_device.cuh"
 
@@ -22,17 +23,7 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, void* out, void* workspace, int inject, int* status,
                                 cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
-struct ProjGemm {
-    const void* a_src;
-    const void* b_src;
-    int Ta, Tb;
-    const void* w;
-    int N;
-    int T_out;
-    void* out[3];
-};
-cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
-                             int plain, int* status, cudaStream_t stream);
+
 }  // namespace txl
 
 namespace {
@@ -212,7 +203,16 @@ int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
 
 int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L, int M, int H,
                  int d_h, void* q, void* k, void* v, void* stream) {
+    return txl_qkv_proj_ex(h, TXL_LAYOUT_ROWS, mem, TXL_LAYOUT_ROWS, w_qkv, B, L, M, H, d_h, q, k, v,
+                           stream);
+}
+
+int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout,
+                    const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
+                    void* v, void* stream) {
     if (!h || !w_qkv || !q || !k || !v || (M > 0 && !mem)) return TXL_ERR_INVALID_ARG;
+    const auto layout_ok = [](int l) { return l == TXL_LAYOUT_ROWS || l == TXL_LAYOUT_HEADS; };
+    if (!layout_ok(h_layout) || !layout_ok(mem_layout)) return TXL_ERR_INVALID_ARG;
     if (B <= 0 || L <= 0 || M < 0 || H <= 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
     if (d_h != 64 || H % 4 != 0 || L % 128 != 0 || M % 128 != 0) return TXL_ERR_UNSUPPORTED;
     const long long d = (long long)H * d_h;
@@ -237,9 +237,11 @@ int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned char* w = static_cast<const unsigned char*>(w_qkv);
     // one launch: q from h and W_q; k, v from [mem; h] and the W_k, W_v rows
+    const int hh = h_layout == TXL_LAYOUT_HEADS, mh = mem_layout == TXL_LAYOUT_HEADS;
     const txl::ProjGemm gm[2] = {
-        {nullptr, h, 0, L, w, (int)d, L, {q, nullptr, nullptr}},
-        {M > 0 ? mem : nullptr, h, M, L, w + (size_t)d * d * 2, (int)(2 * d), M + L, {k, v, nullptr}}};
+        {nullptr, h, 0, L, 0, hh, w, (int)d, L, {q, nullptr, nullptr}},
+        {M > 0 ? mem : nullptr, h, M, L, mh, hh, w + (size_t)d * d * 2, (int)(2 * d), M + L,
+         {k, v, nullptr}}};
     cudaError_t e = txl::launch_proj_gemm(gm, 2, B, (int)d, (int)d, H, d_h, 0, status, st);
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
@@ -255,7 +257,7 @@ int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_
     if (overlap(r_k, nr, emb, nr) || overlap(r_k, nr, w_r, (size_t)d * d * 2)) return TXL_ERR_ALIAS;
     int* status = dev_status_ptr();
     if (!status) return TXL_ERR_CUDA;
-    const txl::ProjGemm gm = {nullptr, emb, 0, K, w_r, (int)d, K, {r_k, nullptr, nullptr}};
+    const txl::ProjGemm gm = {nullptr, emb, 0, K, 0, 0, w_r, (int)d, K, {r_k, nullptr, nullptr}};
     cudaError_t e = txl::launch_proj_gemm(&gm, 1, 1, (int)d, (int)d, H, d_h, 1, status,
                                           static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;

@@ -99,3 +99,117 @@ class SegmentDriver:
             m.copy_(s)
         torch.cuda.synchronize(self.mems[0].device)  # later rolls see the restored memories
         self.segments_done = int(sd.get("segments_done", 0))
+
+
+def _roll(mem: torch.Tensor, h: torch.Tensor, stream) -> None:
+    """Tail_M roll of one memory with the layer input h, in either layout:
+    rows ([B, M, d] with [B, L, d]) or heads ([B, H, M, d_h] with
+    [B, H, L, d_h], rolled as B*H independent rows of d_h elements)."""
+    if mem.dim() == 4:
+        B, H, M, dh = mem.shape
+        _lib.mem_update(mem.view(B * H, M, dh), h.view(B * H, h.shape[2], dh), stream=stream)
+    else:
+        _lib.mem_update(mem, h, stream=stream)
+
+
+class AttnStack:
+    """A stack of relative-attention layers over per-layer recurrence
+    memories, every step in libtxl.so: for each segment and layer n
+
+        q, k, v = txl_qkv_proj_ex(h, mems[n], W_qkv[n])     tensor-core projections
+        txl_mem_update(mems[n], h)                           Tail_M, in place
+        h = txl_attn_fwd(q, k, v, r_k[n], u[n], v[n])        fused attention
+
+    ("Transformer-XL模型 核心源码阅读笔记", RelPartialLearnableMultiHeadAttn.forward
+    and MemTransformerLM._update_mems; "Transformer-XL" notes, sections
+    "Batched Tensor Contract" and "Segment-Level Recurrence").  Each layer's
+    attention output is the next layer's input, kept in the heads layout
+    [B, H, L, d_h] that the attention writes and the projections read; the
+    output projection, residual, layer norm and feed-forward of a full layer
+    are not part of this stack.  Layer 0's input arrives as rows [B, L, d];
+    so layer 0's memory is rows [B, M, d] and every other memory is heads
+    [B, H, M, d_h].  r_k[n] ([M+L, H, d_h]) depends on M and L only, so it is
+    projected once, by the caller (txl_r_proj).
+
+    The roll of mems[n] reads h after its projection has read mems[n]; all
+    launches go to one stream, which orders every dependency of the
+    recurrence.  q, k and v are one set of buffers reused by every layer; each
+    layer's output has its own buffer (the next layer's input and the source
+    of its memory roll).
+    """
+
+    def __init__(self, w_qkv: Sequence[torch.Tensor], r_k: Sequence[torch.Tensor],
+                 u: Sequence[torch.Tensor], v_bias: Sequence[torch.Tensor],
+                 mems: Sequence[torch.Tensor], scale: float, n_head: int, seg_len: int,
+                 stream: torch.cuda.Stream | None = None):
+        n = len(mems)
+        if not (len(w_qkv) == len(r_k) == len(u) == len(v_bias) == n) or n == 0:
+            raise ValueError("need one weight, r_k, u, v and memory per layer")
+        m0 = mems[0]
+        if m0.dim() != 3:
+            raise ValueError("layer 0's memory must be rows [B, M, d]")
+        B, M, d = m0.shape
+        H = n_head
+        if d % H:
+            raise ValueError("d must be a multiple of n_head")
+        dh = d // H
+        for m in mems[1:]:
+            if m.shape != (B, H, M, dh):
+                raise ValueError("memories of layers >= 1 must be heads [B, H, M, d_h]")
+        for m in mems:
+            if not (m.is_cuda and m.is_contiguous() and m.dtype == torch.bfloat16):
+                raise ValueError("memories must be contiguous bf16 CUDA tensors")
+        self.w_qkv, self.r_k, self.u, self.v_bias = list(w_qkv), list(r_k), list(u), list(v_bias)
+        self.mems = list(mems)
+        self.scale, self.H, self.L = float(scale), H, int(seg_len)
+        self.B, self.M, self.d, self.dh = B, M, d, dh
+        dev = m0.device
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        L = self.L
+        self.q = torch.empty((B, H, L, dh), **bf)
+        self.k = torch.empty((B, H, M + L, dh), **bf)
+        self.v = torch.empty((B, H, M + L, dh), **bf)
+        self.outs = [torch.empty((B, H, L, dh), **bf) for _ in range(n)]
+        self.segments_done = 0
+
+    @property
+    def n_layers(self) -> int:
+        return len(self.mems)
+
+    def run_segment(self, h0: torch.Tensor, trace: list | None = None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+        """One segment through every layer; h0 is [B, L, d] bf16 on the device.
+        Returns the last layer's attention output [B, H, L, d_h]: ``out`` if
+        given, else a buffer of the stack that the next segment overwrites.
+        With ``trace`` (tests), appends per layer the inputs each kernel saw
+        and what it wrote."""
+        if h0.shape != (self.B, self.L, self.d):
+            raise ValueError(f"h0 must be [{self.B}, {self.L}, {self.d}]")
+        h = h0
+        with torch.cuda.stream(self.stream):
+            for n, mem in enumerate(self.mems):
+                rec = None
+                if trace is not None:
+                    rec = {"n": n, "h": h.clone(), "mem": mem.clone()}
+                _lib.qkv_proj(h, mem, self.w_qkv[n], self.H, q=self.q, k=self.k, v=self.v,
+                              stream=self.stream)
+                _roll(mem, h, self.stream)
+                dst = out if (out is not None and n == len(self.mems) - 1) else self.outs[n]
+                o = _lib.attn_fwd(self.q, self.k, self.v, self.r_k[n], self.u[n], self.v_bias[n],
+                                  self.scale, out=dst, stream=self.stream)
+                if rec is not None:
+                    rec.update(q=self.q.clone(), k=self.k.clone(), v=self.v.clone(), out=o.clone())
+                    trace.append(rec)
+                h = o
+        self.segments_done += 1
+        return h
+
+    def state_dict(self) -> dict:
+        """The per-layer memories (checkpoint/resume)."""
+        return {"mems": [m.detach().clone() for m in self.mems], "segments_done": self.segments_done}
+
+    def load_state_dict(self, sd: dict) -> None:
+        for m, s in zip(self.mems, sd["mems"]):
+            m.copy_(s)
+        self.segments_done = int(sd.get("segments_done", 0))
