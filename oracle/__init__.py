@@ -75,6 +75,12 @@ def _load():
                                             ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                             dp, dp, ip, ctypes.c_int, ctypes.c_int]
             lib.oracle_attn_f64.restype = ctypes.c_int
+            lib.oracle_attn_f64_ex.argtypes = [dp, dp, dp, dp, dp, dp,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_int, ctypes.c_int,
+                                               dp, dp, ip, ctypes.c_int, ctypes.c_int]
+            lib.oracle_attn_f64_ex.restype = ctypes.c_int
             lib.oracle_num_cores.argtypes = []
             lib.oracle_num_cores.restype = ctypes.c_int
             _lib = lib
@@ -99,13 +105,15 @@ def num_cores() -> int:
 
 
 def attn(q, k, v, r_k, u, vb, scale: float, pairs=None, want_scores: bool = False,
-         nthreads: int = 0):
+         nthreads: int = 0, same_length: bool = False, mem_len: int | None = None):
     """Relative attention forward in fp64.
 
     q [B,H,L,dh]; k, v [B,H,M+L,dh]; r_k [M+L,H,dh] (row r <-> distance
     M+L-1-r); u, vb [H,dh].  ``pairs`` optionally lists flat b*H+h indices to
     compute (other rows of the result are NaN).  Returns ``out`` [B,H,L,dh]
     or ``(out, scores)`` with scores [B,H,L,M+L] (-inf where masked).
+    ``same_length`` adds the source notes' lower mask (every query sees the
+    same number of keys) for the configured ``mem_len`` (default: M).
     """
     q, k, v, r_k, u, vb = (_f64(t) for t in (q, k, v, r_k, u, vb))
     B, H, L, dh = q.shape
@@ -125,9 +133,10 @@ def attn(q, k, v, r_k, u, vb, scale: float, pairs=None, want_scores: bool = Fals
         npairs = int(parr.size)
     else:
         parr, pp, npairs = None, None, 0
-    rc = _load().oracle_attn_f64(
+    rc = _load().oracle_attn_f64_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(r_k), _ptr(u), _ptr(vb),
-        B, H, L, M, dh, float(scale), _ptr(out),
+        B, H, L, M, dh, float(scale), int(bool(same_length)), int(M if mem_len is None else mem_len),
+        _ptr(out),
         _ptr(scores) if scores is not None else None,
         pp, npairs, int(nthreads))
     if rc < 0:

@@ -16,6 +16,13 @@
  *      p = j - M, memory keys p < 0 are all visible and current keys are
  *      visible when p <= i);
  *
+ *   with same_length (source-reading notes, MemTransformerLM._forward: every
+ *   query attends over the same number of keys), the mask adds the lower
+ *   triangle tril(ones, -mask_shift_len) to triu(ones, 1+mlen), where
+ *   mask_len = klen - mem_len and mask_shift_len = qlen - mask_len when
+ *   mask_len > 0, else qlen; so additionally
+ *     allow(i, j)  requires  j - i > -mask_shift_len;
+ *
  *   dist(i, j) = M + i - j, the relative distance query minus key, and the
  *   position row used is r_k[M+L-1-dist] because the position sequence runs
  *   from M+L-1 down to 0 ("Transformer-XL模型 核心源码阅读笔记", section
@@ -46,6 +53,8 @@
 typedef struct {
     const double *q, *k, *v, *r, *u, *vb;
     int B, H, L, M, dh;
+    int same_length;
+    int mask_shift_len; /* used when same_length */
     double scale;
     double *out;
     double *scores;
@@ -77,7 +86,8 @@ static int attn_pair(const oracle_job *J, int bh) {
         const double *qi = Q + (size_t)i * dh;
         double m = -INFINITY;
         for (int j = 0; j < K; ++j) {
-            int allow = (j <= M + i);
+            int allow = (j - i <= M);
+            if (J->same_length && !(j - i > -J->mask_shift_len)) allow = 0;
             if (!allow) {
                 s[j] = -INFINITY;
                 continue;
@@ -143,14 +153,21 @@ int oracle_num_cores(void) {
  * nthreads <= 0 uses every online core.  Returns the thread count used,
  * or a negative value on bad arguments / allocation failure.
  */
-int oracle_attn_f64(const double *q, const double *k, const double *v,
-                    const double *r_k, const double *u, const double *vb,
-                    int B, int H, int L, int M, int dh, double scale,
-                    double *out, double *scores, const int *pairs, int npairs,
-                    int nthreads) {
+int oracle_attn_f64_ex(const double *q, const double *k, const double *v,
+                       const double *r_k, const double *u, const double *vb,
+                       int B, int H, int L, int M, int dh, double scale,
+                       int same_length, int mem_len,
+                       double *out, double *scores, const int *pairs, int npairs,
+                       int nthreads) {
     if (B <= 0 || H <= 0 || L <= 0 || M < 0 || dh <= 0) return -1;
     if (!q || !k || !v || !r_k || !u || !vb || !out) return -1;
+    if (same_length && mem_len < 0) return -1;
     oracle_job J;
+    {
+        const int klen = M + L, mask_len = klen - mem_len;
+        J.same_length = same_length != 0;
+        J.mask_shift_len = mask_len > 0 ? L - mask_len : L;
+    }
     J.q = q; J.k = k; J.v = v; J.r = r_k; J.u = u; J.vb = vb;
     J.B = B; J.H = H; J.L = L; J.M = M; J.dh = dh;
     J.scale = scale; J.out = out; J.scores = scores;
@@ -173,4 +190,14 @@ int oracle_attn_f64(const double *q, const double *k, const double *v,
     free(th);
     pthread_mutex_destroy(&J.mu);
     return J.failed ? -2 : (started ? started : 1);
+}
+
+/* The plain causal mask (same_length off). */
+int oracle_attn_f64(const double *q, const double *k, const double *v,
+                    const double *r_k, const double *u, const double *vb,
+                    int B, int H, int L, int M, int dh, double scale,
+                    double *out, double *scores, const int *pairs, int npairs,
+                    int nthreads) {
+    return oracle_attn_f64_ex(q, k, v, r_k, u, vb, B, H, L, M, dh, scale, 0, 0, out, scores,
+                              pairs, npairs, nthreads);
 }

@@ -33,6 +33,12 @@ def parse_mask_picture():
     return np.array(pic, dtype=bool)
 
 
+def parse_same_length_picture():
+    rows = read_golden_rows("mask_same_length_M3_L4.txt")
+    return np.array([[c in ("m", "x") for c in ln.split(":", 1)[1].replace("|", " ").split()]
+                     for ln in rows], dtype=bool)
+
+
 def parse_rel_ids():
     return np.array([[int(t) for t in ln.split()] for ln in read_golden_rows("rel_ids_M3_L4.txt")])
 
@@ -63,6 +69,51 @@ def test_mask_picture_one_hot_probe():
         nvis = pic[i].sum()
         np.testing.assert_allclose(probs[i][pic[i]], 1.0 / nvis, rtol=0, atol=1e-15)
         assert np.all(probs[i][~pic[i]] == 0.0)
+
+
+def one_hot_probs(M, L, **kw):
+    """Probability rows of the oracle through the one-hot-V probe."""
+    K = M + L
+    dh = max(8, K)
+    q = rnd(1, 1, L, dh)
+    k = np.zeros((1, 1, K, dh))
+    v = np.zeros((1, 1, K, dh))
+    for j in range(K):
+        v[0, 0, j, j] = 1.0
+    out = oracle.attn(q, k, v, np.zeros((K, 1, dh)), np.zeros((1, dh)), rnd(1, dh), 0.125, **kw)
+    return out[0, 0][:, :K]
+
+
+def test_same_length_mask_picture_one_hot_probe():
+    pic = parse_same_length_picture()
+    probs = one_hot_probs(3, 4, same_length=True, mem_len=3)
+    assert np.array_equal(probs > 0, pic)
+    for i in range(4):
+        np.testing.assert_allclose(probs[i][pic[i]], 1.0 / pic[i].sum(), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("M,L,mem_len", [(3, 4, 3), (2, 4, 3), (0, 5, 2), (8, 3, 8), (5, 6, 6)])
+def test_same_length_every_query_sees_mem_len_keys(M, L, mem_len):
+    """While the context is longer than mem_len, every query attends to the
+    mem_len most recent keys (fewer only where fewer precede it), the latest
+    of which is itself."""
+    if M + L <= mem_len:
+        pytest.skip("context not longer than mem_len")
+    probs = one_hot_probs(M, L, same_length=True, mem_len=mem_len)
+    for i in range(L):
+        vis = np.flatnonzero(probs[i] > 0)
+        assert len(vis) == min(mem_len, M + i + 1)
+        assert vis[-1] == M + i and np.all(np.diff(vis) == 1)
+
+
+def test_same_length_is_the_causal_mask_when_context_fits():
+    for (M, L, mem_len) in [(3, 4, 7), (3, 4, 20), (0, 4, 4)]:
+        a = one_hot_probs(M, L, same_length=True, mem_len=mem_len)
+        pic = parse_mask_picture() if (M, L) == (3, 4) else None
+        b = one_hot_probs(M, L)
+        assert np.array_equal(a > 0, b > 0)
+        if pic is not None:
+            assert np.array_equal(a > 0, pic)
 
 
 def test_mask_count_matches_visible_pair_formula():
