@@ -397,7 +397,7 @@ def run_ours(args, wl: W.Workload):
 # the kernel sources still hash to what was captured.
 _TRAFFIC_CAPTURES = {
     "base512_bf16": {
-        "sha256_prefix": {"attn_tc_bf16.cu": "4fda2ca95b9affce", "txl_device.cuh": "c81e2ad2586a8c56"},
+        "sha256_prefix": {"attn_tc_bf16.cu": "d19c02c446628130", "txl_device.cuh": "c81e2ad2586a8c56"},
         "bytes_per_launch": 60880640,
         "summary": "profiles/attn_tc_bf16_base512_ncu_full.md",
     },

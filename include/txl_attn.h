@@ -84,6 +84,22 @@ int txl_attn_fwd(const void* q, const void* k, const void* v, const void* r_k,
                  int dtype, void* stream);
 
 /*
+ * txl_attn_fwd_ex: txl_attn_fwd with the same_length mask of
+ * "Transformer-XL模型 核心源码阅读笔记" (MemTransformerLM._forward): every query
+ * attends over the same number of keys.  With klen = M+L and mask_len = klen -
+ * mem_len, query i additionally ignores keys j <= i - mask_shift_len, where
+ * mask_shift_len = L - mask_len if mask_len > 0, else L; when M = mem_len each
+ * query sees its mem_len most recent positions, itself included.  mem_len is
+ * the configured memory length (M <= mem_len; M < mem_len while the memory is
+ * still filling), else TXL_ERR_INVALID_ARG.  Key tiles that no query of a
+ * 128-row query tile sees are skipped.  same_length = 0 is txl_attn_fwd.
+ * Everything else (layouts, sizes, errors) as for txl_attn_fwd.
+ */
+int txl_attn_fwd_ex(const void* q, const void* k, const void* v, const void* r_k,
+                    const void* u_bias, const void* v_bias, int B, int H, int L, int M, int d_h,
+                    float scale, int same_length, int mem_len, void* out, int dtype, void* stream);
+
+/*
  * Scratch bytes txl_attn_fwd_ws needs for these sizes (0 when the call runs
  * without splitting the keys).  Never negative; 0 also for invalid sizes.
  */
@@ -201,6 +217,26 @@ int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_
  */
 int txl_mem_update(void* mems, const void* hids, int B, int L, int M, int d,
                    int dtype, void* stream);
+
+/*
+ * txl_mem_update_ext: txl_mem_update keeping the last ext_len rows of hids
+ * out of the memory ("Transformer-XL模型 核心源码阅读笔记",
+ * MemTransformerLM._update_mems: the cached span of [mems; hids] ends ext_len
+ * rows before its end, those rows serving as extended context of the next
+ * segment instead).  The result is the Tail_M roll with hids[:, :L-ext_len]
+ * (an unchanged memory when ext_len >= L); hids is still [B, L, d].
+ * ext_len < 0 returns TXL_ERR_INVALID_ARG.  ext_len = 0 is txl_mem_update.
+ *
+ * txl_mem_reset: mems [B, rows, d] (any layout whose batch rows are
+ * contiguous, e.g. [B, H, M, d_h] with rows = H*M, d = d_h); every batch row
+ * b with flags[b] != 0 (flags: B bytes in device memory) is set to zero bits
+ * ("Transformer-XL" notes, section "Batched Streams": a row whose stream
+ * enters a new document gets an empty memory; the flag is per row, not per
+ * batch).  Other rows are untouched.  Asynchronous on `stream`.
+ */
+int txl_mem_update_ext(void* mems, const void* hids, int B, int L, int M, int d, int ext_len,
+                       int dtype, void* stream);
+int txl_mem_reset(void* mems, const void* flags, int B, int rows, int d, int dtype, void* stream);
 
 /*
  * Waits for `stream`, then reports and clears the device status word:

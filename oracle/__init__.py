@@ -162,6 +162,15 @@ def mem_update(mem, hid, mem_len: int, ext_len: int = 0) -> np.ndarray:
     return np.ascontiguousarray(cat[:, beg:end])
 
 
+def mem_reset(mem, flags) -> np.ndarray:
+    """Per-row memory reset ("Transformer-XL" notes, section "Batched
+    Streams": rows whose stream enters a new document get zeros; the flag is
+    per batch row).  mem [B, ...] of any dtype, flags [B]; bit-exact."""
+    out = np.array(mem, copy=True)
+    out[np.asarray(flags).astype(bool)] = 0
+    return out
+
+
 def _heads(x: np.ndarray, n_head: int) -> np.ndarray:
     """[B, T, n_head*d_head] -> [B, n_head, T, d_head]."""
     B, T, d = x.shape

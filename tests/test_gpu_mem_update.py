@@ -64,3 +64,41 @@ def test_tail_m_rejects_overlap():
     with pytest.raises(txl.TxlError) as e:
         txl.mem_update(mems, hids)
     assert e.value.code == -4
+
+
+@pytest.mark.parametrize("B,M,L,d,ext,dtype", [
+    (2, 8, 16, 64, 4, torch.bfloat16),     # L - ext >= M: copy from h with an offset
+    (3, 12, 10, 64, 3, torch.bfloat16),    # L - ext < M: chains over memory and h
+    (2, 5, 9, 6, 2, torch.float32),        # 24-byte rows
+    (1, 7, 4, 8, 4, torch.bfloat16),       # ext = L: the memory stays
+    (1, 7, 4, 8, 9, torch.bfloat16),       # ext > L: likewise
+    (8, 3200, 128, 1024, 64, torch.bfloat16),  # long-memory shape
+])
+def test_tail_m_ext_len_bit_exact(B, M, L, d, ext, dtype):
+    g = torch.Generator().manual_seed(B * 17 + M + L + ext)
+    mem = torch.randn(B, M, d, generator=g).to(dtype)
+    hid = torch.randn(B, L, d, generator=g).to(dtype)
+    expect = oracle.mem_update(bits(mem), bits(hid), M, ext_len=ext)
+    dm = mem.cuda()
+    txl.mem_update(dm, hid.cuda(), ext_len=ext)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    assert np.array_equal(bits(dm), expect)
+
+
+@pytest.mark.parametrize("shape,dtype", [
+    ((4, 128, 512), torch.bfloat16),          # rows layout [B, M, d]
+    ((3, 8, 128, 64), torch.bfloat16),        # heads layout [B, H, M, d_h]
+    ((5, 7, 3), torch.float32),               # odd sizes: scalar path
+    ((22, 512, 512), torch.bfloat16),         # base-size memory
+])
+def test_mem_reset_bit_exact(shape, dtype):
+    g = torch.Generator().manual_seed(sum(shape))
+    mem = torch.randn(*shape, generator=g).to(dtype)
+    flags = (torch.arange(shape[0]) % 3 == 1)
+    expect = oracle.mem_reset(bits(mem), flags.numpy())
+    dm = mem.cuda()
+    txl.mem_reset(dm, flags.cuda())
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    assert np.array_equal(bits(dm), expect)

@@ -34,7 +34,7 @@ def rows(x):
     return x.permute(0, 2, 1, 3).reshape(B, T, H * dh)
 
 
-def make_stack():
+def make_stack(same_length=False, ext_len=0):
     dev = torch.device("cuda")
     p = W.make_params(WL)
     H, d, L, M = WL.H, WL.d, WL.L, WL.M
@@ -46,31 +46,42 @@ def make_stack():
     vb = [p.v.to(dev, BF)] * WL.layers
     m0 = W.initial_memories(WL)
     mems = [m0[0].to(dev, BF)] + [W._split_heads(m, H).to(dev, BF) for m in m0[1:]]
-    return txl.AttnStack(w_qkv, r_k, u, vb, mems, WL.scale, H, L), w_qkv, r_k, u, vb
+    return (txl.AttnStack(w_qkv, r_k, u, vb, mems, WL.scale, H, L, same_length=same_length,
+                          ext_len=ext_len), w_qkv, r_k, u, vb)
 
 
-def test_stack_calls_and_memories_match_oracle():
-    stack, w_qkv, r_k, u, vb = make_stack()
+@pytest.mark.parametrize("same_length,ext_len,reset", [(False, 0, False), (True, 32, True)])
+def test_stack_calls_and_memories_match_oracle(same_length, ext_len, reset):
+    """The second case adds the MemTransformerLM options: same_length
+    attention, ext_len rolls, and a per-row reset of batch row 1 before the
+    third segment."""
+    stack, w_qkv, r_k, u, vb = make_stack(same_length, ext_len)
     M = WL.M
     ref_mem = [bits(m) for m in stack.mems]
     trace = []
+    flags = torch.tensor([False, True])
     for s in range(WL.segments):
+        if reset and s == 2:
+            stack.reset_rows(flags.cuda())
         h0 = W.segment_input(WL, s).cuda().to(BF)
         stack.run_segment(h0, trace=trace)
     torch.cuda.synchronize()
     assert txl.sync_status() == 0
     assert len(trace) == WL.segments * WL.layers
-    for c in trace:
+    for idx, c in enumerate(trace):
         n = c["n"]
+        if reset and idx == 2 * WL.layers:  # the reset before segment 2
+            ref_mem = [oracle.mem_reset(m, flags.numpy()) for m in ref_mem]
         # the memory this call saw is the oracle's roll of the earlier segments
         assert np.array_equal(bits(c["mem"]), ref_mem[n])
         mem, h = c["mem"], c["h"]
         if mem.dim() == 4:
             B, H, _, dh = mem.shape
-            nxt = oracle.mem_update(bits(mem).reshape(B * H, M, dh), bits(h).reshape(B * H, -1, dh), M)
+            nxt = oracle.mem_update(bits(mem).reshape(B * H, M, dh), bits(h).reshape(B * H, -1, dh), M,
+                                    ext_len=ext_len)
             ref_mem[n] = nxt.reshape(B, H, M, dh)
         else:
-            ref_mem[n] = oracle.mem_update(bits(mem), bits(h), M)
+            ref_mem[n] = oracle.mem_update(bits(mem), bits(h), M, ext_len=ext_len)
         # projections on the inputs the call saw
         rq, rk, rv = oracle.qkv_proj(rows(h).cpu(), rows(mem).cpu(), w_qkv[n].cpu(), WL.H)
         for got, ref in ((c["q"], rq), (c["k"], rk), (c["v"], rv)):
@@ -78,7 +89,7 @@ def test_stack_calls_and_memories_match_oracle():
             assert np.abs(g - ref).max() <= tol(ref), n
         # attention on the q, k, v the call saw
         cpu = [t.cpu() for t in (c["q"], c["k"], c["v"], r_k[n], u[n], vb[n])]
-        ref = oracle.attn(*cpu, WL.scale)
+        ref = oracle.attn(*cpu, WL.scale, same_length=same_length, mem_len=M)
         got = c["out"].float().cpu().double().numpy()
         assert np.abs(got - ref).max() <= tol(ref), n
     # each layer's input is the previous layer's output

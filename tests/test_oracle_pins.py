@@ -421,3 +421,11 @@ def test_r_proj_is_rowwise_product_split_into_heads():
             for e in range(dh):
                 ref = sum(emb[t, c] * w[hh * dh + e, c] for c in range(d))
                 assert abs(r[t, hh, e] - ref) < 1e-12
+
+
+def test_mem_reset_zeroes_exactly_the_flagged_rows():
+    mem = np.arange(3 * 2 * 4, dtype=np.int16).reshape(3, 2, 4) + 1
+    out = oracle.mem_reset(mem, [False, True, False])
+    assert np.array_equal(out[0], mem[0]) and np.array_equal(out[2], mem[2])
+    assert np.array_equal(out[1], np.zeros((2, 4), dtype=np.int16))
+    assert np.array_equal(oracle.mem_reset(mem, [0, 0, 0]), mem)

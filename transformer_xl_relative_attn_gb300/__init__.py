@@ -4,7 +4,7 @@ recurrence memory.
 Public API (all computation runs in libtxl.so's CUDA kernels):
     attn_fwd, attn_fwd_ws, attn_workspace_bytes   relative attention forward
     attn_fwd_noalloc                              the same with the library's static scratch
-    mem_update                                    Tail_M memory roll, in place
+    mem_update, mem_reset                         Tail_M memory roll (ext_len), per-row reset, in place
     qkv_proj, r_proj                              head-split input projections (tensor cores)
     sync_status, check_status                     device status word
     SegmentDriver                                 multi-segment, multi-layer driver (caller's projections)
@@ -12,12 +12,12 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
 """
 from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
                    attn_workspace_bytes,
-                   check_status, debug_inject, header_functions, load, mem_update, qkv_proj, r_proj,
+                   check_status, debug_inject, header_functions, load, mem_reset, mem_update, qkv_proj, r_proj,
                    status_string,
                    sync_status, version, LIB_PATH)
 from .driver import AttnStack, SegmentDriver
 
 __all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
            "attn_workspace_bytes",
-           "check_status", "debug_inject", "header_functions", "load", "mem_update", "qkv_proj", "r_proj",
+           "check_status", "debug_inject", "header_functions", "load", "mem_reset", "mem_update", "qkv_proj", "r_proj",
            "status_string", "sync_status", "version", "SegmentDriver", "AttnStack", "LIB_PATH"]

@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.txl_attn_fwd.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
         lib.txl_attn_fwd.restype = i
+        lib.txl_attn_fwd_ex.argtypes = [vp] * 6 + [i] * 5 + [f, i, i, vp, i, vp]
+        lib.txl_attn_fwd_ex.restype = i
         lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
         lib.txl_attn_fwd_ws.restype = i
         lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
@@ -68,6 +70,10 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_workspace_bytes.restype = sz
         lib.txl_mem_update.argtypes = [vp, vp] + [i] * 5 + [vp]
         lib.txl_mem_update.restype = i
+        lib.txl_mem_update_ext.argtypes = [vp, vp] + [i] * 6 + [vp]
+        lib.txl_mem_update_ext.restype = i
+        lib.txl_mem_reset.argtypes = [vp, vp] + [i] * 4 + [vp]
+        lib.txl_mem_reset.restype = i
         lib.txl_sync_status.argtypes = [vp]
         lib.txl_sync_status.restype = i
         lib.txl_status_string.argtypes = [i]
@@ -147,11 +153,22 @@ def _attn_args(q, k, v, r_k, u, vb, scale, out):
     return B, H, L, M, dh, float(scale), out
 
 
-def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None) -> torch.Tensor:
-    """Relative attention forward (txl_attn_fwd).  Shapes: q [B,H,L,dh];
-    k, v [B,H,M+L,dh] (memory rows first); r_k [M+L,H,dh] (row r <->
-    distance M+L-1-r); u, vb [H,dh].  Returns out [B,H,L,dh]."""
+def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None, same_length=False,
+             mem_len=None) -> torch.Tensor:
+    """Relative attention forward (txl_attn_fwd, or txl_attn_fwd_ex with
+    same_length).  Shapes: q [B,H,L,dh]; k, v [B,H,M+L,dh] (memory rows
+    first); r_k [M+L,H,dh] (row r <-> distance M+L-1-r); u, vb [H,dh].
+    same_length: every query attends over the same number of keys, for the
+    configured memory length mem_len (default M).  Returns out [B,H,L,dh]."""
     B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    if same_length:
+        rc = load().txl_attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                                    u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, 1,
+                                    M if mem_len is None else int(mem_len), out.data_ptr(),
+                                    _dtype_code(q), _stream(stream, q.device))
+        if rc != 0:
+            raise TxlError(rc, "txl_attn_fwd_ex")
+        return out
     rc = load().txl_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
                              u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(),
                              _dtype_code(q), _stream(stream, q.device))
@@ -253,19 +270,45 @@ def r_proj(emb, w_r, H, out=None, stream=None):
     return out
 
 
-def mem_update(mems: torch.Tensor, hids: torch.Tensor, stream=None) -> torch.Tensor:
-    """Tail_M roll in place (txl_mem_update): mems [B,M,d] <- newest M rows of
-    [mems; hids], hids [B,L,d].  Returns mems."""
+def mem_update(mems: torch.Tensor, hids: torch.Tensor, stream=None, ext_len: int = 0) -> torch.Tensor:
+    """Tail_M roll in place (txl_mem_update, or txl_mem_update_ext when
+    ext_len > 0): mems [B,M,d] <- newest M rows of [mems; hids[:, :L-ext_len]],
+    hids [B,L,d].  Returns mems."""
     if mems.dim() != 3 or hids.dim() != 3:
         raise ValueError("mems must be [B, M, d] and hids [B, L, d]")
     B, M, d = mems.shape
     L = hids.shape[1]
     _need(mems, "mems", (B, M, d), mems.dtype)
     _need(hids, "hids", (B, L, d), mems.dtype)
+    if ext_len:
+        rc = load().txl_mem_update_ext(mems.data_ptr(), hids.data_ptr(), B, L, M, d, int(ext_len),
+                                       _dtype_code(mems), _stream(stream, mems.device))
+        if rc != 0:
+            raise TxlError(rc, "txl_mem_update_ext")
+        return mems
     rc = load().txl_mem_update(mems.data_ptr(), hids.data_ptr(), B, L, M, d, _dtype_code(mems),
                                _stream(stream, mems.device))
     if rc != 0:
         raise TxlError(rc, "txl_mem_update")
+    return mems
+
+
+def mem_reset(mems: torch.Tensor, flags: torch.Tensor, stream=None) -> torch.Tensor:
+    """txl_mem_reset: zeroes batch row b of mems (any contiguous [B, ...]
+    layout) wherever flags[b] is set; flags is a bool or uint8 CUDA tensor
+    [B].  Returns mems."""
+    if mems.dim() < 2 or not mems.is_cuda or not mems.is_contiguous():
+        raise ValueError("mems must be a contiguous CUDA tensor [B, ...]")
+    B = mems.shape[0]
+    d = mems.shape[-1]
+    rows = mems.numel() // (B * d) if B * d else 0
+    if flags.shape != (B,) or flags.device != mems.device or flags.dtype not in (torch.bool, torch.uint8):
+        raise ValueError("flags must be a bool/uint8 tensor [B] on the memory's device")
+    f = flags.contiguous()
+    rc = load().txl_mem_reset(mems.data_ptr(), f.data_ptr(), B, rows, d, _dtype_code(mems),
+                              _stream(stream, mems.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_mem_reset")
     return mems
 
 

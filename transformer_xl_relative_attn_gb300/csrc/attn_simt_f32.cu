@@ -6,7 +6,8 @@
 // for its key ("Transformer-XL模型 核心源码阅读笔记", section "Build the
 // model", RelPartialLearnableMultiHeadAttn.forward: AC + BD after the shift),
 // keys past M+i are masked ("Transformer-XL" notes, section "Causal Mask With
-// Memory"), and the chunk's probabilities are broadcast lane by lane while
+// Memory"; with same_length also keys before i+1-lo_shift, per the source
+// notes' MemTransformerLM._forward), and the chunk's probabilities are broadcast lane by lane while
 // each lane accumulates its own output columns.  The relative shift is the
 // row index M+L-1-(M+i-j) of R; no shifted score matrix is formed.
 #include <cstdint>
@@ -21,7 +22,7 @@ __global__ void __launch_bounds__(32 * kSimtWarps)
 attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                      const float* __restrict__ v, const float* __restrict__ r,
                      const float* __restrict__ ub, const float* __restrict__ vb, int B, int H,
-                     int L, int M, int dh, float scale, float* __restrict__ out) {
+                     int L, int M, int dh, float scale, int lo_shift, float* __restrict__ out) {
     __shared__ float s_qu[kSimtWarps][kSimtMaxD];
     __shared__ float s_qv[kSimtWarps][kSimtMaxD];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -40,13 +41,14 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     __syncwarp();
     const float* kb = k + bh * (long long)K * dh;
     const float* vbase = v + bh * (long long)K * dh;
-    const int nvis = M + i + 1;  // keys 0..M+i are visible
+    const int nvis = M + i + 1;  // keys up to M+i are visible
+    const int jlo = max(0, i + 1 - lo_shift);  // ... from jlo on (0 unless same_length)
     const int ncol = (dh + 31) / 32;
     float acc[kSimtMaxD / 32];
 #pragma unroll
     for (int c = 0; c < kSimtMaxD / 32; ++c) acc[c] = 0.f;
     float m = -INFINITY, l = 0.f;
-    for (int j0 = 0; j0 < nvis; j0 += 32) {
+    for (int j0 = jlo; j0 < nvis; j0 += 32) {
         const int j = j0 + lane;
         float s = -INFINITY;
         if (j < nvis) {
@@ -95,12 +97,12 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
 cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
                                  const float* ub, const float* vb, int B, int H, int L, int M,
-                                 int dh, float scale, float* out, cudaStream_t stream) {
+                                 int dh, float scale, int lo_shift, float* out, cudaStream_t stream) {
     const long long rows = (long long)B * H * L;
     const long long blocks = (rows + kSimtWarps - 1) / kSimtWarps;
     if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     attn_simt_f32_kernel<<<(unsigned)blocks, 32 * kSimtWarps, 0, stream>>>(
-        q, k, v, r, ub, vb, B, H, L, M, dh, scale, out);
+        q, k, v, r, ub, vb, B, H, L, M, dh, scale, lo_shift, out);
     return cudaGetLastError();
 }
 

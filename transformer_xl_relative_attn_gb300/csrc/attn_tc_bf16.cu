@@ -131,6 +131,7 @@ struct TcParams {
     float scale_log2;  // scale * log2(e), folded into q+u and q+v
     int inject;        // 1: withhold the first score-ready signal (timeout test)
     int* status;       // device status word
+    int lo_shift;      // keys j < i + 1 - lo_shift are masked too (same_length; 1 << 30: none)
 };
 
 struct TcShared {
@@ -162,7 +163,7 @@ struct Item {
 // splits of an item are adjacent, and units are dealt to CTAs in snake order
 // (rounds alternate direction) to even out the load.  A split takes a
 // contiguous range of tile pairs, so t0 is even.
-template <bool SPLIT>
+template <bool SPLIT, bool LOWER>
 __device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
     const int G = gridDim.x, c = blockIdx.x;
     const int w = k * G + ((k & 1) ? (G - 1 - c) : c);  // below 2^31: checked at launch
@@ -181,13 +182,20 @@ __device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
     const int rows_valid = min(tc::BM, p.L - it.i0);
     const int kmax = p.M + it.i0 + rows_valid - 1;  // last key any row of the tile sees
     const int all = kmax / tc::BN + 1;
-    it.t0 = 0;
-    it.ntiles = all;
+    // first key any row of the tile sees (same_length), rounded down to a
+    // tile pair: tiles below it are skipped
+    int tlo = 0;
+    if constexpr (LOWER) {
+        const int jmin = it.i0 + 1 - p.lo_shift;
+        tlo = jmin > 0 ? ((jmin / tc::BN) & ~1) : 0;
+    }
+    it.t0 = tlo;
+    it.ntiles = all - tlo;
     if constexpr (SPLIT) {
-        const int pairs = (all + 1) >> 1;
+        const int pairs = (all - tlo + 1) >> 1;
         const int lo = pairs * sp / p.nsplit, hi = pairs * (sp + 1) / p.nsplit;
-        it.t0 = 2 * lo;
-        it.ntiles = min(2 * hi, all) - it.t0;
+        it.t0 = tlo + 2 * lo;
+        it.ntiles = min(tlo + 2 * hi, all) - it.t0;
     }
     it.rbase = p.L - it.i0 - tc::BM + tc::SLOT * it.t0;  // R row of the unit's slot 0
     it.unit = w;
@@ -288,8 +296,10 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
 }
 
 // SPLIT: the units are key splits of items and write partial results (see
-// attn_combine_kernel); otherwise every unit is a whole item.
-template <bool SPLIT>
+// attn_combine_kernel); otherwise every unit is a whole item.  LOWER: the
+// same_length lower key bound is applied (tiles below it skipped, keys below
+// it masked).
+template <bool SPLIT, bool LOWER>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
 attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
@@ -408,7 +418,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         Item cur;
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
-        for (int k = 0; ok && item_of<SPLIT>(p, k, cur); ++k) {
+        for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, cur); ++k) {
             // the first item's q tile; a failed wait leaves ok false, and the
             // group still reaches this item's merge barriers below
             if (k == 0) {
@@ -416,7 +426,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 write_q(cur, 0, 0);
             }
             Item nxt;
-            const bool has_next = item_of<SPLIT>(p, k + 1, nxt);
+            const bool has_next = item_of<SPLIT, LOWER>(p, k + 1, nxt);
             // the next item's q tile: loaded once this group holds the current
             // item's first scores, turned into (q+bias)c after that tile
             bool next_issued = !has_next, next_written = !has_next;
@@ -448,8 +458,12 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tc_fence_after();
                 }
                 const int j0 = (cur.t0 + t) * BN;
-                const bool need_mask = (j0 + BN - 1) > (p.M + cur.i0);
-                const int jlim = p.M + i - j0;  // keys jj > jlim are masked
+                // the diagonal crosses the tile, or (same_length) the lower bound
+                // of the tile's last row lies past its first key
+                const bool need_mask =
+                    (j0 + BN - 1) > (p.M + cur.i0) || (LOWER && j0 < cur.i0 + BM - p.lo_shift);
+                const int jlim = p.M + i - j0;       // keys jj > jlim are masked
+                const int jlo = i + 1 - p.lo_shift - j0;  // and keys jj < jlo
                 float sc[BN];
                 float tmax = -INFINITY;
 #pragma unroll
@@ -485,7 +499,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     if (need_mask) {
 #pragma unroll
                         for (int x = 0; x < 32; ++x)
-                            if (32 * q2 + x > jlim) sc[32 * q2 + x] = -INFINITY;
+                            if (32 * q2 + x > jlim || (LOWER && 32 * q2 + x < jlo))
+                                sc[32 * q2 + x] = -INFINITY;
                     }
 #pragma unroll
                     for (int x = 0; x < 32; x += 2)
@@ -663,7 +678,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             int kv_s = 0, r_s = 0;     // K/V stage and R box counters at the item start
             int gbase = 0;             // global position-slot counter at the item start
             Item is;
-            for (int ks = 0; ok && item_of<SPLIT>(p, ks, is); ++ks) {
+            for (int ks = 0; ok && item_of<SPLIT, LOWER>(p, ks, is); ++ks) {
                 const int npairs = (is.ntiles + 1) >> 1;
                 const int nrb = npairs + 1;  // R boxes of the item (slots 0 .. 2*npairs+1)
                 wait(&sh->q_ready, ks & 1);
@@ -739,7 +754,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dV0 = smem_desc_sw128(s_base + OFF_KV + SZ_BOX, BN * 128, 1024);
             constexpr uint32_t U_Q = SZ_Q >> 4, U_T = SZ_T >> 4, U_BOX = SZ_BOX >> 4;
             Item ip;
-            bool p_valid = item_of<SPLIT>(p, 0, ip);
+            bool p_valid = item_of<SPLIT, LOWER>(p, 0, ip);
             int kp = 0, tp = 0, kv_p = 0;
             int pc0 = 0, pc1 = 0;  // P tiles consumed, per group
             while (ok && p_valid) {
@@ -768,7 +783,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     kv_p += (ip.ntiles + 1) >> 1;
                     tp = 0;
                     ++kp;
-                    p_valid = item_of<SPLIT>(p, kp, ip);
+                    p_valid = item_of<SPLIT, LOWER>(p, kp, ip);
                 }
             }
             if (leader) mma_commit(&sh->drain);
@@ -781,7 +796,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             int kvc = 0, rc = 0;  // loads issued into each ring
             bool ok = true;
             Item it;
-            for (int k = 0; ok && item_of<SPLIT>(p, k, it); ++k) {
+            for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
                 const int nkv = (it.ntiles + 1) >> 1;  // K/V stages of this item
                 const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
                 int rb = 0;
@@ -960,15 +975,18 @@ size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M) {
 
 cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
                                 const void* ub, const void* vb, int B, int H, int L, int M,
-                                float scale, void* out, void* workspace, int inject, int* status,
-                                cudaStream_t stream) {
+                                float scale, int lo_shift, void* out, void* workspace, int inject,
+                                int* status, cudaStream_t stream) {
     using namespace tc;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false>,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<true>,
+            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1004,11 +1022,14 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.H = H;
     p.L = L;
     p.M = M;
+    p.lo_shift = lo_shift;
     p.n_qtiles = (L + BM - 1) / BM;
     const long long n_items = (long long)B * H * p.n_qtiles;
     if (n_items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_items = (int)n_items;
-    p.nsplit = workspace ? attn_tc_bf16_splits(B, H, L, M) : 1;
+    // the same_length bound runs unsplit (txl_attn_fwd_ex takes no workspace)
+    const bool lower = lo_shift < (1 << 30);
+    p.nsplit = (workspace && !lower) ? attn_tc_bf16_splits(B, H, L, M) : 1;
     if ((long long)p.n_items * p.nsplit + 2ll * num_sms() >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_units = p.n_items * p.nsplit;
     const size_t units = (size_t)p.n_units;
@@ -1020,9 +1041,11 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
     if (p.nsplit > 1)
-        attn_tc_bf16_kernel<true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+        attn_tc_bf16_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+    else if (lower)
+        attn_tc_bf16_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
     else
-        attn_tc_bf16_kernel<false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+        attn_tc_bf16_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const long long threads = (long long)B * H * L * 8;

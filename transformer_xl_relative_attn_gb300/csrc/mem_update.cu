@@ -5,6 +5,11 @@
 // of [M_tau; H_tau]).  With L >= M every new row comes from h.  With L < M
 // row r takes mem[r+L] while r+L < M, else h[r+L-M].
 //
+// With ext_len > 0 the last ext_len rows of h are kept out of the memory
+// ("Transformer-XL模型 核心源码阅读笔记", MemTransformerLM._update_mems: the
+// cached span ends ext_len rows before the end of [mem; h]): the roll above
+// with the first L - ext_len rows of h in place of h.
+//
 // In place without a workspace (details at each kernel).  Adjacent threads
 // own adjacent vectors of a row, so every warp access is contiguous.
 #include <cstdint>
@@ -46,7 +51,7 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(V* __restrict__ mem, con
 // block of kChain sources before storing them.
 template <typename V, typename I>
 __global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, const V* __restrict__ hid,
-                                                         int L, int M, I rowv, I total) {
+                                                         int L, int M, I rowv, I total, I hstride) {
     const I t = (I)blockIdx.x * 256 + threadIdx.x;
     if (t >= total) return;
     const I col = t % rowv;
@@ -54,7 +59,7 @@ __global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, co
     const int c = (int)(cb % (I)L);
     const I b = cb / (I)L;
     V* mrow = mem + b * (I)M * rowv + col;
-    const V* hrow = hid + b * (I)L * rowv + col;
+    const V* hrow = hid + b * hstride + col;
     for (int r0 = c; r0 < M; r0 += kChain * L) {
         V buf[kChain];
 #pragma unroll
@@ -73,37 +78,54 @@ __global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, co
     }
 }
 
+// Zeroes the memory rows of every batch row b with flags[b] != 0 (a batch
+// row whose stream starts a new document; "Transformer-XL" notes, section
+// "Batched Streams": the reset is per row).  mem is [B, rows, row]; one
+// thread per vector.
+template <typename V, typename I>
+__global__ void __launch_bounds__(256) mem_reset_kernel(V* __restrict__ mem, const unsigned char* __restrict__ flags,
+                                                        I per_b, I total) {
+    const I e = (I)blockIdx.x * 256 + threadIdx.x;
+    if (e >= total) return;
+    if (flags[e / per_b]) mem[e] = V{};
+}
+
 // Launches the roll with the widest vector the alignment allows and 32-bit
-// index arithmetic whenever the element counts fit.
-cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int M, size_t row_bytes,
-                          cudaStream_t stream) {
+// index arithmetic whenever the element counts fit.  L rows of each batch
+// row of hid take part; consecutive batch rows of hid are L_stride rows
+// apart (L < L_stride when trailing rows are held back).
+cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride, int M,
+                          size_t row_bytes, cudaStream_t stream) {
+    if (L <= 0 || M <= 0) return cudaSuccess;  // nothing new enters, or no memory
     auto go = [&](auto tag) -> cudaError_t {
         using V = decltype(tag);
         const long long rowv = (long long)(row_bytes / sizeof(V));
         if (L >= M) {
             const long long seg = (long long)M * rowv, total = (long long)B * seg;
-            const long long hsz = (long long)B * L * rowv;
+            const long long hsz = (long long)B * L_stride * rowv;
             const long long blocks = (total + 256 * kCopyUnroll - 1) / (256 * kCopyUnroll);
             if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
             if (hsz < 0x7FFFFFFFll - 256 * kCopyUnroll)
                 tail_copy_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
                     static_cast<V*>(mem), static_cast<const V*>(hid), (int)total, (int)seg,
-                    (int)(L * rowv), (int)((L - M) * rowv));
+                    (int)(L_stride * rowv), (int)((L - M) * rowv));
             else
                 tail_copy_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), total, seg, L * rowv,
+                    static_cast<V*>(mem), static_cast<const V*>(hid), total, seg, L_stride * rowv,
                     (L - M) * rowv);
         } else {
             const long long total = (long long)B * L * rowv;
-            const long long msz = (long long)B * M * rowv;
+            const long long msz = (long long)B * (M > L_stride ? M : L_stride) * rowv;
             const long long blocks = (total + 255) / 256;
             if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
             if (msz < 0x7FFFFFFFll - 256)
                 tail_chain_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, (int)rowv, (int)total);
+                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, (int)rowv, (int)total,
+                    (int)(L_stride * rowv));
             else
                 tail_chain_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, rowv, total);
+                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, rowv, total,
+                    (long long)L_stride * rowv);
         }
         return cudaGetLastError();
     };
@@ -111,6 +133,28 @@ cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int M, size_
     if (row_bytes % 16 == 0 && a % 16 == 0) return go(uint4{});
     if (row_bytes % 8 == 0 && a % 8 == 0) return go(uint2{});
     if (row_bytes % 4 == 0 && a % 4 == 0) return go(uint32_t{});
+    return go(uint16_t{});
+}
+
+cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long long per_b_bytes,
+                             cudaStream_t stream) {
+    auto go = [&](auto tag) -> cudaError_t {
+        using V = decltype(tag);
+        const long long per_b = per_b_bytes / (long long)sizeof(V), total = (long long)B * per_b;
+        const long long blocks = (total + 255) / 256;
+        if (total == 0) return cudaSuccess;
+        if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+        if (total < 0x7FFFFFFFll - 256)
+            mem_reset_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<V*>(mem), flags,
+                                                                           (int)per_b, (int)total);
+        else
+            mem_reset_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<V*>(mem), flags,
+                                                                                 per_b, total);
+        return cudaGetLastError();
+    };
+    const uintptr_t a = reinterpret_cast<uintptr_t>(mem);
+    if (per_b_bytes % 16 == 0 && a % 16 == 0) return go(uint4{});
+    if (per_b_bytes % 4 == 0 && a % 4 == 0) return go(uint32_t{});
     return go(uint16_t{});
 }
 

@@ -13,15 +13,17 @@
 namespace txl {
 __device__ int g_dev_status = 0;
 
-cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int M, size_t row_bytes,
-                          cudaStream_t stream);
+cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride, int M,
+                          size_t row_bytes, cudaStream_t stream);
+cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long long per_b_bytes,
+                             cudaStream_t stream);
 cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
                                  const float* ub, const float* vb, int B, int H, int L, int M,
-                                 int dh, float scale, float* out, cudaStream_t stream);
+                                 int dh, float scale, int lo_shift, float* out, cudaStream_t stream);
 cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
                                 const void* ub, const void* vb, int B, int H, int L, int M,
-                                float scale, void* out, void* workspace, int inject, int* status,
-                                cudaStream_t stream);
+                                float scale, int lo_shift, void* out, void* workspace, int inject,
+                                int* status, cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
 
 }  // namespace txl
@@ -93,9 +95,21 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* r_k
     return TXL_OK;
 }
 
+// No lower key bound: the plain causal mask with memory.
+constexpr int kNoLowerBound = 1 << 30;
+
+// same_length (source-reading notes, MemTransformerLM._forward): with klen =
+// M+L and mask_len = klen - mem_len, query i also ignores keys j <= i -
+// mask_shift_len, where mask_shift_len = L - mask_len if mask_len > 0, else L.
+int lower_shift(int same_length, int L, int M, int mem_len) {
+    if (!same_length) return kNoLowerBound;
+    const long long mask_len = (long long)M + L - mem_len;
+    return mask_len > 0 ? (int)(L - mask_len) : L;
+}
+
 int launch_attn(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
                 const void* v_bias, int B, int H, int L, int M, int d_h, float scale, void* out,
-                int dtype, void* workspace, void* stream) {
+                int dtype, void* workspace, void* stream, int lo_shift = kNoLowerBound) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == TXL_BF16) {
@@ -103,7 +117,7 @@ int launch_attn(const void* q, const void* k, const void* v, const void* r_k, co
         if (!status) return TXL_ERR_CUDA;
         const int inject = g_inject;
         g_inject = 0;
-        e = txl::launch_attn_tc_bf16(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale, out,
+        e = txl::launch_attn_tc_bf16(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale, lo_shift, out,
                                      workspace, inject, status, st);
         if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // tensor-map encoding failed
     } else {
@@ -111,7 +125,7 @@ int launch_attn(const void* q, const void* k, const void* v, const void* r_k, co
             static_cast<const float*>(q), static_cast<const float*>(k),
             static_cast<const float*>(v), static_cast<const float*>(r_k),
             static_cast<const float*>(u_bias), static_cast<const float*>(v_bias), B, H, L, M, d_h,
-            scale, static_cast<float*>(out), st);
+            scale, lo_shift, static_cast<float*>(out), st);
     }
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
@@ -127,6 +141,16 @@ int txl_attn_fwd(const void* q, const void* k, const void* v, const void* r_k,
     if (rc != TXL_OK) return rc;
     return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, nullptr,
                        stream);
+}
+
+int txl_attn_fwd_ex(const void* q, const void* k, const void* v, const void* r_k,
+                    const void* u_bias, const void* v_bias, int B, int H, int L, int M, int d_h,
+                    float scale, int same_length, int mem_len, void* out, int dtype, void* stream) {
+    const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
+    if (rc != TXL_OK) return rc;
+    if (same_length && (mem_len < M || mem_len >= (1 << 30))) return TXL_ERR_INVALID_ARG;
+    return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, nullptr,
+                       stream, lower_shift(same_length, L, M, mem_len));
 }
 
 size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype) {
@@ -158,15 +182,34 @@ int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k
 
 int txl_mem_update(void* mems, const void* hids, int B, int L, int M, int d, int dtype,
                    void* stream) {
+    return txl_mem_update_ext(mems, hids, B, L, M, d, 0, dtype, stream);
+}
+
+int txl_mem_update_ext(void* mems, const void* hids, int B, int L, int M, int d, int ext_len,
+                       int dtype, void* stream) {
     const int es = elem_size(dtype);
-    if (!es || B <= 0 || L <= 0 || M < 0 || d <= 0) return TXL_ERR_INVALID_ARG;
+    if (!es || B <= 0 || L <= 0 || M < 0 || d <= 0 || ext_len < 0) return TXL_ERR_INVALID_ARG;
     if (M == 0) return TXL_OK;
     if (!mems || !hids) return TXL_ERR_INVALID_ARG;
-    if ((long long)B * (M < L ? M : L) * d >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    if ((long long)B * (M > L ? M : L) * d >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
     const size_t row = (size_t)d * es;
     if (overlap(mems, (size_t)B * M * row, hids, (size_t)B * L * row)) return TXL_ERR_ALIAS;
+    const int used = ext_len < L ? L - ext_len : 0;  // rows of h that enter the memory
     const cudaError_t e =
-        txl::launch_tail_m(mems, hids, B, L, M, row, static_cast<cudaStream_t>(stream));
+        txl::launch_tail_m(mems, hids, B, used, L, M, row, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_mem_reset(void* mems, const void* flags, int B, int rows, int d, int dtype, void* stream) {
+    const int es = elem_size(dtype);
+    if (!es || B <= 0 || rows < 0 || d <= 0 || !flags) return TXL_ERR_INVALID_ARG;
+    if (rows == 0) return TXL_OK;
+    if (!mems) return TXL_ERR_INVALID_ARG;
+    const long long per_b = (long long)rows * d * es;
+    if ((long long)B * per_b >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    if (overlap(mems, (size_t)(B * per_b), flags, (size_t)B)) return TXL_ERR_ALIAS;
+    const cudaError_t e = txl::launch_mem_reset(mems, static_cast<const unsigned char*>(flags), B, per_b,
+                                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 

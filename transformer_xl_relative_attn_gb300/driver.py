@@ -101,15 +101,16 @@ class SegmentDriver:
         self.segments_done = int(sd.get("segments_done", 0))
 
 
-def _roll(mem: torch.Tensor, h: torch.Tensor, stream) -> None:
+def _roll(mem: torch.Tensor, h: torch.Tensor, stream, ext_len: int = 0) -> None:
     """Tail_M roll of one memory with the layer input h, in either layout:
     rows ([B, M, d] with [B, L, d]) or heads ([B, H, M, d_h] with
     [B, H, L, d_h], rolled as B*H independent rows of d_h elements)."""
     if mem.dim() == 4:
         B, H, M, dh = mem.shape
-        _lib.mem_update(mem.view(B * H, M, dh), h.view(B * H, h.shape[2], dh), stream=stream)
+        _lib.mem_update(mem.view(B * H, M, dh), h.view(B * H, h.shape[2], dh), stream=stream,
+                        ext_len=ext_len)
     else:
-        _lib.mem_update(mem, h, stream=stream)
+        _lib.mem_update(mem, h, stream=stream, ext_len=ext_len)
 
 
 class AttnStack:
@@ -131,6 +132,12 @@ class AttnStack:
     [B, H, M, d_h].  r_k[n] ([M+L, H, d_h]) depends on M and L only, so it is
     projected once, by the caller (txl_r_proj).
 
+    Options of the source notes' MemTransformerLM: ``same_length`` (every
+    query attends over the same number of keys, txl_attn_fwd_ex with mem_len
+    = M), ``ext_len`` (the last ext_len rows of each segment stay out of the
+    memory, txl_mem_update_ext), and ``reset_rows`` (per-row memory reset at
+    document boundaries, txl_mem_reset).
+
     The roll of mems[n] reads h after its projection has read mems[n]; all
     launches go to one stream, which orders every dependency of the
     recurrence.  q, k and v are one set of buffers reused by every layer; each
@@ -141,7 +148,8 @@ class AttnStack:
     def __init__(self, w_qkv: Sequence[torch.Tensor], r_k: Sequence[torch.Tensor],
                  u: Sequence[torch.Tensor], v_bias: Sequence[torch.Tensor],
                  mems: Sequence[torch.Tensor], scale: float, n_head: int, seg_len: int,
-                 stream: torch.cuda.Stream | None = None):
+                 stream: torch.cuda.Stream | None = None, same_length: bool = False,
+                 ext_len: int = 0):
         n = len(mems)
         if not (len(w_qkv) == len(r_k) == len(u) == len(v_bias) == n) or n == 0:
             raise ValueError("need one weight, r_k, u, v and memory per layer")
@@ -162,6 +170,7 @@ class AttnStack:
         self.w_qkv, self.r_k, self.u, self.v_bias = list(w_qkv), list(r_k), list(u), list(v_bias)
         self.mems = list(mems)
         self.scale, self.H, self.L = float(scale), H, int(seg_len)
+        self.same_length, self.ext_len = bool(same_length), int(ext_len)
         self.B, self.M, self.d, self.dh = B, M, d, dh
         dev = m0.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -194,16 +203,24 @@ class AttnStack:
                     rec = {"n": n, "h": h.clone(), "mem": mem.clone()}
                 _lib.qkv_proj(h, mem, self.w_qkv[n], self.H, q=self.q, k=self.k, v=self.v,
                               stream=self.stream)
-                _roll(mem, h, self.stream)
+                _roll(mem, h, self.stream, self.ext_len)
                 dst = out if (out is not None and n == len(self.mems) - 1) else self.outs[n]
                 o = _lib.attn_fwd(self.q, self.k, self.v, self.r_k[n], self.u[n], self.v_bias[n],
-                                  self.scale, out=dst, stream=self.stream)
+                                  self.scale, out=dst, stream=self.stream,
+                                  same_length=self.same_length, mem_len=self.M)
                 if rec is not None:
                     rec.update(q=self.q.clone(), k=self.k.clone(), v=self.v.clone(), out=o.clone())
                     trace.append(rec)
                 h = o
         self.segments_done += 1
         return h
+
+    def reset_rows(self, flags: torch.Tensor) -> None:
+        """Zeroes every layer's memory of the batch rows whose flag is set
+        (their streams start a new document); other rows keep theirs."""
+        with torch.cuda.stream(self.stream):
+            for m in self.mems:
+                _lib.mem_reset(m, flags, stream=self.stream)
 
     def state_dict(self) -> dict:
         """The per-layer memories (checkpoint/resume)."""
