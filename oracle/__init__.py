@@ -196,3 +196,47 @@ def r_proj(emb, w_r, n_head: int):
     e64, w64 = _f64(emb), _f64(w_r)
     K, d = e64.shape
     return (e64 @ w64.T).reshape(K, n_head, d // n_head)
+
+
+# ---------------------------------------------------------------------------
+# The rest of a decoder layer ("Transformer-XL模型 核心源码阅读笔记":
+# RelPartialLearnableMultiHeadAttn.forward after the attention, PositionwiseFF,
+# RelPartialLearnableDecoderLayer).  Row-major [B, T, d] activations, fp64.
+# ---------------------------------------------------------------------------
+def layer_norm(x, gamma, beta, eps: float = 1e-5) -> np.ndarray:
+    """nn.LayerNorm over the last axis: (x - mean) / sqrt(var + eps) * gamma +
+    beta with the biased (population) variance of each row."""
+    x64 = _f64(x)
+    mean = x64.mean(axis=-1, keepdims=True)
+    var = ((x64 - mean) ** 2).mean(axis=-1, keepdims=True)
+    return (x64 - mean) / np.sqrt(var + eps) * _f64(gamma) + _f64(beta)
+
+
+def linear(x, w, b=None) -> np.ndarray:
+    """nn.Linear: x W^T (+ b); w [N, K]."""
+    y = _f64(x) @ _f64(w).T
+    return y if b is None else y + _f64(b)
+
+
+def merge_heads(o) -> np.ndarray:
+    """[B, H, T, d_h] -> [B, T, H*d_h] (attn_vec of the notes)."""
+    o64 = _f64(o)
+    B, H, T, dh = o64.shape
+    return o64.transpose(0, 2, 1, 3).reshape(B, T, H * dh)
+
+
+def attn_block_out(w, attn_vec, w_o, ln_g, ln_b, pre_lnorm: bool) -> np.ndarray:
+    """After the attention: attn_out = o_net(attn_vec) (no bias); post-norm
+    LN(w + attn_out), pre-norm w + attn_out."""
+    attn_out = linear(attn_vec, w_o)
+    return _f64(w) + attn_out if pre_lnorm else layer_norm(_f64(w) + attn_out, ln_g, ln_b)
+
+
+def pos_ff(x, w1, b1, w2, b2, ln_g, ln_b, pre_lnorm: bool) -> np.ndarray:
+    """PositionwiseFF: CoreNet = Linear(d, d_inner) -> ReLU -> Linear(d_inner,
+    d); post-norm LN(x + core(x)), pre-norm x + core(LN(x))."""
+    x64 = _f64(x)
+    inp = layer_norm(x64, ln_g, ln_b) if pre_lnorm else x64
+    core = linear(np.maximum(linear(inp, w1, b1), 0.0), w2, b2)
+    return x64 + core if pre_lnorm else layer_norm(x64 + core, ln_g, ln_b)
+

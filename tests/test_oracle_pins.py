@@ -429,3 +429,65 @@ def test_mem_reset_zeroes_exactly_the_flagged_rows():
     assert np.array_equal(out[0], mem[0]) and np.array_equal(out[2], mem[2])
     assert np.array_equal(out[1], np.zeros((2, 4), dtype=np.int16))
     assert np.array_equal(oracle.mem_reset(mem, [0, 0, 0]), mem)
+
+
+# --------------------------------------------------------------------------
+# decoder-layer pieces: LayerNorm, Linear, PositionwiseFF, attention output
+# --------------------------------------------------------------------------
+def test_layer_norm_brute_force_and_invariants():
+    x = rnd(2, 3, 5)
+    g, b = rnd(5), rnd(5)
+    y = oracle.layer_norm(x, g, b)
+    for i in range(2):
+        for t in range(3):
+            row = [float(v) for v in x[i, t]]
+            mu = sum(row) / 5
+            var = sum((v - mu) ** 2 for v in row) / 5
+            for e in range(5):
+                ref = (row[e] - mu) / math.sqrt(var + 1e-5) * g[e] + b[e]
+                assert abs(y[i, t, e] - ref) < 1e-12
+    z = oracle.layer_norm(x * 100.0, np.ones(5), np.zeros(5))
+    np.testing.assert_allclose(z.mean(axis=-1), 0.0, atol=1e-12)
+    np.testing.assert_allclose((z ** 2).mean(axis=-1), 1.0, atol=1e-8)   # eps << var
+
+
+def test_linear_is_x_times_w_transpose_plus_bias():
+    x, w, b = rnd(2, 3, 4), rnd(6, 4), rnd(6)
+    y = oracle.linear(x, w, b)
+    for i in range(2):
+        for t in range(3):
+            for n in range(6):
+                assert abs(y[i, t, n] - (sum(x[i, t, c] * w[n, c] for c in range(4)) + b[n])) < 1e-12
+
+
+def test_pos_ff_special_cases():
+    d, di = 8, 16
+    x = rnd(2, 3, d)
+    g, b = rnd(d), rnd(d)
+    w1, b1, w2 = rnd(di, d), rnd(di), rnd(d, di)
+    zero2, zb = np.zeros((d, di)), np.zeros(d)
+    # a zero second layer leaves the residual path alone
+    np.testing.assert_allclose(oracle.pos_ff(x, w1, b1, zero2, zb, g, b, False),
+                               oracle.layer_norm(x, g, b), atol=1e-12)
+    np.testing.assert_array_equal(oracle.pos_ff(x, w1, b1, zero2, zb, g, b, True), x)
+    # ReLU: a first layer whose outputs are all negative contributes only b2
+    b2 = rnd(d)
+    neg = oracle.pos_ff(x, np.zeros((di, d)), -np.ones(di), w2, b2, g, b, True)
+    np.testing.assert_allclose(neg, x + b2, atol=1e-12)
+    # identity blocks: core(x) = relu(x) for d_inner = d
+    eye = np.eye(d)
+    np.testing.assert_allclose(oracle.pos_ff(x, eye, np.zeros(d), eye, zb, g, b, True),
+                               x + np.maximum(oracle.layer_norm(x, g, b), 0), atol=1e-12)
+
+
+def test_attention_output_block_special_cases():
+    B, H, T, dh = 2, 2, 3, 4
+    d = H * dh
+    w = rnd(B, T, d)
+    o = rnd(B, H, T, dh)
+    g, b = rnd(d), rnd(d)
+    vec = oracle.merge_heads(o)
+    assert vec[1, 2, 1 * dh + 3] == o[1, 1, 2, 3]
+    np.testing.assert_allclose(oracle.attn_block_out(w, vec, np.eye(d), g, b, True), w + vec, atol=1e-12)
+    np.testing.assert_allclose(oracle.attn_block_out(w, vec, np.zeros((d, d)), g, b, False),
+                               oracle.layer_norm(w, g, b), atol=1e-12)
