@@ -200,6 +200,31 @@ int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout
 int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream);
 
 /*
+ * The rest of a decoder layer ("Transformer-XL模型 核心源码阅读笔记":
+ * RelPartialLearnableMultiHeadAttn.forward after the attention, PositionwiseFF,
+ * RelPartialLearnableDecoderLayer), bf16 with fp32 accumulation:
+ *
+ * txl_linear: out [B, T, N] = relu?(x W^T + bias) + resid (nn.Linear layout,
+ *   w [N, K]); x [B, T, K] (TXL_LAYOUT_ROWS) or [B, K/64, T, 64]
+ *   (TXL_LAYOUT_HEADS: an attention output read directly as attn_vec, the
+ *   o_net input); bias [N] and resid [B, T, N] may be null.  Covers o_net
+ *   (no bias), the two CoreNet layers (bias, ReLU on the first) and, in the
+ *   pre-norm layer, their residual adds.  T a multiple of 128, K of 64, N of
+ *   256 (TXL_ERR_UNSUPPORTED); out may be resid itself, no other overlap
+ *   (TXL_ERR_ALIAS).
+ * txl_layer_norm: out [rows, d] = LayerNorm(x + y) * gamma + beta over each
+ *   row (y may be null; nn.LayerNorm: biased variance, eps inside the square
+ *   root).  d in {256, 512, 768, 1024, 1536, 2048}; out may be x or y.
+ *
+ * All pointers are device pointers, 16-byte aligned (TXL_ERR_MISALIGNED).
+ * Asynchronous on `stream`; nothing is allocated.
+ */
+int txl_linear(const void* x, int x_layout, int B, int T, int K, const void* w, int N,
+               const void* bias, const void* resid, int relu, void* out, void* stream);
+int txl_layer_norm(const void* x, const void* y, const void* gamma, const void* beta, long long rows,
+                   int d, float eps, void* out, void* stream);
+
+/*
  * Tail_M memory roll, in place ("Transformer-XL" notes, section
  * "Segment-Level Recurrence": M_{tau+1} = Tail_M([M_tau; H_tau]); source notes
  * MemTransformerLM._update_mems with ext_len = 0 and a full memory).

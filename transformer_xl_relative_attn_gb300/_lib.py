@@ -70,6 +70,10 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_workspace_bytes.restype = sz
         lib.txl_mem_update.argtypes = [vp, vp] + [i] * 5 + [vp]
         lib.txl_mem_update.restype = i
+        lib.txl_linear.argtypes = [vp, i, i, i, i, vp, i, vp, vp, i, vp, vp]
+        lib.txl_linear.restype = i
+        lib.txl_layer_norm.argtypes = [vp, vp, vp, vp, ctypes.c_longlong, i, f, vp, vp]
+        lib.txl_layer_norm.restype = i
         lib.txl_mem_update_ext.argtypes = [vp, vp] + [i] * 6 + [vp]
         lib.txl_mem_update_ext.restype = i
         lib.txl_mem_reset.argtypes = [vp, vp] + [i] * 4 + [vp]
@@ -253,6 +257,60 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
     if rc != 0:
         raise TxlError(rc, "txl_qkv_proj_ex")
     return q, k, v
+
+
+def linear(x, w, bias=None, resid=None, relu=False, out=None, stream=None):
+    """txl_linear: out [B, T, N] = relu?(x W^T + bias) + resid; x [B, T, K]
+    (rows) or [B, H, T, 64] (heads: read as [B, T, H*64]); w [N, K]; bias [N];
+    resid [B, T, N] (may be ``out``).  bf16 CUDA tensors."""
+    if x.dim() == 3:
+        B, T, K = x.shape
+        layout = 0
+    elif x.dim() == 4:
+        B, Hh, T, dh = x.shape
+        if dh != 64:
+            raise ValueError("the heads layout needs d_h = 64")
+        K, layout = Hh * dh, 1
+    else:
+        raise ValueError("x must be [B, T, K] or [B, H, T, 64]")
+    N = w.shape[0]
+    _need(x, "x", tuple(x.shape), torch.bfloat16)
+    _need(w, "w", (N, K), torch.bfloat16)
+    if bias is not None:
+        _need(bias, "bias", (N,), torch.bfloat16)
+    if resid is not None:
+        _need(resid, "resid", (B, T, N), torch.bfloat16)
+    if out is None:
+        out = torch.empty((B, T, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", (B, T, N), torch.bfloat16)
+    rc = load().txl_linear(x.data_ptr(), layout, B, T, K, w.data_ptr(), N,
+                           bias.data_ptr() if bias is not None else 0,
+                           resid.data_ptr() if resid is not None else 0, int(bool(relu)),
+                           out.data_ptr(), _stream(stream, x.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_linear")
+    return out
+
+
+def layer_norm(x, gamma, beta, y=None, eps=1e-5, out=None, stream=None):
+    """txl_layer_norm: LayerNorm(x + y) * gamma + beta over the last axis (y
+    optional); bf16 CUDA tensors; out may be x or y."""
+    d = x.shape[-1]
+    rows = x.numel() // d
+    _need(x, "x", tuple(x.shape), torch.bfloat16)
+    if y is not None:
+        _need(y, "y", tuple(x.shape), torch.bfloat16)
+    _need(gamma, "gamma", (d,), torch.bfloat16)
+    _need(beta, "beta", (d,), torch.bfloat16)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", tuple(x.shape), torch.bfloat16)
+    rc = load().txl_layer_norm(x.data_ptr(), y.data_ptr() if y is not None else 0, gamma.data_ptr(),
+                               beta.data_ptr(), rows, d, float(eps), out.data_ptr(),
+                               _stream(stream, x.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_layer_norm")
+    return out
 
 
 def r_proj(emb, w_r, H, out=None, stream=None):

@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 
 def _deps_mtime() -> float:
-    hdrs = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    hdrs = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+            glob.glob(os.path.join(INCLUDE, "*.h")))
     return max((os.path.getmtime(h) for h in hdrs), default=0.0)
 
 

@@ -75,6 +75,11 @@ struct PgParams {
     int n_tiles;    // tiles of problem 0, then of problem 1
     PgProblem pr[2];
     int* status;
+    // plain outputs only: out = act(acc + bias[col]) + resid (resid laid
+    // out like the output); null / 0 to skip
+    const __nv_bfloat16* bias;
+    const __nv_bfloat16* resid;
+    int relu;
 };
 
 struct PgShared {
@@ -257,6 +262,46 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                     const int head = nd / p.dh, e = nd - head * p.dh;
                     dst = base + (((size_t)b * p.H + head) * pr.T_out + t) * p.dh + e;
                 }
+                if (p.bias || p.relu || p.resid) {
+                    // the row-major epilogue of a plain Linear: bias, ReLU, residual
+                    float f[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) f[x] = __uint_as_float(v[x]);
+                    if (p.bias) {
+                        const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + n);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w4 = __ldg(b4 + q);
+                            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w4);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 bf = __bfloat1622float2(h2[e]);
+                                f[8 * q + 2 * e] += bf.x;
+                                f[8 * q + 2 * e + 1] += bf.y;
+                            }
+                        }
+                    }
+                    if (p.relu) {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) f[x] = fmaxf(f[x], 0.f);
+                    }
+                    if (p.resid) {
+                        const uint4* r4 = reinterpret_cast<const uint4*>(p.resid + (dst - base));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w4 = __ldg(r4 + q);
+                            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w4);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 rf = __bfloat1622float2(h2[e]);
+                                f[8 * q + 2 * e] += rf.x;
+                                f[8 * q + 2 * e + 1] += rf.y;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(f[x]);
+                }
                 uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -340,6 +385,9 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     p.dh = dh;
     p.plain = plain;
     p.status = status;
+    p.bias = nullptr;
+    p.resid = nullptr;
+    p.relu = 0;
     // Both layouts as one 4-D view (element, row t, 64-column chunk k, batch
     // row b), so the kernel loads chunk k of rows t0.. with coordinates
     // (0, t0, k, b) either way.
@@ -383,6 +431,67 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
     proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(maps[0][0], maps[0][1], maps[0][2], maps[1][0],
                                                             maps[1][1], maps[1][2], p);
+    return cudaGetLastError();
+}
+
+// A plain Linear over rows of x (layout 0: [B, T, K]; 1: [B, K / 64, T, 64]):
+// out [B, T, N] = relu?(x W^T + bias) + resid, all bf16, fp32 accumulation.
+cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const void* w, int N,
+                          const void* bias, const void* resid, int relu, void* out, int* status,
+                          cudaStream_t stream) {
+    using namespace pg;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap maps[3];
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)(K / BK), (cuuint64_t)B};
+        const cuuint64_t row = x_heads ? (cuuint64_t)BK * 2 : (cuuint64_t)K * 2;
+        const cuuint64_t chunk = x_heads ? (cuuint64_t)T * BK * 2 : (cuuint64_t)BK * 2;
+        const cuuint64_t strides[3] = {row, chunk, (cuuint64_t)T * K * 2};
+        const cuuint32_t box[4] = {BK, BM, 1, 1};
+        if (!pg_encode(&maps[0], x, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {BK, BN};
+        if (!pg_encode(&maps[2], w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    maps[1] = maps[0];
+    PgParams p;
+    p.B = B;
+    p.K = K;
+    p.d = N;   // one output, row-major [B, T, N]
+    p.H = 1;
+    p.dh = N;
+    p.plain = 1;
+    p.status = status;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.resid = static_cast<const __nv_bfloat16*>(resid);
+    p.relu = relu;
+    PgProblem& pr = p.pr[0];
+    pr.Ta = 0;
+    pr.Tb = T;
+    pr.N = N;
+    pr.T_out = T;
+    pr.n_rt = T / BM;
+    pr.n_nt = N / BN;
+    const long long tiles = (long long)B * pr.n_rt * pr.n_nt;
+    if (tiles <= 0 || tiles > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    pr.tiles = (int)tiles;
+    pr.out[0] = static_cast<__nv_bfloat16*>(out);
+    pr.out[1] = pr.out[2] = nullptr;
+    p.pr[1] = pr;
+    p.pr[1].tiles = 0;
+    p.n_tiles = (int)tiles;
+    const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
+    proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[0], maps[1],
+                                                            maps[2], p);
     return cudaGetLastError();
 }
 

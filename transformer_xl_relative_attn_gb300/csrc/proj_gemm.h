@@ -27,4 +27,11 @@ struct ProjGemm {
 cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
                              int plain, int* status, cudaStream_t stream);
 
+// A plain Linear over rows of x (x_heads = 0: [B, T, K]; 1: [B, K / 64, T,
+// 64]): out [B, T, N] = relu?(x W^T + bias) + resid (bias [N] and resid
+// [B, T, N] may be null).  T a multiple of 128, K of 64, N of 256.
+cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const void* w, int N,
+                          const void* bias, const void* resid, int relu, void* out, int* status,
+                          cudaStream_t stream);
+
 }  // namespace txl

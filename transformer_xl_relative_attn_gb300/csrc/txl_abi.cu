@@ -17,6 +17,8 @@ cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride
                           size_t row_bytes, cudaStream_t stream);
 cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long long per_b_bytes,
                              cudaStream_t stream);
+cudaError_t launch_layer_norm(const void* x, const void* y, const void* gamma, const void* beta,
+                              long long rows, int d, float eps, void* out, cudaStream_t stream);
 cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
                                  const float* ub, const float* vb, int B, int H, int L, int M,
                                  int dh, float scale, int lo_shift, float* out, cudaStream_t stream);
@@ -304,6 +306,43 @@ int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_
     cudaError_t e = txl::launch_proj_gemm(&gm, 1, 1, (int)d, (int)d, H, d_h, 1, status,
                                           static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_linear(const void* x, int x_layout, int B, int T, int K, const void* w, int N,
+               const void* bias, const void* resid, int relu, void* out, void* stream) {
+    if (!x || !w || !out || B <= 0 || T <= 0 || K <= 0 || N <= 0) return TXL_ERR_INVALID_ARG;
+    if (x_layout != TXL_LAYOUT_ROWS && x_layout != TXL_LAYOUT_HEADS) return TXL_ERR_INVALID_ARG;
+    if (T % 128 != 0 || K % 64 != 0 || N % 256 != 0) return TXL_ERR_UNSUPPORTED;
+    if ((long long)B * T * (K > N ? K : N) >= (1ll << 31) || (long long)T >= (1ll << 24))
+        return TXL_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (bias && !aligned16(bias)) ||
+        (resid && !aligned16(resid)))
+        return TXL_ERR_MISALIGNED;
+    const size_t nx = (size_t)B * T * K * 2, nw = (size_t)N * K * 2, no = (size_t)B * T * N * 2;
+    if (overlap(out, no, x, nx) || overlap(out, no, w, nw) || (bias && overlap(out, no, bias, (size_t)N * 2)))
+        return TXL_ERR_ALIAS;
+    if (resid && resid != out && overlap(out, no, resid, no)) return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    const cudaError_t e = txl::launch_linear(x, x_layout == TXL_LAYOUT_HEADS, B, T, K, w, N, bias, resid,
+                                             relu ? 1 : 0, out, status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_layer_norm(const void* x, const void* y, const void* gamma, const void* beta, long long rows,
+                   int d, float eps, void* out, void* stream) {
+    if (!x || !gamma || !beta || !out || rows < 0 || d <= 0 || !(eps >= 0.f)) return TXL_ERR_INVALID_ARG;
+    if (d % 256 != 0 || d > 2048 || d == 1280 || d == 1792) return TXL_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) || (y && !aligned16(y)))
+        return TXL_ERR_MISALIGNED;
+    const size_t n = (size_t)rows * d * 2;
+    if ((out != x && overlap(out, n, x, n)) || (y && out != y && overlap(out, n, y, n)) ||
+        overlap(out, n, gamma, (size_t)d * 2) || overlap(out, n, beta, (size_t)d * 2))
+        return TXL_ERR_ALIAS;
+    const cudaError_t e =
+        txl::launch_layer_norm(x, y, gamma, beta, rows, d, eps, out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 

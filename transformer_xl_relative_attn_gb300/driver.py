@@ -230,3 +230,134 @@ class AttnStack:
         for m, s in zip(self.mems, sd["mems"]):
             m.copy_(s)
         self.segments_done = int(sd.get("segments_done", 0))
+
+
+class DecoderStack:
+    """Full Transformer-XL decoder layers over per-layer recurrence memories
+    ("Transformer-XL模型 核心源码阅读笔记": RelPartialLearnableDecoderLayer =
+    RelPartialLearnableMultiHeadAttn then PositionwiseFF; MemTransformerLM keeps
+    each layer's input as that layer's memory), every step in libtxl.so.  Per
+    segment and layer n, with h the layer input [B, L, d] (rows):
+
+      post-norm (pre_lnorm = False, the notes' default):
+        q, k, v = txl_qkv_proj(h, mems[n])          roll mems[n] with h
+        o   = txl_attn_fwd(q, k, v, r_k[n], u[n], v[n])          [B, H, L, d_h]
+        h1  = LN1(h + o_net(o))                     txl_linear (heads input) + txl_layer_norm
+        h   = LN2(h1 + W2 relu(W1 h1 + b1) + b2)    txl_linear x2 + txl_layer_norm
+      pre-norm:
+        q, k, v = txl_qkv_proj(LN1(h), LN1(mems[n]))
+        h1  = h + o_net(o)                          residual fused into txl_linear
+        h   = h1 + W2 relu(W1 LN2(h1) + b1) + b2
+
+    ``layers[n]`` holds bf16 CUDA tensors: w_qkv [3d, d], w_o [d, d], ln1_g,
+    ln1_b, ln2_g, ln2_b [d], w1 [d_inner, d], b1 [d_inner], w2 [d, d_inner],
+    b2 [d] (nn.Linear layouts).  Memories are rows [B, M, d].  One stream
+    orders every dependency; activations ping-pong between two buffers (a
+    layer's input is dead once its memory has been rolled and its residuals
+    read).
+    """
+
+    _keys = ("w_qkv", "w_o", "ln1_g", "ln1_b", "w1", "b1", "w2", "b2", "ln2_g", "ln2_b")
+
+    def __init__(self, layers: Sequence[dict], r_k: Sequence[torch.Tensor], u: Sequence[torch.Tensor],
+                 v_bias: Sequence[torch.Tensor], mems: Sequence[torch.Tensor], scale: float, n_head: int,
+                 seg_len: int, pre_lnorm: bool = False, stream: torch.cuda.Stream | None = None,
+                 same_length: bool = False, ext_len: int = 0, eps: float = 1e-5):
+        n = len(mems)
+        if not (len(layers) == len(r_k) == len(u) == len(v_bias) == n) or n == 0:
+            raise ValueError("need one parameter set, r_k, u, v and memory per layer")
+        B, M, d = mems[0].shape
+        for m in mems:
+            if m.shape != (B, M, d) or not m.is_cuda or not m.is_contiguous() or m.dtype != torch.bfloat16:
+                raise ValueError("memories must be contiguous bf16 CUDA tensors [B, M, d]")
+        for lp in layers:
+            missing = [k for k in self._keys if k not in lp]
+            if missing:
+                raise ValueError(f"layer parameters missing {missing}")
+        self.layers = [dict(lp) for lp in layers]
+        self.r_k, self.u, self.v_bias, self.mems = list(r_k), list(u), list(v_bias), list(mems)
+        self.scale, self.H, self.L, self.B, self.M, self.d = float(scale), n_head, int(seg_len), B, M, d
+        self.dh = d // n_head
+        self.d_inner = self.layers[0]["w1"].shape[0]
+        self.pre_lnorm, self.same_length, self.ext_len, self.eps = bool(pre_lnorm), bool(same_length), int(ext_len), eps
+        dev = mems[0].device
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        L, H, dh = self.L, self.H, self.dh
+        self.q = torch.empty((B, H, L, dh), **bf)
+        self.k = torch.empty((B, H, M + L, dh), **bf)
+        self.v = torch.empty((B, H, M + L, dh), **bf)
+        self.o = torch.empty((B, H, L, dh), **bf)
+        self.h1 = torch.empty((B, L, d), **bf)
+        self.f1 = torch.empty((B, L, self.d_inner), **bf)
+        self.t = torch.empty((B, L, d), **bf)
+        self.act = [torch.empty((B, L, d), **bf), torch.empty((B, L, d), **bf)]
+        if self.pre_lnorm:
+            self.hn = torch.empty((B, L, d), **bf)
+            self.mn = torch.empty((B, M, d), **bf)
+        self.segments_done = 0
+
+    @property
+    def n_layers(self) -> int:
+        return len(self.mems)
+
+    def run_segment(self, h0: torch.Tensor, trace: list | None = None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+        """One segment through every layer; h0 [B, L, d] bf16 on the device.
+        Returns the last layer's output [B, L, d] (``out`` if given, else a
+        buffer the next segment overwrites).  ``trace`` (tests) collects the
+        inputs and outputs of every step."""
+        if h0.shape != (self.B, self.L, self.d):
+            raise ValueError(f"h0 must be [{self.B}, {self.L}, {self.d}]")
+        st, eps = self.stream, self.eps
+        h = h0
+        with torch.cuda.stream(st):
+            for n, mem in enumerate(self.mems):
+                lp = self.layers[n]
+                rec = {"n": n, "h": h.clone(), "mem": mem.clone()} if trace is not None else None
+                if self.pre_lnorm:
+                    _lib.layer_norm(h, lp["ln1_g"], lp["ln1_b"], eps=eps, out=self.hn, stream=st)
+                    _lib.layer_norm(mem, lp["ln1_g"], lp["ln1_b"], eps=eps, out=self.mn, stream=st)
+                    _lib.qkv_proj(self.hn, self.mn, lp["w_qkv"], self.H, q=self.q, k=self.k, v=self.v, stream=st)
+                else:
+                    _lib.qkv_proj(h, mem, lp["w_qkv"], self.H, q=self.q, k=self.k, v=self.v, stream=st)
+                _roll(mem, h, st, self.ext_len)
+                _lib.attn_fwd(self.q, self.k, self.v, self.r_k[n], self.u[n], self.v_bias[n], self.scale,
+                              out=self.o, stream=st, same_length=self.same_length, mem_len=self.M)
+                last = n == len(self.mems) - 1
+                dst = out if (out is not None and last) else self.act[(n + 1) % 2] if h is not self.act[(n + 1) % 2] \
+                    else self.act[n % 2]
+                if self.pre_lnorm:
+                    _lib.linear(self.o, lp["w_o"], resid=h, out=self.h1, stream=st)
+                    _lib.layer_norm(self.h1, lp["ln2_g"], lp["ln2_b"], eps=eps, out=self.t, stream=st)
+                    _lib.linear(self.t, lp["w1"], bias=lp["b1"], relu=True, out=self.f1, stream=st)
+                    _lib.linear(self.f1, lp["w2"], bias=lp["b2"], resid=self.h1, out=dst, stream=st)
+                else:
+                    _lib.linear(self.o, lp["w_o"], out=self.t, stream=st)
+                    _lib.layer_norm(h, lp["ln1_g"], lp["ln1_b"], y=self.t, eps=eps, out=self.h1, stream=st)
+                    _lib.linear(self.h1, lp["w1"], bias=lp["b1"], relu=True, out=self.f1, stream=st)
+                    _lib.linear(self.f1, lp["w2"], bias=lp["b2"], out=self.t, stream=st)
+                    _lib.layer_norm(self.h1, lp["ln2_g"], lp["ln2_b"], y=self.t, eps=eps, out=dst, stream=st)
+                if rec is not None:
+                    rec.update(q=self.q.clone(), k=self.k.clone(), v=self.v.clone(), o=self.o.clone(),
+                               h1=self.h1.clone(), f1=self.f1.clone(), out=dst.clone())
+                    if self.pre_lnorm:
+                        rec.update(hn=self.hn.clone(), mn=self.mn.clone(), h1n=self.t.clone())
+                    trace.append(rec)
+                h = dst
+        self.segments_done += 1
+        return h
+
+    def reset_rows(self, flags: torch.Tensor) -> None:
+        """Zeroes every layer's memory of the flagged batch rows."""
+        with torch.cuda.stream(self.stream):
+            for m in self.mems:
+                _lib.mem_reset(m, flags, stream=self.stream)
+
+    def state_dict(self) -> dict:
+        return {"mems": [m.detach().clone() for m in self.mems], "segments_done": self.segments_done}
+
+    def load_state_dict(self, sd: dict) -> None:
+        for m, s in zip(self.mems, sd["mems"]):
+            m.copy_(s)
+        self.segments_done = int(sd.get("segments_done", 0))
