@@ -380,6 +380,8 @@ def run_ours(args, wl: W.Workload):
             # call copied in, every output copied out
             result["e2e_attn_calls"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb,
                                                    scratch, flops_step, ws)
+            if wl.d % 256 == 0 and wl.d <= 2048:
+                result["decoder_stack"] = measure_decoder(args, wl, dev, flops_step, ws)
         else:
             result["e2e"] = measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch,
                                         flops_step, ws)
@@ -643,6 +645,83 @@ def measure_e2e_stack(args, wl, dev, flops_step, ws):
             "tokens_per_s": round(ws * wl.B * wl.L * S * steps / el, 1),
             "api": "AttnStack.run_segment per segment (txl_qkv_proj_ex, txl_mem_update, txl_attn_fwd "
                    "per layer); host hidden states in, last layer's attention output out"}
+
+
+def measure_decoder(args, wl, dev, flops_step, ws, d_inner_mult=4):
+    """Full decoder layers (DecoderStack, post-norm: attention, o_net,
+    LayerNorm, feed-forward with d_inner = 4 d, LayerNorm) over the same
+    segments, end to end with host I/O as in measure_e2e_stack.  Reports
+    tokens/s and the attention TFLOP/s that this step sustains."""
+    import transformer_xl_relative_attn_gb300 as txl
+    bf = torch.bfloat16
+    stream = torch.cuda.Stream(device=dev)
+    d, H, L, M = wl.d, wl.H, wl.L, wl.M
+    di = d_inner_mult * d
+    g = torch.Generator().manual_seed(7)
+
+    def n(*shape, std):
+        return torch.empty(shape).normal_(0.0, std, generator=g).to(dev, bf)
+
+    with torch.cuda.stream(stream):
+        layers = [{"w_qkv": n(3 * d, d, std=0.02), "w_o": n(d, d, std=0.02),
+                   "ln1_g": torch.ones(d, dtype=bf, device=dev), "ln1_b": torch.zeros(d, dtype=bf, device=dev),
+                   "w1": n(di, d, std=0.02), "b1": n(di, std=0.02), "w2": n(d, di, std=0.02),
+                   "b2": n(d, std=0.02), "ln2_g": torch.ones(d, dtype=bf, device=dev),
+                   "ln2_b": torch.zeros(d, dtype=bf, device=dev)} for _ in range(wl.layers)]
+        emb = W.sinusoid(torch.arange(M + L - 1, -1, -1), d).to(dev, bf)
+        r_k = [txl.r_proj(emb, n(d, d, std=0.02), H, stream=stream) for _ in range(wl.layers)]
+        u = [n(H, wl.dh, std=0.02)] * wl.layers
+        vb = [n(H, wl.dh, std=0.02)] * wl.layers
+        mems = [n(wl.B, M, d, std=1.0) for _ in range(wl.layers)]
+    stream.synchronize()
+    stack = txl.DecoderStack(layers, r_k, u, vb, mems, wl.scale, H, L, stream=stream)
+    S = wl.segments
+    h_host = [W.segment_input(wl, s).to(bf).pin_memory() for s in range(S)]
+    h_dev = [torch.empty(h.shape, dtype=bf, device=dev) for h in h_host]
+    o_dev = [torch.empty(h.shape, dtype=bf, device=dev) for h in h_host]
+    o_host = [torch.empty(h.shape, dtype=bf).pin_memory() for h in h_host]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    steps = max(3, min(args.steps, 10))
+
+    def one():
+        arrived = [torch.cuda.Event() for _ in range(S)]
+        with torch.cuda.stream(up):
+            for s in range(S):
+                h_dev[s].copy_(h_host[s], non_blocking=True)
+                arrived[s].record(up)
+        for s in range(S):
+            stream.wait_event(arrived[s])
+            stack.run_segment(h_dev[s], out=o_dev[s])
+            written = torch.cuda.Event()
+            written.record(stream)
+            down.wait_event(written)
+            with torch.cuda.stream(down):
+                o_host[s].copy_(o_dev[s], non_blocking=True)
+        for st in (stream, down):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            up.wait_event(ev)
+            stream.wait_event(ev)
+
+    one()
+    torch.cuda.synchronize()
+    txl.check_status()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = reduce_max(time.perf_counter() - t0, ws)
+    txl.check_status()
+    # dense flops of the layer besides attention: qkv, o_net, two FF layers
+    T = wl.B * L
+    other = 2 * wl.layers * S * (T * d * d + wl.B * (M + L) * 2 * d * d + T * d * d + 2 * T * d * di)
+    return {"ms_per_step": round(1e3 * el / steps, 3),
+            "tokens_per_s": round(ws * wl.B * L * S * steps / el, 1),
+            "attn_tflops": round(ws * flops_step * steps / el / 1e12, 3),
+            "all_matmul_tflops": round(ws * (flops_step + other) * steps / el / 1e12, 3),
+            "d_inner": di, "norm": "post", "steps": steps,
+            "api": "DecoderStack.run_segment per segment; host hidden states in, last layer output out"}
 
 
 def cpu_baseline_and_parity(wl, calls, rks, u, vb):
