@@ -567,7 +567,9 @@ def build_stack(wl, dev, stream):
     """An AttnStack of the workload's layers with the library's own
     projections: W_q, W_k, W_v stacked in the nn.Linear layout, r_k of every
     layer projected once by txl_r_proj from the sinusoid of distances
-    M+L-1 .. 0, layer 0's memory in rows, the others in heads."""
+    M+L-1 .. 0, layer 0's memory in rows, the others in heads.  When L < M
+    the memories are ring buffers (each segment writes L rows instead of
+    moving M)."""
     import transformer_xl_relative_attn_gb300 as txl
     bf = torch.bfloat16
     p = W.make_params(wl)
@@ -581,7 +583,8 @@ def build_stack(wl, dev, stream):
         m0 = W.initial_memories(wl)
         mems = [m0[0].to(dev, bf)] + [W._split_heads(m, H).to(dev, bf) for m in m0[1:]]
     stream.synchronize()
-    return txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, wl.L, stream=stream)
+    ring = wl.L < wl.M and wl.L % 128 == 0 and wl.M % 128 == 0
+    return txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, wl.L, stream=stream, ring=ring)
 
 
 def measure_e2e_stack(args, wl, dev, flops_step, ws):
@@ -643,8 +646,10 @@ def measure_e2e_stack(args, wl, dev, flops_step, ws):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1e3 * el / steps, 3),
             "tokens_per_s": round(ws * wl.B * wl.L * S * steps / el, 1),
-            "api": "AttnStack.run_segment per segment (txl_qkv_proj_ex, txl_mem_update, txl_attn_fwd "
-                   "per layer); host hidden states in, last layer's attention output out"}
+            "api": "AttnStack.run_segment per segment (txl_qkv_proj_ring, txl_mem_update or "
+                   "txl_mem_ring_push, txl_attn_fwd per layer); host hidden states in, last layer's "
+                   "attention output out",
+            "memory": "ring buffer" if stack.ring else "Tail_M copy"}
 
 
 def measure_decoder(args, wl, dev, flops_step, ws, d_inner_mult=4):

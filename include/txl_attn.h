@@ -197,6 +197,28 @@ int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L
 int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout,
                     const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
                     void* v, void* stream);
+
+/*
+ * Ring-buffer memory (the survey's alternative to the Tail_M copy): a memory
+ * of M rows whose logical row t is stored at row (start + t) mod M.
+ *
+ * txl_qkv_proj_ring: txl_qkv_proj_ex reading mem as a ring starting at
+ *   mem_start (0 <= mem_start < M, a multiple of 128: every 128-row tile of
+ *   the ring is then contiguous; TXL_ERR_UNSUPPORTED otherwise).  Same result
+ *   as txl_qkv_proj_ex on the logical (unrotated) memory.
+ * txl_mem_ring_push: the ring counterpart of txl_mem_update.  For L < M the
+ *   L rows of hids [B, L, d] overwrite the ring's L oldest rows (hids row r
+ *   at ring row (start + r) mod M) and *new_start = (start + L) mod M: L rows
+ *   are written instead of M moved.  For L >= M the ring is refilled with the
+ *   newest M rows and *new_start = 0.  The logical memory afterwards equals
+ *   txl_mem_update's result.  Arguments and errors as txl_mem_update, plus
+ *   start in [0, M) (TXL_ERR_INVALID_ARG) and new_start a host pointer.
+ */
+int txl_qkv_proj_ring(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+                      const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
+                      void* v, void* stream);
+int txl_mem_ring_push(void* ring, const void* hids, int B, int L, int M, int d, int start,
+                      int* new_start, int dtype, void* stream);
 int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream);
 
 /*

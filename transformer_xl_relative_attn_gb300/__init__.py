@@ -5,6 +5,7 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
     attn_fwd, attn_fwd_ws, attn_workspace_bytes   relative attention forward
     attn_fwd_noalloc                              the same with the library's static scratch
     mem_update, mem_reset                         Tail_M memory roll (ext_len), per-row reset, in place
+    mem_ring_push                                 ring-buffer memory update (qkv_proj reads the ring)
     qkv_proj, r_proj                              head-split input projections (tensor cores)
     linear, layer_norm                            o_net / feed-forward GEMMs, fused residual LayerNorm
     sync_status, check_status                     device status word
@@ -14,12 +15,12 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
 """
 from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
                    attn_workspace_bytes,
-                   check_status, debug_inject, header_functions, layer_norm, linear, load, mem_reset, mem_update, qkv_proj, r_proj,
+                   check_status, debug_inject, header_functions, layer_norm, linear, load, mem_reset, mem_ring_push, mem_update, qkv_proj, r_proj,
                    status_string,
                    sync_status, version, LIB_PATH)
 from .driver import AttnStack, DecoderStack, SegmentDriver
 
 __all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
            "attn_workspace_bytes",
-           "check_status", "debug_inject", "header_functions", "layer_norm", "linear", "load", "mem_reset", "mem_update", "qkv_proj", "r_proj",
+           "check_status", "debug_inject", "header_functions", "layer_norm", "linear", "load", "mem_reset", "mem_ring_push", "mem_update", "qkv_proj", "r_proj",
            "status_string", "sync_status", "version", "SegmentDriver", "AttnStack", "DecoderStack", "LIB_PATH"]

@@ -64,6 +64,10 @@ def load() -> ctypes.CDLL:
         lib.txl_qkv_proj.restype = i
         lib.txl_qkv_proj_ex.argtypes = [vp, i, vp, i, vp] + [i] * 5 + [vp] * 4
         lib.txl_qkv_proj_ex.restype = i
+        lib.txl_qkv_proj_ring.argtypes = [vp, i, vp, i, i, vp] + [i] * 5 + [vp] * 4
+        lib.txl_qkv_proj_ring.restype = i
+        lib.txl_mem_ring_push.argtypes = [vp, vp] + [i] * 5 + [ctypes.POINTER(ctypes.c_int), i, vp]
+        lib.txl_mem_ring_push.restype = i
         lib.txl_r_proj.argtypes = [vp, vp] + [i] * 3 + [vp, vp]
         lib.txl_r_proj.restype = i
         lib.txl_attn_workspace_bytes.argtypes = [i] * 6
@@ -213,11 +217,13 @@ def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
     return out
 
 
-def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
+def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0):
     """txl_qkv_proj_ex: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
     h is [B, L, d] (rows) or [B, H, L, d_h] (heads: an attention output),
     mem likewise [B, M, d] or [B, H, M, d_h] (M may be 0); w_qkv [3d, d]; bf16
-    CUDA tensors.  Returns (q [B, H, L, d_h], k, v [B, H, M+L, d_h])."""
+    CUDA tensors.  mem_start: mem is a ring whose logical row 0 is stored at
+    row mem_start (txl_qkv_proj_ring).  Returns (q [B, H, L, d_h], k, v
+    [B, H, M+L, d_h])."""
     if h.dim() == 3:
         B, L, d = h.shape
         h_layout = 0
@@ -251,11 +257,11 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None):
     _need(q, "q", (B, H, L, dh), torch.bfloat16)
     _need(k, "k", (B, H, M + L, dh), torch.bfloat16)
     _need(v, "v", (B, H, M + L, dh), torch.bfloat16)
-    rc = load().txl_qkv_proj_ex(h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
-                                w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                _stream(stream, h.device))
+    rc = load().txl_qkv_proj_ring(h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
+                                  int(mem_start), w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(),
+                                  k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
     if rc != 0:
-        raise TxlError(rc, "txl_qkv_proj_ex")
+        raise TxlError(rc, "txl_qkv_proj_ring")
     return q, k, v
 
 
@@ -349,6 +355,23 @@ def mem_update(mems: torch.Tensor, hids: torch.Tensor, stream=None, ext_len: int
     if rc != 0:
         raise TxlError(rc, "txl_mem_update")
     return mems
+
+
+def mem_ring_push(ring: torch.Tensor, hids: torch.Tensor, start: int, stream=None) -> int:
+    """txl_mem_ring_push: ring [B, M, d] (logical row t at row (start+t) % M)
+    takes the rows of hids [B, L, d]; returns the new start."""
+    if ring.dim() != 3 or hids.dim() != 3:
+        raise ValueError("ring must be [B, M, d] and hids [B, L, d]")
+    B, M, d = ring.shape
+    L = hids.shape[1]
+    _need(ring, "ring", (B, M, d), ring.dtype)
+    _need(hids, "hids", (B, L, d), ring.dtype)
+    new = ctypes.c_int(0)
+    rc = load().txl_mem_ring_push(ring.data_ptr(), hids.data_ptr(), B, L, M, d, int(start), ctypes.byref(new),
+                                  _dtype_code(ring), _stream(stream, ring.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_mem_ring_push")
+    return int(new.value)
 
 
 def mem_reset(mems: torch.Tensor, flags: torch.Tensor, stream=None) -> torch.Tensor:

@@ -136,6 +136,49 @@ cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride
     return go(uint16_t{});
 }
 
+// Ring-buffer memory (L < M): the L new rows of each batch row overwrite the
+// L oldest rows of the ring, row r of h landing at ring row (start + r) mod M;
+// the ring then starts at (start + L) mod M.  The logical memory (ring read
+// from its start) equals the Tail_M roll of [mem; h], at the cost of writing
+// L rows instead of moving M.  One thread per vector.
+template <typename V, typename I>
+__global__ void __launch_bounds__(256) ring_push_kernel(V* __restrict__ ring, const V* __restrict__ hid,
+                                                        int L, int M, int start, I rowv, I total) {
+    const I e = (I)blockIdx.x * 256 + threadIdx.x;
+    if (e >= total) return;
+    const I col = e % rowv;
+    const I br = e / rowv;  // (b, r) of the source row
+    const int r = (int)(br % (I)L);
+    const I b = br / (I)L;
+    int pos = start + r;
+    if (pos >= M) pos -= M;
+    ring[(b * (I)M + pos) * rowv + col] = hid[e];
+}
+
+cudaError_t launch_ring_push(void* ring, const void* hid, int B, int L, int M, int start,
+                             size_t row_bytes, cudaStream_t stream) {
+    auto go = [&](auto tag) -> cudaError_t {
+        using V = decltype(tag);
+        const long long rowv = (long long)(row_bytes / sizeof(V));
+        const long long total = (long long)B * L * rowv, rsz = (long long)B * M * rowv;
+        const long long blocks = (total + 255) / 256;
+        if (total == 0) return cudaSuccess;
+        if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+        if (rsz < 0x7FFFFFFFll - 256)
+            ring_push_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<V*>(ring), static_cast<const V*>(hid), L, M, start, (int)rowv, (int)total);
+        else
+            ring_push_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<V*>(ring), static_cast<const V*>(hid), L, M, start, rowv, total);
+        return cudaGetLastError();
+    };
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ring) | reinterpret_cast<uintptr_t>(hid);
+    if (row_bytes % 16 == 0 && a % 16 == 0) return go(uint4{});
+    if (row_bytes % 8 == 0 && a % 8 == 0) return go(uint2{});
+    if (row_bytes % 4 == 0 && a % 4 == 0) return go(uint32_t{});
+    return go(uint16_t{});
+}
+
 cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long long per_b_bytes,
                              cudaStream_t stream) {
     auto go = [&](auto tag) -> cudaError_t {

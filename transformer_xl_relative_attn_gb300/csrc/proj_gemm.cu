@@ -61,6 +61,7 @@ constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0);
 // then Tb rows of source b (current), times the problem's weights.
 struct PgProblem {
     int Ta, Tb;     // rows per batch from source a, then source b (Ta a multiple of BM)
+    int a_start;    // source a is a ring: logical row t is stored at row (a_start + t) % Ta
     int N;          // output columns (a multiple of BN)
     int T_out;      // rows per (batch, head) of the outputs
     int n_rt, n_nt, tiles;
@@ -159,7 +160,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                 const int Ta = p.pr[g].Ta;
                 // a row tile lies wholly in one source (Ta is a multiple of BM)
                 const CUtensorMap* mA = t0 < Ta ? (g ? &tmA1 : &tmA0) : (g ? &tmB1 : &tmB0);
-                const int ta = t0 < Ta ? t0 : t0 - Ta;
+                // a_start and t0 are multiples of BM, so a ring tile never wraps
+                const int ta = t0 < Ta ? (t0 + p.pr[g].a_start) % Ta : t0 - Ta;
                 const CUtensorMap* mW = g ? &tmW1 : &tmW0;
                 for (int k = 0; k < ksteps; ++k, ++c) {
                     const int s = c % STAGES;
@@ -417,6 +419,7 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         PgProblem& pr = p.pr[g];
         pr.Ta = q.Ta;
         pr.Tb = q.Tb;
+        pr.a_start = q.a_start;
         pr.N = q.N;
         pr.T_out = q.T_out;
         pr.n_rt = (q.Ta + q.Tb) / BM;
@@ -477,6 +480,7 @@ cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const
     PgProblem& pr = p.pr[0];
     pr.Ta = 0;
     pr.Tb = T;
+    pr.a_start = 0;
     pr.N = N;
     pr.T_out = T;
     pr.n_rt = T / BM;

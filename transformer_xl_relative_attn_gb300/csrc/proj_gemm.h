@@ -16,6 +16,7 @@ struct ProjGemm {
     int N;
     int T_out;             // rows per (batch row, head) of the outputs
     void* out[3];          // output column c -> out[c / d]
+    int a_start;           // a_src is a ring of Ta rows starting at this row (a multiple of 128)
 };
 
 // One launch of up to two projection GEMMs: out[c / d] <- rows of [a_src;

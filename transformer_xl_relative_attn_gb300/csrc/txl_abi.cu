@@ -17,6 +17,8 @@ cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride
                           size_t row_bytes, cudaStream_t stream);
 cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long long per_b_bytes,
                              cudaStream_t stream);
+cudaError_t launch_ring_push(void* ring, const void* hid, int B, int L, int M, int start,
+                             size_t row_bytes, cudaStream_t stream);
 cudaError_t launch_layer_norm(const void* x, const void* y, const void* gamma, const void* beta,
                               long long rows, int d, float eps, void* out, cudaStream_t stream);
 cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
@@ -202,6 +204,31 @@ int txl_mem_update_ext(void* mems, const void* hids, int B, int L, int M, int d,
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 
+int txl_mem_ring_push(void* ring, const void* hids, int B, int L, int M, int d, int start,
+                      int* new_start, int dtype, void* stream) {
+    const int es = elem_size(dtype);
+    if (!es || B <= 0 || L <= 0 || M < 0 || d <= 0 || !new_start) return TXL_ERR_INVALID_ARG;
+    if (start < 0 || (M > 0 && start >= M) || (M == 0 && start != 0)) return TXL_ERR_INVALID_ARG;
+    if (M == 0) {
+        *new_start = 0;
+        return TXL_OK;
+    }
+    if (!ring || !hids) return TXL_ERR_INVALID_ARG;
+    if ((long long)B * (M > L ? M : L) * d >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    const size_t row = (size_t)d * es;
+    if (overlap(ring, (size_t)B * M * row, hids, (size_t)B * L * row)) return TXL_ERR_ALIAS;
+    cudaError_t e;
+    if (L >= M) {
+        // the whole memory is replaced by the newest M rows: the Tail_M copy
+        e = txl::launch_tail_m(ring, hids, B, L, L, M, row, static_cast<cudaStream_t>(stream));
+        *new_start = 0;
+    } else {
+        e = txl::launch_ring_push(ring, hids, B, L, M, start, row, static_cast<cudaStream_t>(stream));
+        *new_start = (start + L) % M;
+    }
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
 int txl_mem_reset(void* mems, const void* flags, int B, int rows, int d, int dtype, void* stream) {
     const int es = elem_size(dtype);
     if (!es || B <= 0 || rows < 0 || d <= 0 || !flags) return TXL_ERR_INVALID_ARG;
@@ -255,9 +282,18 @@ int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L
 int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout,
                     const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
                     void* v, void* stream) {
+    return txl_qkv_proj_ring(h, h_layout, mem, mem_layout, 0, w_qkv, B, L, M, H, d_h, q, k, v, stream);
+}
+
+int txl_qkv_proj_ring(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+                      const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
+                      void* v, void* stream) {
     if (!h || !w_qkv || !q || !k || !v || (M > 0 && !mem)) return TXL_ERR_INVALID_ARG;
     const auto layout_ok = [](int l) { return l == TXL_LAYOUT_ROWS || l == TXL_LAYOUT_HEADS; };
     if (!layout_ok(h_layout) || !layout_ok(mem_layout)) return TXL_ERR_INVALID_ARG;
+    if (mem_start < 0 || (M > 0 && mem_start >= M) || (M == 0 && mem_start != 0))
+        return TXL_ERR_INVALID_ARG;
+    if (mem_start % 128 != 0) return TXL_ERR_UNSUPPORTED;
     if (B <= 0 || L <= 0 || M < 0 || H <= 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
     if (d_h != 64 || H % 4 != 0 || L % 128 != 0 || M % 128 != 0) return TXL_ERR_UNSUPPORTED;
     const long long d = (long long)H * d_h;
@@ -286,7 +322,7 @@ int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout
     const txl::ProjGemm gm[2] = {
         {nullptr, h, 0, L, 0, hh, w, (int)d, L, {q, nullptr, nullptr}},
         {M > 0 ? mem : nullptr, h, M, L, mh, hh, w + (size_t)d * d * 2, (int)(2 * d), M + L,
-         {k, v, nullptr}}};
+         {k, v, nullptr}, mem_start}};
     cudaError_t e = txl::launch_proj_gemm(gm, 2, B, (int)d, (int)d, H, d_h, 0, status, st);
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;

@@ -101,6 +101,15 @@ class SegmentDriver:
         self.segments_done = int(sd.get("segments_done", 0))
 
 
+def _push(mem: torch.Tensor, h: torch.Tensor, start: int, stream) -> int:
+    """Ring-buffer update of one memory with the layer input h (either
+    layout); returns the new ring start."""
+    if mem.dim() == 4:
+        B, H, M, dh = mem.shape
+        return _lib.mem_ring_push(mem.view(B * H, M, dh), h.view(B * H, h.shape[2], dh), start, stream=stream)
+    return _lib.mem_ring_push(mem, h, start, stream=stream)
+
+
 def _roll(mem: torch.Tensor, h: torch.Tensor, stream, ext_len: int = 0) -> None:
     """Tail_M roll of one memory with the layer input h, in either layout:
     rows ([B, M, d] with [B, L, d]) or heads ([B, H, M, d_h] with
@@ -136,7 +145,11 @@ class AttnStack:
     query attends over the same number of keys, txl_attn_fwd_ex with mem_len
     = M), ``ext_len`` (the last ext_len rows of each segment stay out of the
     memory, txl_mem_update_ext), and ``reset_rows`` (per-row memory reset at
-    document boundaries, txl_mem_reset).
+    document boundaries, txl_mem_reset).  With ``ring`` the memories are ring
+    buffers sharing one start row: the projections read them through
+    txl_qkv_proj_ring and txl_mem_ring_push writes each segment's L rows over
+    the oldest ones instead of moving all M (``logical_mems`` gives the
+    unrotated view; ring needs M and L multiples of 128 and ext_len = 0).
 
     The roll of mems[n] reads h after its projection has read mems[n]; all
     launches go to one stream, which orders every dependency of the
@@ -149,7 +162,7 @@ class AttnStack:
                  u: Sequence[torch.Tensor], v_bias: Sequence[torch.Tensor],
                  mems: Sequence[torch.Tensor], scale: float, n_head: int, seg_len: int,
                  stream: torch.cuda.Stream | None = None, same_length: bool = False,
-                 ext_len: int = 0):
+                 ext_len: int = 0, ring: bool = False):
         n = len(mems)
         if not (len(w_qkv) == len(r_k) == len(u) == len(v_bias) == n) or n == 0:
             raise ValueError("need one weight, r_k, u, v and memory per layer")
@@ -171,6 +184,9 @@ class AttnStack:
         self.mems = list(mems)
         self.scale, self.H, self.L = float(scale), H, int(seg_len)
         self.same_length, self.ext_len = bool(same_length), int(ext_len)
+        self.ring, self.start = bool(ring), 0
+        if self.ring and (self.ext_len or int(seg_len) % 128 or m0.shape[1] % 128):
+            raise ValueError("ring memories need ext_len = 0 and M, L multiples of 128")
         self.B, self.M, self.d, self.dh = B, M, d, dh
         dev = m0.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -202,8 +218,11 @@ class AttnStack:
                 if trace is not None:
                     rec = {"n": n, "h": h.clone(), "mem": mem.clone()}
                 _lib.qkv_proj(h, mem, self.w_qkv[n], self.H, q=self.q, k=self.k, v=self.v,
-                              stream=self.stream)
-                _roll(mem, h, self.stream, self.ext_len)
+                              stream=self.stream, mem_start=self.start if self.ring else 0)
+                if self.ring:
+                    new_start = _push(mem, h, self.start, self.stream)
+                else:
+                    _roll(mem, h, self.stream, self.ext_len)
                 dst = out if (out is not None and n == len(self.mems) - 1) else self.outs[n]
                 o = _lib.attn_fwd(self.q, self.k, self.v, self.r_k[n], self.u[n], self.v_bias[n],
                                   self.scale, out=dst, stream=self.stream,
@@ -212,8 +231,18 @@ class AttnStack:
                     rec.update(q=self.q.clone(), k=self.k.clone(), v=self.v.clone(), out=o.clone())
                     trace.append(rec)
                 h = o
+        if self.ring:
+            self.start = new_start
         self.segments_done += 1
         return h
+
+    def logical_mems(self) -> list:
+        """Copies of the memories in logical order (oldest row first)."""
+        out = []
+        for m in self.mems:
+            ax = 1 if m.dim() == 3 else 2
+            out.append(torch.roll(m, -self.start, dims=ax) if self.ring and self.start else m.clone())
+        return out
 
     def reset_rows(self, flags: torch.Tensor) -> None:
         """Zeroes every layer's memory of the batch rows whose flag is set
@@ -223,13 +252,15 @@ class AttnStack:
                 _lib.mem_reset(m, flags, stream=self.stream)
 
     def state_dict(self) -> dict:
-        """The per-layer memories (checkpoint/resume)."""
-        return {"mems": [m.detach().clone() for m in self.mems], "segments_done": self.segments_done}
+        """The per-layer memories (checkpoint/resume), with the ring start."""
+        return {"mems": [m.detach().clone() for m in self.mems], "segments_done": self.segments_done,
+                "start": self.start}
 
     def load_state_dict(self, sd: dict) -> None:
         for m, s in zip(self.mems, sd["mems"]):
             m.copy_(s)
         self.segments_done = int(sd.get("segments_done", 0))
+        self.start = int(sd.get("start", 0))
 
 
 class DecoderStack:
