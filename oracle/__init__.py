@@ -240,3 +240,63 @@ def pos_ff(x, w1, b1, w2, b2, ln_g, ln_b, pre_lnorm: bool) -> np.ndarray:
     core = linear(np.maximum(linear(inp, w1, b1), 0.0), w2, b2)
     return x64 + core if pre_lnorm else layer_norm(x64 + core, ln_g, ln_b)
 
+
+
+# ---------------------------------------------------------------------------
+# Backward of the attention ("Transformer-XL" notes, zty624: training with a
+# stop-gradient memory -- the memory enters the segment as a constant input,
+# so gradients stop at the memory rows' keys and values and never reach the
+# earlier segment).  Derived from the forward definition above:
+#   s_ij  = scale ((q_i + u) . k_j + (q_i + v) . R_dist(i,j))   (allowed pairs)
+#   P     = softmax_j(s),  O_i = sum_j P_ij V_j
+#   dV_j  = sum_i P_ij dO_i
+#   dP_ij = dO_i . V_j,    dS_ij = P_ij (dP_ij - dO_i . O_i)
+#   dq_i  = scale sum_j dS_ij (k_j + R_dist)
+#   dk_j  = scale sum_i dS_ij (q_i + u)
+#   dR_r  = scale sum over pairs with R row r of dS_ij (q_i + v)
+#   du    = scale sum_ij dS_ij k_j,   dv = scale sum_ij dS_ij R_dist
+# (u, v and R are shared by the batch; u, v per head.)  fp64, one query row
+# at a time.
+# ---------------------------------------------------------------------------
+def attn_bwd(q, k, v, r_k, u, vb, scale: float, dout, same_length: bool = False,
+             mem_len: int | None = None):
+    """Returns dict of fp64 gradients dq [B,H,L,dh], dk, dv [B,H,M+L,dh],
+    dr [M+L,H,dh], du, dvb [H,dh] of sum(out * dout)."""
+    q, k, v, r, u, vb, g = (_f64(t) for t in (q, k, v, r_k, u, vb, dout))
+    B, H, L, dh = q.shape
+    K = k.shape[2]
+    M = K - L
+    if same_length:
+        ml = M if mem_len is None else mem_len
+        mask_len = K - ml
+        shift = L - mask_len if mask_len > 0 else L
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dr = np.zeros_like(r)
+    du = np.zeros_like(u)
+    dvb = np.zeros_like(vb)
+    j = np.arange(K)
+    for b in range(B):
+        for h in range(H):
+            for i in range(L):
+                allow = (j - i) <= M
+                if same_length:
+                    allow &= (j - i) > -shift
+                js = j[allow]
+                rows = K - 1 - (M + i - js)          # R row of each allowed pair
+                Rj = r[rows, h]                        # [n, dh]
+                kj = k[b, h, js]
+                s = scale * ((kj @ (q[b, h, i] + u[h])) + (Rj @ (q[b, h, i] + vb[h])))
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                o = p @ v[b, h, js]
+                dP = v[b, h, js] @ g[b, h, i]
+                dS = p * (dP - g[b, h, i] @ o)
+                dv[b, h, js] += np.outer(p, g[b, h, i])
+                dq[b, h, i] = scale * (dS @ (kj + Rj))
+                dk[b, h, js] += scale * np.outer(dS, q[b, h, i] + u[h])
+                np.add.at(dr[:, h], rows, scale * np.outer(dS, q[b, h, i] + vb[h]))
+                du[h] += scale * (dS @ kj)
+                dvb[h] += scale * (dS @ Rj)
+    return {"dq": dq, "dk": dk, "dv": dv, "dr": dr, "du": du, "dvb": dvb}

@@ -491,3 +491,32 @@ def test_attention_output_block_special_cases():
     np.testing.assert_allclose(oracle.attn_block_out(w, vec, np.eye(d), g, b, True), w + vec, atol=1e-12)
     np.testing.assert_allclose(oracle.attn_block_out(w, vec, np.zeros((d, d)), g, b, False),
                                oracle.layer_norm(w, g, b), atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# attention backward: central finite differences of the forward oracle
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("same_length", [False, True])
+def test_attn_backward_matches_finite_differences(same_length):
+    B, H, L, M, dh = 1, 2, 3, 2, 4
+    K = M + L
+    x = {"q": rnd(B, H, L, dh), "k": rnd(B, H, K, dh), "v": rnd(B, H, K, dh),
+         "r": rnd(K, H, dh), "u": rnd(H, dh), "vb": rnd(H, dh)}
+    g = rnd(B, H, L, dh)
+    scale = 0.4
+    kw = dict(same_length=True, mem_len=2) if same_length else {}
+
+    def loss(t):
+        return float((oracle.attn(t["q"], t["k"], t["v"], t["r"], t["u"], t["vb"], scale, **kw) * g).sum())
+
+    grads = oracle.attn_bwd(x["q"], x["k"], x["v"], x["r"], x["u"], x["vb"], scale, g, **kw)
+    names = {"q": "dq", "k": "dk", "v": "dv", "r": "dr", "u": "du", "vb": "dvb"}
+    eps = 1e-6
+    for name, gname in names.items():
+        for idx in np.ndindex(x[name].shape):
+            hi = {kk: vv.copy() for kk, vv in x.items()}
+            lo = {kk: vv.copy() for kk, vv in x.items()}
+            hi[name][idx] += eps
+            lo[name][idx] -= eps
+            fd = (loss(hi) - loss(lo)) / (2 * eps)
+            assert abs(fd - grads[gname][idx]) < 1e-7, (name, idx, fd, grads[gname][idx])
