@@ -222,6 +222,25 @@ int txl_mem_ring_push(void* ring, const void* hids, int B, int L, int M, int d, 
 int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream);
 
 /*
+ * txl_attn_bwd: gradients of sum(out * dout) for the attention of
+ * txl_attn_fwd / txl_attn_fwd_ex (same inputs, same mask options), for
+ * training with a stop-gradient memory ("Transformer-XL" notes: the memory is
+ * a constant input of the segment; its rows' dk, dv are returned and the
+ * caller drops them).  Inputs in dtype (TXL_BF16 or TXL_F32), d_h <= 256;
+ * gradients in fp32, device buffers the call overwrites:
+ *   dq [B, H, L, d_h], dk, dv [B, H, M+L, d_h], dr [M+L, H, d_h] (summed
+ *   over the batch), du, dvb [H, d_h] (summed over batch and query rows).
+ * P is recomputed from q, k, r_k, u, v (no forward state is kept).  CUDA-core
+ * arithmetic with fp32 atomics for the summed gradients: a correctness path
+ * whose summation order is not fixed.  Errors as txl_attn_fwd; gradient
+ * buffers must not overlap the inputs or each other (TXL_ERR_ALIAS).
+ */
+int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                 const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
+                 int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,
+                 float* dvb, int dtype, void* stream);
+
+/*
  * The rest of a decoder layer ("Transformer-XL模型 核心源码阅读笔记":
  * RelPartialLearnableMultiHeadAttn.forward after the attention, PositionwiseFF,
  * RelPartialLearnableDecoderLayer), bf16 with fp32 accumulation:

@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_fwd.restype = i
         lib.txl_attn_fwd_ex.argtypes = [vp] * 6 + [i] * 5 + [f, i, i, vp, i, vp]
         lib.txl_attn_fwd_ex.restype = i
+        lib.txl_attn_bwd.argtypes = [vp] * 7 + [i] * 5 + [f, i, i] + [vp] * 6 + [i, vp]
+        lib.txl_attn_bwd.restype = i
         lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
         lib.txl_attn_fwd_ws.restype = i
         lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
@@ -183,6 +185,26 @@ def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None, same_length
     if rc != 0:
         raise TxlError(rc, "txl_attn_fwd")
     return out
+
+
+def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=None, stream=None):
+    """txl_attn_bwd: fp32 gradients of sum(out * dout) with respect to q, k,
+    v, r_k, u and vb (stop-gradient memory: the memory rows' dk, dv are
+    included and left to the caller).  Returns a dict dq, dk, dv, dr, du, dvb."""
+    B, H, L, M, dh, scale, _ = _attn_args(q, k, v, r_k, u, vb, scale, dout)
+    _need(dout, "dout", (B, H, L, dh), q.dtype)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty((B, H, L, dh), **f32), "dk": torch.empty((B, H, M + L, dh), **f32),
+         "dv": torch.empty((B, H, M + L, dh), **f32), "dr": torch.empty((M + L, H, dh), **f32),
+         "du": torch.empty((H, dh), **f32), "dvb": torch.empty((H, dh), **f32)}
+    rc = load().txl_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(),
+                             vb.data_ptr(), dout.data_ptr(), B, H, L, M, dh, scale, int(bool(same_length)),
+                             M if mem_len is None else int(mem_len),
+                             *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")],
+                             _dtype_code(q), _stream(stream, q.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_attn_bwd")
+    return g
 
 
 def attn_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16) -> int:

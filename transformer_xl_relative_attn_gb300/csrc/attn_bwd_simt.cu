@@ -1,0 +1,185 @@
+// Backward of the relative attention on CUDA cores (fp32 arithmetic, inputs
+// fp32 or bf16, gradients fp32), for training with a stop-gradient memory
+// ("Transformer-XL" notes, zty624: the memory is a constant input of the
+// segment, so nothing flows into the previous segment; the memory rows'
+// keys and values still get their gradients, which the caller drops).
+//
+// From the forward s_ij = scale ((q_i+u).k_j + (q_i+v).R[K-1-(M+i-j)]),
+// P = softmax_j(s), O_i = sum_j P_ij V_j, and dO:
+//   dP_ij = dO_i . V_j,   D_i = sum_j P_ij dP_ij  (= dO_i . O_i),
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dq_i = scale sum_j dS_ij (k_j + R_ij),  dk_j += scale dS_ij (q_i + u),
+//   dV_j += P_ij dO_i,  dR_row += scale dS_ij (q_i + v),
+//   du += scale sum_j dS_ij k_j,  dv += scale sum_j dS_ij R_ij.
+//
+// One warp owns one query row of one (batch row, head) and sweeps its
+// visible keys three times, one key per lane: (1) row max and sum of exp,
+// (2) D_i, (3) dS, with the per-key contributions broadcast lane by lane
+// while each lane owns output columns lane, lane+32, ...  dq is written once;
+// dk, dV, dR, du and dv are summed over query rows with fp32 atomics into
+// buffers the host zeroes first.  A correctness path: its cost is the
+// atomics, not the arithmetic.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace txl {
+
+constexpr int kBwdMaxD = 256;
+constexpr int kBwdWarps = 4;
+
+__device__ __forceinline__ float ld_f(const float* p) { return *p; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kBwdWarps)
+attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                     const T* __restrict__ r, const T* __restrict__ ub, const T* __restrict__ vb,
+                     const T* __restrict__ dout, int B, int H, int L, int M, int dh, float scale,
+                     int lo_shift, float* __restrict__ dq, float* __restrict__ dk,
+                     float* __restrict__ dv, float* __restrict__ dr, float* __restrict__ du,
+                     float* __restrict__ dvb) {
+    __shared__ float s_qu[kBwdWarps][kBwdMaxD];
+    __shared__ float s_qv[kBwdWarps][kBwdMaxD];
+    __shared__ float s_do[kBwdWarps][kBwdMaxD];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kBwdWarps + warp;
+    if (row >= (long long)B * H * L) return;
+    const int i = (int)(row % L);
+    const long long bh = row / L;
+    const int h = (int)(bh % H);
+    const int K = M + L;
+    for (int t = lane; t < dh; t += 32) {
+        const float x = ld_f(q + row * dh + t);
+        s_qu[warp][t] = x + ld_f(ub + h * dh + t);
+        s_qv[warp][t] = x + ld_f(vb + h * dh + t);
+        s_do[warp][t] = ld_f(dout + row * dh + t);
+    }
+    __syncwarp();
+    const T* kb = k + bh * (long long)K * dh;
+    const T* vbase = v + bh * (long long)K * dh;
+    const int nvis = M + i + 1;                   // keys up to M+i
+    const int jlo = max(0, i + 1 - lo_shift);     // ... from jlo on (same_length)
+    const int ncol = (dh + 31) / 32;
+
+    auto score = [&](int j) {
+        const int dist = M + i - j;
+        const T* kj = kb + (long long)j * dh;
+        const T* rj = r + ((long long)(K - 1 - dist) * H + h) * dh;
+        float ac = 0.f, bd = 0.f;
+        for (int t = 0; t < dh; ++t) {
+            ac = fmaf(s_qu[warp][t], ld_f(kj + t), ac);
+            bd = fmaf(s_qv[warp][t], ld_f(rj + t), bd);
+        }
+        return scale * (ac + bd);
+    };
+    auto dprob = [&](int j) {
+        const T* vj = vbase + (long long)j * dh;
+        float a = 0.f;
+        for (int t = 0; t < dh; ++t) a = fmaf(s_do[warp][t], ld_f(vj + t), a);
+        return a;
+    };
+
+    // (1) row max and sum of exp
+    float m = -INFINITY, l = 0.f;
+    for (int j0 = jlo; j0 < nvis; j0 += 32) {
+        const int j = j0 + lane;
+        const float s = j < nvis ? score(j) : -INFINITY;
+        float cm = s;
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        const float mn = fmaxf(m, cm);
+        float e = j < nvis ? expf(s - mn) : 0.f;
+        for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+        l = l * expf(m - mn) + e;
+        m = mn;
+    }
+    const float inv_l = 1.f / l;
+    // (2) D = sum_j P_ij dP_ij
+    float D = 0.f;
+    for (int j0 = jlo; j0 < nvis; j0 += 32) {
+        const int j = j0 + lane;
+        float c = 0.f;
+        if (j < nvis) c = expf(score(j) - m) * inv_l * dprob(j);
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        D += c;
+    }
+    // (3) dS and the contributions
+    float gq_c[kBwdMaxD / 32], gq_p[kBwdMaxD / 32];
+#pragma unroll
+    for (int c = 0; c < kBwdMaxD / 32; ++c) gq_c[c] = gq_p[c] = 0.f;
+    for (int j0 = jlo; j0 < nvis; j0 += 32) {
+        const int j = j0 + lane;
+        float p = 0.f, ds = 0.f;
+        if (j < nvis) {
+            p = expf(score(j) - m) * inv_l;
+            ds = p * (dprob(j) - D);
+        }
+        const int nk = min(32, nvis - j0);
+        for (int jj = 0; jj < nk; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, p, jj);
+            const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+            const int jk = j0 + jj;
+            const long long rrow = (long long)(K - 1 - (M + i - jk));
+            const T* kj = kb + (long long)jk * dh;
+            const T* rj = r + (rrow * H + h) * dh;
+            float* dkj = dk + (bh * K + jk) * dh;
+            float* dvj = dv + (bh * K + jk) * dh;
+            float* drj = dr + (rrow * H + h) * dh;
+#pragma unroll
+            for (int c = 0; c < kBwdMaxD / 32; ++c) {
+                const int t = lane + 32 * c;
+                if (c < ncol && t < dh) {
+                    gq_c[c] = fmaf(dsj, ld_f(kj + t), gq_c[c]);
+                    gq_p[c] = fmaf(dsj, ld_f(rj + t), gq_p[c]);
+                    atomicAdd(dkj + t, scale * dsj * s_qu[warp][t]);
+                    atomicAdd(dvj + t, pj * s_do[warp][t]);
+                    atomicAdd(drj + t, scale * dsj * s_qv[warp][t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < kBwdMaxD / 32; ++c) {
+        const int t = lane + 32 * c;
+        if (c < ncol && t < dh) {
+            dq[row * dh + t] = scale * (gq_c[c] + gq_p[c]);
+            atomicAdd(du + h * dh + t, scale * gq_c[c]);
+            atomicAdd(dvb + h * dh + t, scale * gq_p[c]);
+        }
+    }
+}
+
+// Zeroes the summed gradients, then one launch over all query rows.
+cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, const void* r,
+                                 const void* ub, const void* vb, const void* dout, int bf16, int B,
+                                 int H, int L, int M, int dh, float scale, int lo_shift, float* dq,
+                                 float* dk, float* dv, float* dr, float* du, float* dvb,
+                                 cudaStream_t stream) {
+    const long long K = (long long)M + L;
+    const size_t nkv = (size_t)B * H * K * dh * sizeof(float);
+    const size_t nr = (size_t)K * H * dh * sizeof(float), nb = (size_t)H * dh * sizeof(float);
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(dk, 0, nkv, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dv, 0, nkv, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dr, 0, nr, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(du, 0, nb, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dvb, 0, nb, stream)) != cudaSuccess) return e;
+    const long long rows = (long long)B * H * L;
+    const long long blocks = (rows + kBwdWarps - 1) / kBwdWarps;
+    if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    if (bf16)
+        attn_bwd_simt_kernel<__nv_bfloat16><<<(unsigned)blocks, 32 * kBwdWarps, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+            static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(r),
+            static_cast<const __nv_bfloat16*>(ub), static_cast<const __nv_bfloat16*>(vb),
+            static_cast<const __nv_bfloat16*>(dout), B, H, L, M, dh, scale, lo_shift, dq, dk, dv, dr,
+            du, dvb);
+    else
+        attn_bwd_simt_kernel<float><<<(unsigned)blocks, 32 * kBwdWarps, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            static_cast<const float*>(r), static_cast<const float*>(ub), static_cast<const float*>(vb),
+            static_cast<const float*>(dout), B, H, L, M, dh, scale, lo_shift, dq, dk, dv, dr, du, dvb);
+    return cudaGetLastError();
+}
+
+}  // namespace txl

@@ -19,6 +19,11 @@ cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long 
                              cudaStream_t stream);
 cudaError_t launch_ring_push(void* ring, const void* hid, int B, int L, int M, int start,
                              size_t row_bytes, cudaStream_t stream);
+cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, const void* r,
+                                 const void* ub, const void* vb, const void* dout, int bf16, int B,
+                                 int H, int L, int M, int dh, float scale, int lo_shift, float* dq,
+                                 float* dk, float* dv, float* dr, float* du, float* dvb,
+                                 cudaStream_t stream);
 cudaError_t launch_layer_norm(const void* x, const void* y, const void* gamma, const void* beta,
                               long long rows, int d, float eps, void* out, cudaStream_t stream);
 cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v, const float* r,
@@ -155,6 +160,41 @@ int txl_attn_fwd_ex(const void* q, const void* k, const void* v, const void* r_k
     if (same_length && (mem_len < M || mem_len >= (1 << 30))) return TXL_ERR_INVALID_ARG;
     return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, nullptr,
                        stream, lower_shift(same_length, L, M, mem_len));
+}
+
+int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                 const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
+                 int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,
+                 float* dvb, int dtype, void* stream) {
+    const int es = elem_size(dtype);
+    if (!es) return TXL_ERR_INVALID_ARG;
+    if (!q || !k || !v || !r_k || !u_bias || !v_bias || !dout || !dq || !dk || !dv || !dr || !du || !dvb)
+        return TXL_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || L <= 0 || M < 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
+    if (same_length && (mem_len < M || mem_len >= (1 << 30))) return TXL_ERR_INVALID_ARG;
+    if (d_h > 256) return TXL_ERR_UNSUPPORTED;
+    const long long K = (long long)M + L;
+    if (K >= (1ll << 30) || (long long)B * H * K * d_h >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    const void* ins[7] = {q, k, v, r_k, u_bias, v_bias, dout};
+    const void* outs[6] = {dq, dk, dv, dr, du, dvb};
+    for (const void* p : ins)
+        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
+    for (const void* p : outs)
+        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
+    const size_t nq = (size_t)B * H * L * d_h, nkv = (size_t)B * H * K * d_h, nr = (size_t)K * H * d_h,
+                 nb = (size_t)H * d_h;
+    const size_t in_n[7] = {nq * es, nkv * es, nkv * es, nr * es, nb * es, nb * es, nq * es};
+    const size_t out_n[6] = {nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
+    for (int o = 0; o < 6; ++o) {
+        for (int i2 = 0; i2 < 7; ++i2)
+            if (overlap(outs[o], out_n[o], ins[i2], in_n[i2])) return TXL_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 6; ++o2)
+            if (overlap(outs[o], out_n[o], outs[o2], out_n[o2])) return TXL_ERR_ALIAS;
+    }
+    const cudaError_t e = txl::launch_attn_bwd_simt(q, k, v, r_k, u_bias, v_bias, dout, dtype == TXL_BF16, B, H,
+                                                    L, M, d_h, scale, lower_shift(same_length, L, M, mem_len),
+                                                    dq, dk, dv, dr, du, dvb, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 
 size_t txl_attn_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype) {
