@@ -301,6 +301,7 @@ def run_ours(args, wl: W.Workload):
     attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
     roll_ms = time_rolls(calls, mems, stream)
     proj = time_projections(wl, dev, stream, peaks)
+    bwd = time_backward(wl, calls, rks, u, vb, dev) if wl.dh <= 256 else None
     txl.check_status()
     flops_call = wl.attn_flops()
     flops_step = flops_call * n_calls
@@ -356,6 +357,7 @@ def run_ours(args, wl: W.Workload):
         # the Tail_M roll timed alone after the timed region (in the step it
         # runs on a second stream in the gaps between attention kernels)
         "projections": proj,
+        "backward": bwd,
         "roofline_mem_update": {
             "kernel": "tail_copy_kernel" if wl.L >= wl.M else "tail_chain_kernel",
             "bound": "hbm",
@@ -727,6 +729,36 @@ def measure_decoder(args, wl, dev, flops_step, ws, d_inner_mult=4):
             "all_matmul_tflops": round(ws * (flops_step + other) * steps / el / 1e12, 3),
             "d_inner": di, "norm": "post", "steps": steps,
             "api": "DecoderStack.run_segment per segment; host hidden states in, last layer output out"}
+
+
+def time_backward(wl, calls, rks, u, vb, dev):
+    """txl_attn_bwd on the workload's first call (bf16 inputs, fp32
+    gradients), timed alone with CUDA events: 1 warm-up, 3 timed calls.
+    Algorithmic work 12 d_h FLOPs per visible pair (the six contractions
+    dV, dP, dq content, dq position, dk, dR); a CUDA-core path, so the peak
+    is the fp32 FMA rate of the SMs at their maximum clock
+    (152 SMs x 128 FMA/clk x 2 FLOP x 2.07 GHz = 80.5 TFLOP/s)."""
+    import transformer_xl_relative_attn_gb300 as txl
+    c = calls[0]
+    g = torch.randn(c["q"].shape, generator=torch.Generator().manual_seed(0)).to(dev, c["q"].dtype)
+    args = (c["q"], c["k"], c["v"], rks[0], u, vb, g, wl.scale)
+    txl.attn_bwd(*args)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        txl.attn_bwd(*args)
+    e1.record()
+    torch.cuda.synchronize()
+    txl.check_status()
+    ms = e0.elapsed_time(e1) / 3
+    flops = 12 * wl.dh * wl.B * wl.H * wl.visible_pairs()
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"kernel": "attn_bwd_simt_kernel", "ms": round(ms, 3), "tflops": round(tf, 3),
+            "bound": "alu", "peak": round(peak, 1), "frac": round(tf / peak, 4),
+            "peak_source": "derived: fp32 FMA units x max SM clock",
+            "flops": flops, "measured": "the workload's first call alone, CUDA events, 3 calls"}
 
 
 def cpu_baseline_and_parity(wl, calls, rks, u, vb):

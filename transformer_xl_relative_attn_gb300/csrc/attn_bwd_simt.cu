@@ -149,7 +149,212 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     }
 }
 
-// Zeroes the summed gradients, then one launch over all query rows.
+
+// Block-cooperative version for d_h <= 64: a CTA of 8 warps owns 32
+// consecutive query rows of one (batch row, head), 4 per warp, and sweeps the
+// keys any of them sees in chunks of 32.  Each chunk's K and V rows and the
+// 63 R rows its 32 x 32 pairs use are staged in shared memory once for all
+// 32 query rows (rows padded to 65 floats: lane-per-key reads hit distinct
+// banks).  Sweep 1 gives each row its max and sum of exp, sweep 2 its D_i,
+// sweep 3 dS: dq stays in registers (columns split over lanes) and the dk,
+// dV and dR contributions go to shared tiles of the chunk (shared atomics),
+// flushed to the global sums with one fp32 atomic per element per chunk.
+constexpr int kQR = 32;         // query rows per CTA
+constexpr int kRPW = 4;         // query rows per warp (8 warps)
+constexpr int kDT = 64;         // d_h capacity
+constexpr int kPad = 65;        // padded row of a staged tile
+constexpr int kSpan = 63;       // distances one 32 x 32 block of pairs covers
+constexpr size_t kTiledSmem =
+    (size_t)(3 * kQR * kDT + 2 * kQR * kPad + kSpan * kPad + 2 * kQR * kDT + kSpan * kDT) * sizeof(float);
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                      const T* __restrict__ r, const T* __restrict__ ub, const T* __restrict__ vb,
+                      const T* __restrict__ dout, int B, int H, int L, int M, int dh, float scale,
+                      int lo_shift, float* __restrict__ dq, float* __restrict__ dk,
+                      float* __restrict__ dv, float* __restrict__ dr, float* __restrict__ du,
+                      float* __restrict__ dvb) {
+    extern __shared__ float sm[];
+    float* s_qu = sm;                    // [32 rows][64]
+    float* s_qv = s_qu + kQR * kDT;
+    float* s_do = s_qv + kQR * kDT;
+    float* t_k = s_do + kQR * kDT;       // [32 keys][65] of the chunk
+    float* t_v = t_k + kQR * kPad;
+    float* t_r = t_v + kQR * kPad;       // [63 slots][65]: slot = row - key + 31
+    float* s_dk = t_r + kSpan * kPad;    // [32 keys][64]
+    float* s_dv = s_dk + kQR * kDT;
+    float* s_dr = s_dv + kQR * kDT;      // [63 slots][64]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nqt = (L + kQR - 1) / kQR;
+    const long long bh = blockIdx.x / nqt;
+    const int i0 = (int)(blockIdx.x % nqt) * kQR;
+    const int h = (int)(bh % H);
+    const int K = M + L;
+    for (int idx = tid; idx < kQR * kDT; idx += 256) {
+        const int rr = idx / kDT, t = idx % kDT, i = i0 + rr;
+        float a = 0.f, b = 0.f, c = 0.f;
+        if (i < L && t < dh) {
+            const float x = ld_f(q + (bh * L + i) * dh + t);
+            a = x + ld_f(ub + h * dh + t);
+            b = x + ld_f(vb + h * dh + t);
+            c = ld_f(dout + (bh * L + i) * dh + t);
+        }
+        s_qu[idx] = a;
+        s_qv[idx] = b;
+        s_do[idx] = c;
+        s_dk[idx] = 0.f;
+        s_dv[idx] = 0.f;
+    }
+    for (int idx = tid; idx < kSpan * kDT; idx += 256) s_dr[idx] = 0.f;
+    const int imax = min(i0 + kQR - 1, L - 1);
+    const int jstart = max(0, i0 + 1 - lo_shift), jend = M + imax + 1;
+
+    // stage the chunk at j0: K, V rows j0 .. j0+31 and the R row of each slot
+    auto stage = [&](int j0) {
+        __syncthreads();
+        for (int idx = tid; idx < kQR * kDT; idx += 256) {
+            const int jj = idx / kDT, t = idx % kDT, j = j0 + jj;
+            float a = 0.f, b = 0.f;
+            if (j < K && t < dh) {
+                a = ld_f(k + (bh * K + j) * dh + t);
+                b = ld_f(v + (bh * K + j) * dh + t);
+            }
+            t_k[jj * kPad + t] = a;
+            t_v[jj * kPad + t] = b;
+        }
+        for (int idx = tid; idx < kSpan * kDT; idx += 256) {
+            const int sl = idx / kDT, t = idx % kDT;
+            const long long rrow = (long long)K - 1 - (M + (sl - 31) + i0 - j0);
+            t_r[sl * kPad + t] = (rrow >= 0 && rrow < K && t < dh) ? ld_f(r + (rrow * H + h) * dh + t) : 0.f;
+        }
+        __syncthreads();
+    };
+    // score of (row rr, key j0 + lane) from the staged tiles
+    auto score = [&](int rr, int jj) {
+        const float* kr = t_k + jj * kPad;
+        const float* rrw = t_r + (rr - jj + 31) * kPad;
+        float ac = 0.f, bd = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < dh; ++t) {
+            ac = fmaf(s_qu[rr * kDT + t], kr[t], ac);
+            bd = fmaf(s_qv[rr * kDT + t], rrw[t], bd);
+        }
+        return scale * (ac + bd);
+    };
+    auto dprob = [&](int rr, int jj) {
+        const float* vr = t_v + jj * kPad;
+        float a = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < dh; ++t) a = fmaf(s_do[rr * kDT + t], vr[t], a);
+        return a;
+    };
+    auto visible = [&](int i, int j) { return i < L && j < jend && j <= M + i && j >= i + 1 - lo_shift; };
+
+    float m[kRPW], l[kRPW], D[kRPW];
+#pragma unroll
+    for (int w = 0; w < kRPW; ++w) {
+        m[w] = -INFINITY;
+        l[w] = 0.f;
+        D[w] = 0.f;
+    }
+    // sweep 1: max and sum of exp
+    for (int j0 = jstart; j0 < jend; j0 += 32) {
+        stage(j0);
+#pragma unroll
+        for (int w = 0; w < kRPW; ++w) {
+            const int rr = warp * kRPW + w, i = i0 + rr, j = j0 + lane;
+            const float s = visible(i, j) ? score(rr, lane) : -INFINITY;
+            float cm = s;
+            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            const float mn = fmaxf(m[w], cm);
+            if (mn == -INFINITY) continue;  // no visible key of this row yet
+            float e = visible(i, j) ? expf(s - mn) : 0.f;
+            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            l[w] = l[w] * expf(m[w] - mn) + e;
+            m[w] = mn;
+        }
+    }
+    // sweep 2: D = sum_j P dP
+    for (int j0 = jstart; j0 < jend; j0 += 32) {
+        stage(j0);
+#pragma unroll
+        for (int w = 0; w < kRPW; ++w) {
+            const int rr = warp * kRPW + w, i = i0 + rr, j = j0 + lane;
+            float c = visible(i, j) ? expf(score(rr, lane) - m[w]) / l[w] * dprob(rr, lane) : 0.f;
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            D[w] += c;
+        }
+    }
+    // sweep 3: dS and the contributions
+    float gc[kRPW][2], gp[kRPW][2];
+#pragma unroll
+    for (int w = 0; w < kRPW; ++w) gc[w][0] = gc[w][1] = gp[w][0] = gp[w][1] = 0.f;
+    for (int j0 = jstart; j0 < jend; j0 += 32) {
+        stage(j0);
+#pragma unroll
+        for (int w = 0; w < kRPW; ++w) {
+            const int rr = warp * kRPW + w, i = i0 + rr, j = j0 + lane;
+            float p = 0.f, ds = 0.f;
+            if (visible(i, j)) {
+                p = expf(score(rr, lane) - m[w]) / l[w];
+                ds = p * (dprob(rr, lane) - D[w]);
+            }
+            for (int jj = 0; jj < 32; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, p, jj);
+                const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+                if (pj == 0.f && dsj == 0.f) continue;  // invisible (warp-uniform)
+                const int slot = rr - jj + 31;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int t = lane + 32 * c;
+                    if (t < dh) {
+                        gc[w][c] = fmaf(dsj, t_k[jj * kPad + t], gc[w][c]);
+                        gp[w][c] = fmaf(dsj, t_r[slot * kPad + t], gp[w][c]);
+                        atomicAdd(s_dk + jj * kDT + t, scale * dsj * s_qu[rr * kDT + t]);
+                        atomicAdd(s_dv + jj * kDT + t, pj * s_do[rr * kDT + t]);
+                        atomicAdd(s_dr + slot * kDT + t, scale * dsj * s_qv[rr * kDT + t]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kQR * kDT; idx += 256) {
+            const int jj = idx / kDT, t = idx % kDT, jk = j0 + jj;
+            if (jk < jend && t < dh) {
+                const float a = s_dk[idx], b = s_dv[idx];
+                if (a != 0.f) atomicAdd(dk + (bh * K + jk) * dh + t, a);
+                if (b != 0.f) atomicAdd(dv + (bh * K + jk) * dh + t, b);
+            }
+            s_dk[idx] = 0.f;
+            s_dv[idx] = 0.f;
+        }
+        for (int idx = tid; idx < kSpan * kDT; idx += 256) {
+            const int sl = idx / kDT, t = idx % kDT;
+            const long long rrow = (long long)K - 1 - (M + (sl - 31) + i0 - j0);
+            const float a = s_dr[idx];
+            if (a != 0.f && t < dh && rrow >= 0 && rrow < K) atomicAdd(dr + (rrow * H + h) * dh + t, a);
+            s_dr[idx] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int w = 0; w < kRPW; ++w) {
+        const int i = i0 + warp * kRPW + w;
+        if (i >= L) break;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int t = lane + 32 * c;
+            if (t < dh) {
+                dq[(bh * L + i) * dh + t] = scale * (gc[w][c] + gp[w][c]);
+                atomicAdd(du + h * dh + t, scale * gc[w][c]);
+                atomicAdd(dvb + h * dh + t, scale * gp[w][c]);
+            }
+        }
+    }
+}
+
+// Zeroes the summed gradients, then one launch: the block-cooperative kernel
+// for d_h <= 64, else one query row per warp.
 cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, const void* r,
                                  const void* ub, const void* vb, const void* dout, int bf16, int B,
                                  int H, int L, int M, int dh, float scale, int lo_shift, float* dq,
@@ -164,6 +369,33 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, co
     if ((e = cudaMemsetAsync(dr, 0, nr, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(du, 0, nb, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dvb, 0, nb, stream)) != cudaSuccess) return e;
+    if (dh <= kDT) {
+        static bool attr_set = false;
+        if (!attr_set) {
+            if ((e = cudaFuncSetAttribute(attn_bwd_tiled_kernel<float>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem)) != cudaSuccess)
+                return e;
+            if ((e = cudaFuncSetAttribute(attn_bwd_tiled_kernel<__nv_bfloat16>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem)) != cudaSuccess)
+                return e;
+            attr_set = true;
+        }
+        const long long blocks = (long long)B * H * ((L + kQR - 1) / kQR);
+        if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+        if (bf16)
+            attn_bwd_tiled_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, kTiledSmem, stream>>>(
+                static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(r),
+                static_cast<const __nv_bfloat16*>(ub), static_cast<const __nv_bfloat16*>(vb),
+                static_cast<const __nv_bfloat16*>(dout), B, H, L, M, dh, scale, lo_shift, dq, dk, dv, dr,
+                du, dvb);
+        else
+            attn_bwd_tiled_kernel<float><<<(unsigned)blocks, 256, kTiledSmem, stream>>>(
+                static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+                static_cast<const float*>(r), static_cast<const float*>(ub), static_cast<const float*>(vb),
+                static_cast<const float*>(dout), B, H, L, M, dh, scale, lo_shift, dq, dk, dv, dr, du, dvb);
+        return cudaGetLastError();
+    }
     const long long rows = (long long)B * H * L;
     const long long blocks = (rows + kBwdWarps - 1) / kBwdWarps;
     if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
