@@ -83,3 +83,77 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         txl.attn_fwd(q, k, k, torch.zeros(7, 1, 64, dtype=torch.bfloat16),
                      torch.zeros(1, 64, dtype=torch.bfloat16), torch.zeros(1, 64, dtype=torch.bfloat16))
+
+
+# --------------------------------------------------------------------------
+# the entry points added beyond the attention operator: bad arguments are
+# rejected on the host, before any CUDA call
+# --------------------------------------------------------------------------
+O = A + (1 << 30)   # a second fake address, far from A
+
+
+def test_attn_fwd_ex_rejects_bad_mem_len(lib):
+    def call(**kw):
+        a = dict(same_length=1, mem_len=3)
+        a.update(kw)
+        return lib.txl_attn_fwd_ex(A, A, A, A, A, A, 1, 1, 4, 3, 64, 0.125, a["same_length"], a["mem_len"],
+                                   O, txl.TXL_BF16, None)
+    assert call(mem_len=2) == -1      # mem_len < M
+    assert call(mem_len=-1) == -1
+
+
+def test_qkv_proj_rejects_bad_sizes_layouts_and_rings(lib):
+    def call(h_layout=0, mem_layout=0, start=0, L=128, M=128, H=4, dh=64, q=O, k=O + (1 << 26), v=O + (1 << 27)):
+        return lib.txl_qkv_proj_ring(A, h_layout, A + (1 << 24), mem_layout, start, A + (1 << 25), 1, L, M, H,
+                                     dh, q, k, v, None)
+    assert call(h_layout=2) == -1
+    assert call(mem_layout=-1) == -1
+    assert call(start=128) == -1      # start must be < M
+    assert call(start=64, M=256) == -2  # not a multiple of 128
+    assert call(L=100) == -2
+    assert call(dh=32) == -2
+    assert call(H=6) == -2
+    assert call(q=O + 8) == -3
+    assert call(q=A) == -4            # q over h
+
+
+def test_linear_and_layer_norm_reject_bad_arguments(lib):
+    def lin(x_layout=0, T=128, K=256, N=256, out=O, resid=0, bias=0):
+        return lib.txl_linear(A, x_layout, 1, T, K, A + (1 << 25), N, bias, resid, 0, out, None)
+    assert lin(x_layout=3) == -1
+    assert lin(T=100) == -2
+    assert lin(K=100) == -2
+    assert lin(N=128) == -2
+    assert lin(out=O + 2) == -3
+    assert lin(out=A) == -4
+    assert lin(resid=O + 64) == -4    # partly overlapping the output
+    def ln(d=512, out=O, y=0, eps=1e-5):
+        return lib.txl_layer_norm(A, y, A + (1 << 25), A + (1 << 26), 64, d, ctypes.c_float(eps), out, None)
+    assert ln(d=500) == -2
+    assert ln(d=1280) == -2
+    assert ln(eps=-1.0) == -1
+    assert ln(out=O + 4) == -3
+    assert ln(out=A + 64) == -4       # overlaps x without being x
+
+
+def test_memory_calls_reject_bad_arguments(lib):
+    new = ctypes.c_int(-1)
+    assert lib.txl_mem_update_ext(A, O, 1, 4, 3, 8, -1, txl.TXL_BF16, None) == -1
+    assert lib.txl_mem_ring_push(A, O, 1, 4, 8, 8, 8, ctypes.byref(new), txl.TXL_BF16, None) == -1  # start >= M
+    assert lib.txl_mem_ring_push(A, O, 1, 4, 8, 8, 0, None, txl.TXL_BF16, None) == -1
+    assert lib.txl_mem_ring_push(A, A + 16, 1, 4, 8, 8, 0, ctypes.byref(new), txl.TXL_BF16, None) == -4
+    assert lib.txl_mem_reset(A, 0, 2, 8, 8, txl.TXL_BF16, None) == -1   # no flags
+    assert lib.txl_mem_reset(A, A + 16, 2, 8, 8, txl.TXL_BF16, None) == -4
+
+
+def test_attn_bwd_rejects_bad_arguments(lib):
+    g = [O + (i << 24) for i in range(6)]
+    def call(dh=64, dtype=txl.TXL_BF16, grads=g, same_length=0, mem_len=3):
+        return lib.txl_attn_bwd(A, A, A, A, A, A, A, 1, 1, 4, 3, dh, 0.125, same_length, mem_len, *grads,
+                                dtype, None)
+    assert call(dtype=5) == -1
+    assert call(dh=512) == -2
+    assert call(grads=[O + 4] + g[1:]) == -3
+    assert call(grads=[A] + g[1:]) == -4           # dq over the inputs
+    assert call(grads=[g[0], g[0]] + g[2:]) == -4  # two gradients overlap
+    assert call(same_length=1, mem_len=1) == -1
