@@ -755,7 +755,7 @@ def time_backward(wl, calls, rks, u, vb, dev):
     flops = 12 * wl.dh * wl.B * wl.H * wl.visible_pairs()
     peak = 152 * 128 * 2 * 2.07e9 / 1e12
     tf = flops / (ms * 1e-3) / 1e12
-    return {"kernel": "attn_bwd_simt_kernel", "ms": round(ms, 3), "tflops": round(tf, 3),
+    return {"kernel": "attn_bwd_tiled_kernel" if wl.dh <= 64 else "attn_bwd_simt_kernel", "ms": round(ms, 3), "tflops": round(tf, 3),
             "bound": "alu", "peak": round(peak, 1), "frac": round(tf / peak, 4),
             "peak_source": "derived: fp32 FMA units x max SM clock",
             "flops": flops, "measured": "the workload's first call alone, CUDA events, 3 calls"}

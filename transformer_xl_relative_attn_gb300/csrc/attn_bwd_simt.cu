@@ -155,17 +155,19 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 // keys any of them sees in chunks of 32.  Each chunk's K and V rows and the
 // 63 R rows its 32 x 32 pairs use are staged in shared memory once for all
 // 32 query rows (rows padded to 65 floats: lane-per-key reads hit distinct
-// banks).  Sweep 1 gives each row its max and sum of exp, sweep 2 its D_i,
-// sweep 3 dS: dq stays in registers (columns split over lanes) and the dk,
-// dV and dR contributions go to shared tiles of the chunk (shared atomics),
-// flushed to the global sums with one fp32 atomic per element per chunk.
+// banks).  Sweep 1 gives each row its max, its sum of exp and D_i (online),
+// sweep 2 the chunk's P and dS tiles in shared memory, from which every
+// contribution is a small product (dq per row in registers; dk, dV per key
+// and dR per distance summed over the 32 rows), flushed to the global sums
+// with one fp32 atomic per element per chunk.
 constexpr int kQR = 32;         // query rows per CTA
 constexpr int kRPW = 4;         // query rows per warp (8 warps)
 constexpr int kDT = 64;         // d_h capacity
 constexpr int kPad = 65;        // padded row of a staged tile
 constexpr int kSpan = 63;       // distances one 32 x 32 block of pairs covers
+constexpr int kPS = 33;         // padded row of the P and dS tiles
 constexpr size_t kTiledSmem =
-    (size_t)(3 * kQR * kDT + 2 * kQR * kPad + kSpan * kPad + 2 * kQR * kDT + kSpan * kDT) * sizeof(float);
+    (size_t)(3 * kQR * kDT + 2 * kQR * kPad + kSpan * kPad + 2 * kQR * kPS) * sizeof(float);
 
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
@@ -182,9 +184,8 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     float* t_k = s_do + kQR * kDT;       // [32 keys][65] of the chunk
     float* t_v = t_k + kQR * kPad;
     float* t_r = t_v + kQR * kPad;       // [63 slots][65]: slot = row - key + 31
-    float* s_dk = t_r + kSpan * kPad;    // [32 keys][64]
-    float* s_dv = s_dk + kQR * kDT;
-    float* s_dr = s_dv + kQR * kDT;      // [63 slots][64]
+    float* s_p = t_r + kSpan * kPad;     // [32 rows][33]: P of the chunk
+    float* s_s = s_p + kQR * kPS;        // [32 rows][33]: dS of the chunk
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nqt = (L + kQR - 1) / kQR;
     const long long bh = blockIdx.x / nqt;
@@ -203,10 +204,7 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         s_qu[idx] = a;
         s_qv[idx] = b;
         s_do[idx] = c;
-        s_dk[idx] = 0.f;
-        s_dv[idx] = 0.f;
     }
-    for (int idx = tid; idx < kSpan * kDT; idx += 256) s_dr[idx] = 0.f;
     const int imax = min(i0 + kQR - 1, L - 1);
     const int jstart = max(0, i0 + 1 - lo_shift), jend = M + imax + 1;
 
@@ -258,38 +256,42 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         l[w] = 0.f;
         D[w] = 0.f;
     }
-    // sweep 1: max and sum of exp
+    // sweep 1: max, sum of exp and D = sum_j P dP, online (the sums are
+    // rescaled whenever the running max grows; D is divided by l at the end)
     for (int j0 = jstart; j0 < jend; j0 += 32) {
         stage(j0);
 #pragma unroll
         for (int w = 0; w < kRPW; ++w) {
             const int rr = warp * kRPW + w, i = i0 + rr, j = j0 + lane;
-            const float s = visible(i, j) ? score(rr, lane) : -INFINITY;
+            const bool vis = visible(i, j);
+            const float s = vis ? score(rr, lane) : -INFINITY;
             float cm = s;
             for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
             const float mn = fmaxf(m[w], cm);
             if (mn == -INFINITY) continue;  // no visible key of this row yet
-            float e = visible(i, j) ? expf(s - mn) : 0.f;
-            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-            l[w] = l[w] * expf(m[w] - mn) + e;
+            const float e = vis ? expf(s - mn) : 0.f;
+            float es = e, ed = vis ? e * dprob(rr, lane) : 0.f;
+            for (int o = 16; o > 0; o >>= 1) {
+                es += __shfl_xor_sync(0xffffffffu, es, o);
+                ed += __shfl_xor_sync(0xffffffffu, ed, o);
+            }
+            const float a = expf(m[w] - mn);
+            l[w] = l[w] * a + es;
+            D[w] = D[w] * a + ed;
             m[w] = mn;
         }
     }
-    // sweep 2: D = sum_j P dP
-    for (int j0 = jstart; j0 < jend; j0 += 32) {
-        stage(j0);
 #pragma unroll
-        for (int w = 0; w < kRPW; ++w) {
-            const int rr = warp * kRPW + w, i = i0 + rr, j = j0 + lane;
-            float c = visible(i, j) ? expf(score(rr, lane) - m[w]) / l[w] * dprob(rr, lane) : 0.f;
-            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-            D[w] += c;
-        }
-    }
-    // sweep 3: dS and the contributions
-    float gc[kRPW][2], gp[kRPW][2];
+    for (int w = 0; w < kRPW; ++w)
+        if (l[w] > 0.f) D[w] /= l[w];
+    // sweep 2: P and dS of each chunk into shared tiles, then every
+    // contribution as a small product over those tiles: thread (row or key
+    // or distance slot = tid / 8, columns tid % 8 + 8c) with no shuffles and
+    // no shared atomics; dk, dV, dR flushed with one global atomic each.
+    const int rid = tid >> 3, cg = tid & 7;
+    float gc[8], gp[8];
 #pragma unroll
-    for (int w = 0; w < kRPW; ++w) gc[w][0] = gc[w][1] = gp[w][0] = gp[w][1] = 0.f;
+    for (int c = 0; c < 8; ++c) gc[c] = gp[c] = 0.f;
     for (int j0 = jstart; j0 < jend; j0 += 32) {
         stage(j0);
 #pragma unroll
@@ -300,54 +302,79 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
                 p = expf(score(rr, lane) - m[w]) / l[w];
                 ds = p * (dprob(rr, lane) - D[w]);
             }
-            for (int jj = 0; jj < 32; ++jj) {
-                const float pj = __shfl_sync(0xffffffffu, p, jj);
-                const float dsj = __shfl_sync(0xffffffffu, ds, jj);
-                if (pj == 0.f && dsj == 0.f) continue;  // invisible (warp-uniform)
-                const int slot = rr - jj + 31;
+            s_p[rr * kPS + lane] = p;
+            s_s[rr * kPS + lane] = ds;
+        }
+        __syncthreads();
+        // dq of row rid: sum over the chunk's keys
+        for (int jj = 0; jj < 32; ++jj) {
+            const float dsv = s_s[rid * kPS + jj];
+            const float* kr = t_k + jj * kPad;
+            const float* rw = t_r + (rid - jj + 31) * kPad;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int t = lane + 32 * c;
+            for (int c = 0; c < 8; ++c) {
+                const int t = cg + 8 * c;
+                gc[c] = fmaf(dsv, kr[t], gc[c]);
+                gp[c] = fmaf(dsv, rw[t], gp[c]);
+            }
+        }
+        // dk, dV of key rid: sums over the 32 query rows
+        {
+            const int jk = j0 + rid;
+            float ak[8], av[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ak[c] = av[c] = 0.f;
+            for (int rr = 0; rr < kQR; ++rr) {
+                const float dsv = s_s[rr * kPS + rid], pv = s_p[rr * kPS + rid];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int t = cg + 8 * c;
+                    ak[c] = fmaf(dsv, s_qu[rr * kDT + t], ak[c]);
+                    av[c] = fmaf(pv, s_do[rr * kDT + t], av[c]);
+                }
+            }
+            if (jk < jend) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int t = cg + 8 * c;
                     if (t < dh) {
-                        gc[w][c] = fmaf(dsj, t_k[jj * kPad + t], gc[w][c]);
-                        gp[w][c] = fmaf(dsj, t_r[slot * kPad + t], gp[w][c]);
-                        atomicAdd(s_dk + jj * kDT + t, scale * dsj * s_qu[rr * kDT + t]);
-                        atomicAdd(s_dv + jj * kDT + t, pj * s_do[rr * kDT + t]);
-                        atomicAdd(s_dr + slot * kDT + t, scale * dsj * s_qv[rr * kDT + t]);
+                        if (ak[c] != 0.f) atomicAdd(dk + (bh * K + jk) * dh + t, scale * ak[c]);
+                        if (av[c] != 0.f) atomicAdd(dv + (bh * K + jk) * dh + t, av[c]);
                     }
                 }
             }
         }
-        __syncthreads();
-        for (int idx = tid; idx < kQR * kDT; idx += 256) {
-            const int jj = idx / kDT, t = idx % kDT, jk = j0 + jj;
-            if (jk < jend && t < dh) {
-                const float a = s_dk[idx], b = s_dv[idx];
-                if (a != 0.f) atomicAdd(dk + (bh * K + jk) * dh + t, a);
-                if (b != 0.f) atomicAdd(dv + (bh * K + jk) * dh + t, b);
-            }
-            s_dk[idx] = 0.f;
-            s_dv[idx] = 0.f;
-        }
-        for (int idx = tid; idx < kSpan * kDT; idx += 256) {
-            const int sl = idx / kDT, t = idx % kDT;
+        // dR of distance slots rid and rid + 32: pairs (rr, jj = rr - slot + 31)
+        for (int sl = rid; sl < kSpan; sl += 32) {
             const long long rrow = (long long)K - 1 - (M + (sl - 31) + i0 - j0);
-            const float a = s_dr[idx];
-            if (a != 0.f && t < dh && rrow >= 0 && rrow < K) atomicAdd(dr + (rrow * H + h) * dh + t, a);
-            s_dr[idx] = 0.f;
+            if (rrow < 0 || rrow >= K) continue;
+            float ar[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ar[c] = 0.f;
+            const int r_lo = sl > 31 ? sl - 31 : 0, r_hi = sl < 31 ? sl : 31;
+            for (int rr = r_lo; rr <= r_hi; ++rr) {
+                const float dsv = s_s[rr * kPS + (rr - sl + 31)];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) ar[c] = fmaf(dsv, s_qv[rr * kDT + cg + 8 * c], ar[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int t = cg + 8 * c;
+                if (t < dh && ar[c] != 0.f) atomicAdd(dr + (rrow * H + h) * dh + t, scale * ar[c]);
+            }
         }
     }
+    {
+        const int i = i0 + rid;
+        if (i < L) {
 #pragma unroll
-    for (int w = 0; w < kRPW; ++w) {
-        const int i = i0 + warp * kRPW + w;
-        if (i >= L) break;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int t = lane + 32 * c;
-            if (t < dh) {
-                dq[(bh * L + i) * dh + t] = scale * (gc[w][c] + gp[w][c]);
-                atomicAdd(du + h * dh + t, scale * gc[w][c]);
-                atomicAdd(dvb + h * dh + t, scale * gp[w][c]);
+            for (int c = 0; c < 8; ++c) {
+                const int t = cg + 8 * c;
+                if (t < dh) {
+                    dq[(bh * L + i) * dh + t] = scale * (gc[c] + gp[c]);
+                    atomicAdd(du + h * dh + t, scale * gc[c]);
+                    atomicAdd(dvb + h * dh + t, scale * gp[c]);
+                }
             }
         }
     }
