@@ -15,10 +15,11 @@
 // one tile list, so the smaller one does not leave a partial round of its own.
 // One CTA per SM walks output tiles of 128 rows x 256 columns; K (= d) is
 // streamed in 64-element steps through a 4-stage TMA ring (A tile 16 KB, B tile
-// 32 KB, 128B swizzle).  Roles (256 threads): warp 0 lane 0 issues the TMA
+// 32 KB, 128B swizzle).  Roles (384 threads): warp 0 lane 0 issues the TMA
 // loads, warp 1 issues the MMAs (whole warp, one elected lane: M=128, N=256,
-// K=16 per instruction into a TMEM accumulator), warps 4-7 drain the
-// accumulator (one row per thread) to bf16 global stores.  Two accumulators of
+// K=16 per instruction into a TMEM accumulator), warps 4-11 drain the
+// accumulator (one row per thread; warps w and w+4 split the 256 columns) to
+// bf16 global stores, with the optional bias / ReLU / residual epilogue.  Two accumulators of
 // 256 columns let the epilogue of one tile overlap the MMAs of the next.
 // Every wait is bounded (1 s) and reports through the device status word.
 #include <cstdint>
@@ -45,7 +46,7 @@ constexpr int BM = 128;     // rows per tile (TMEM lanes)
 constexpr int BN = 256;     // columns per tile (MMA N)
 constexpr int BK = 64;      // K per stage: one 128-byte swizzle row of bf16
 constexpr int STAGES = 4;
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 384;  // warp 0 TMA, 1 MMA, 2-3 idle, 4-11 epilogue
 constexpr uint32_t SZ_A = BM * BK * 2;  // 16 KB
 constexpr uint32_t SZ_B = BN * BK * 2;  // 32 KB
 constexpr uint32_t OFF_A = 0;
@@ -131,7 +132,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh->acc_full[a], 1);
-            mbar_init(&sh->acc_empty[a], 4);  // one arrival per epilogue warp
+            mbar_init(&sh->acc_empty[a], 8);  // one arrival per epilogue warp
         }
         mbar_init(&sh->drain, 1);
         sh->abort = 0;
@@ -230,6 +231,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     } else if (warp >= 4) {
         // ---------------------------------------------------- epilogue
         const int wq = warp & 3;
+        const int chalf = (warp - 4) >> 2;  // columns 128 * chalf .. +127 of the tile
         const int row = wq * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         bool ok = true;
@@ -245,11 +247,11 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
             const PgProblem& pr = p.pr[g];
             const int t = t0 + row;
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = 4 * chalf; cc < 4 * chalf + 4; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_off + acc * BN + 32 * cc, v);
                 tmem_wait_ld();
-                if (cc == BN / 32 - 1) {
+                if (cc == 4 * chalf + 3) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
