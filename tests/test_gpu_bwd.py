@@ -27,7 +27,8 @@ def check(ci, g, rtol, atol, **kw):
 
 @pytest.mark.parametrize("B,H,L,M,dh", [(1, 2, 8, 8, 16), (2, 3, 33, 20, 32), (1, 2, 70, 0, 64),
                                          (1, 1, 40, 90, 64),
-                                         (1, 2, 20, 12, 128)])   # d_h > 64: one query row per warp
+                                         (1, 2, 20, 12, 128),    # d_h > 64: one query row per warp
+                                         (1, 2, 35, 9, 18)])     # d_h not a multiple of 4
 def test_f32_backward_matches_oracle(B, H, L, M, dh):
     ci = W.random_call_inputs(B, H, L, M, dh, dtype=torch.float32, std=0.5, seed=L + M)
     g = torch.randn(B, H, L, dh, generator=torch.Generator().manual_seed(1))

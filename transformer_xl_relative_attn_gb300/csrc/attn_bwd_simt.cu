@@ -154,8 +154,9 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 // consecutive query rows of one (batch row, head), 4 per warp, and sweeps the
 // keys any of them sees in chunks of 32.  Each chunk's K and V rows and the
 // 63 R rows its 32 x 32 pairs use are staged in shared memory once for all
-// 32 query rows (rows padded to 65 floats: lane-per-key reads hit distinct
-// banks).  Sweep 1 gives each row its max, its sum of exp and D_i (online),
+// 32 query rows; every product reads 16-byte vectors (staged rows padded to
+// 68 floats, 17 vectors, so the 8 lanes of a quarter warp reading 8 keys'
+// rows hit distinct banks).  Sweep 1 gives each row its max, its sum of exp and D_i (online),
 // sweep 2 the chunk's P and dS tiles in shared memory, from which every
 // contribution is a small product (dq per row in registers; dk, dV per key
 // and dR per distance summed over the 32 rows), flushed to the global sums
@@ -163,7 +164,7 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 constexpr int kQR = 32;         // query rows per CTA
 constexpr int kRPW = 4;         // query rows per warp (8 warps)
 constexpr int kDT = 64;         // d_h capacity
-constexpr int kPad = 65;        // padded row of a staged tile
+constexpr int kPad = 68;        // padded row of a staged tile (17 x 16 bytes)
 constexpr int kSpan = 63;       // distances one 32 x 32 block of pairs covers
 constexpr int kPS = 33;         // padded row of the P and dS tiles
 constexpr size_t kTiledSmem =
@@ -229,22 +230,31 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         __syncthreads();
     };
     // score of (row rr, key j0 + lane) from the staged tiles
+    // 16-byte views (padding beyond d_h is zero, so whole vectors are summed)
+    const float4* q4u = reinterpret_cast<const float4*>(s_qu);
+    const float4* q4v = reinterpret_cast<const float4*>(s_qv);
+    const float4* d4o = reinterpret_cast<const float4*>(s_do);
+    const float4* k4 = reinterpret_cast<const float4*>(t_k);
+    const float4* v4 = reinterpret_cast<const float4*>(t_v);
+    const float4* r4 = reinterpret_cast<const float4*>(t_r);
+    constexpr int RV = kDT / 4, TV = kPad / 4;  // vectors per row of the row tiles, staged tiles
+    auto dot4 = [](float4 a, float4 b, float c) {
+        return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, c))));
+    };
     auto score = [&](int rr, int jj) {
-        const float* kr = t_k + jj * kPad;
-        const float* rrw = t_r + (rr - jj + 31) * kPad;
+        const int kb4 = jj * TV, rb4 = (rr - jj + 31) * TV;
         float ac = 0.f, bd = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < dh; ++t) {
-            ac = fmaf(s_qu[rr * kDT + t], kr[t], ac);
-            bd = fmaf(s_qv[rr * kDT + t], rrw[t], bd);
+#pragma unroll
+        for (int u = 0; u < RV; ++u) {
+            ac = dot4(q4u[rr * RV + u], k4[kb4 + u], ac);
+            bd = dot4(q4v[rr * RV + u], r4[rb4 + u], bd);
         }
         return scale * (ac + bd);
     };
     auto dprob = [&](int rr, int jj) {
-        const float* vr = t_v + jj * kPad;
         float a = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < dh; ++t) a = fmaf(s_do[rr * kDT + t], vr[t], a);
+#pragma unroll
+        for (int u = 0; u < RV; ++u) a = dot4(d4o[rr * RV + u], v4[jj * TV + u], a);
         return a;
     };
     auto visible = [&](int i, int j) { return i < L && j < jend && j <= M + i && j >= i + 1 - lo_shift; };
@@ -289,9 +299,16 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     // or distance slot = tid / 8, columns tid % 8 + 8c) with no shuffles and
     // no shared atomics; dk, dV, dR flushed with one global atomic each.
     const int rid = tid >> 3, cg = tid & 7;
-    float gc[8], gp[8];
+    // thread columns: 4 cg .. 4 cg + 3 (vector cg) and 32 + 4 cg .. (vector 8 + cg)
+    auto fma4 = [](float s, float4 a, float4& acc) {
+        acc.x = fmaf(s, a.x, acc.x);
+        acc.y = fmaf(s, a.y, acc.y);
+        acc.z = fmaf(s, a.z, acc.z);
+        acc.w = fmaf(s, a.w, acc.w);
+    };
+    float4 gc[2], gp[2];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) gc[c] = gp[c] = 0.f;
+    for (int c = 0; c < 2; ++c) gc[c] = gp[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = jstart; j0 < jend; j0 += 32) {
         stage(j0);
 #pragma unroll
@@ -309,37 +326,42 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         // dq of row rid: sum over the chunk's keys
         for (int jj = 0; jj < 32; ++jj) {
             const float dsv = s_s[rid * kPS + jj];
-            const float* kr = t_k + jj * kPad;
-            const float* rw = t_r + (rid - jj + 31) * kPad;
+            const int kb4 = jj * TV, rb4 = (rid - jj + 31) * TV;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int t = cg + 8 * c;
-                gc[c] = fmaf(dsv, kr[t], gc[c]);
-                gp[c] = fmaf(dsv, rw[t], gp[c]);
+            for (int c = 0; c < 2; ++c) {
+                fma4(dsv, k4[kb4 + 8 * c + cg], gc[c]);
+                fma4(dsv, r4[rb4 + 8 * c + cg], gp[c]);
             }
         }
         // dk, dV of key rid: sums over the 32 query rows
         {
             const int jk = j0 + rid;
-            float ak[8], av[8];
+            float4 ak[2], av[2];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) ak[c] = av[c] = 0.f;
+            for (int c = 0; c < 2; ++c) ak[c] = av[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int rr = 0; rr < kQR; ++rr) {
                 const float dsv = s_s[rr * kPS + rid], pv = s_p[rr * kPS + rid];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int t = cg + 8 * c;
-                    ak[c] = fmaf(dsv, s_qu[rr * kDT + t], ak[c]);
-                    av[c] = fmaf(pv, s_do[rr * kDT + t], av[c]);
+                for (int c = 0; c < 2; ++c) {
+                    fma4(dsv, q4u[rr * RV + 8 * c + cg], ak[c]);
+                    fma4(pv, d4o[rr * RV + 8 * c + cg], av[c]);
                 }
             }
             if (jk < jend) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int t = cg + 8 * c;
+                for (int c = 0; c < 2; ++c) {
+                    const int t = 32 * c + 4 * cg;
                     if (t < dh) {
-                        if (ak[c] != 0.f) atomicAdd(dk + (bh * K + jk) * dh + t, scale * ak[c]);
-                        if (av[c] != 0.f) atomicAdd(dv + (bh * K + jk) * dh + t, av[c]);
+                        float* pk = dk + (bh * K + jk) * dh + t;
+                        float* pv2 = dv + (bh * K + jk) * dh + t;
+                        const float ek[4] = {ak[c].x, ak[c].y, ak[c].z, ak[c].w};
+                        const float ev[4] = {av[c].x, av[c].y, av[c].z, av[c].w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            if (t + x >= dh) break;
+                            if (ek[x] != 0.f) atomicAdd(pk + x, scale * ek[x]);
+                            if (ev[x] != 0.f) atomicAdd(pv2 + x, ev[x]);
+                        }
                     }
                 }
             }
@@ -348,19 +370,25 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         for (int sl = rid; sl < kSpan; sl += 32) {
             const long long rrow = (long long)K - 1 - (M + (sl - 31) + i0 - j0);
             if (rrow < 0 || rrow >= K) continue;
-            float ar[8];
+            float4 ar[2];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) ar[c] = 0.f;
+            for (int c = 0; c < 2; ++c) ar[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             const int r_lo = sl > 31 ? sl - 31 : 0, r_hi = sl < 31 ? sl : 31;
             for (int rr = r_lo; rr <= r_hi; ++rr) {
                 const float dsv = s_s[rr * kPS + (rr - sl + 31)];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) ar[c] = fmaf(dsv, s_qv[rr * kDT + cg + 8 * c], ar[c]);
+                for (int c = 0; c < 2; ++c) fma4(dsv, q4v[rr * RV + 8 * c + cg], ar[c]);
             }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int t = cg + 8 * c;
-                if (t < dh && ar[c] != 0.f) atomicAdd(dr + (rrow * H + h) * dh + t, scale * ar[c]);
+            for (int c = 0; c < 2; ++c) {
+                const int t = 32 * c + 4 * cg;
+                if (t < dh) {
+                    float* pr = dr + (rrow * H + h) * dh + t;
+                    const float e[4] = {ar[c].x, ar[c].y, ar[c].z, ar[c].w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        if (t + x < dh && e[x] != 0.f) atomicAdd(pr + x, scale * e[x]);
+                }
             }
         }
     }
@@ -368,12 +396,18 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         const int i = i0 + rid;
         if (i < L) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int t = cg + 8 * c;
+            for (int c = 0; c < 2; ++c) {
+                const int t = 32 * c + 4 * cg;
                 if (t < dh) {
-                    dq[(bh * L + i) * dh + t] = scale * (gc[c] + gp[c]);
-                    atomicAdd(du + h * dh + t, scale * gc[c]);
-                    atomicAdd(dvb + h * dh + t, scale * gp[c]);
+                    const float ec[4] = {gc[c].x, gc[c].y, gc[c].z, gc[c].w};
+                    const float ep[4] = {gp[c].x, gp[c].y, gp[c].z, gp[c].w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        if (t + x >= dh) break;
+                        dq[(bh * L + i) * dh + t + x] = scale * (ec[x] + ep[x]);
+                        atomicAdd(du + h * dh + t + x, scale * ec[x]);
+                        atomicAdd(dvb + h * dh + t + x, scale * ep[x]);
+                    }
                 }
             }
         }
