@@ -571,7 +571,7 @@ def build_stack(wl, dev, stream):
     layer projected once by txl_r_proj from the sinusoid of distances
     M+L-1 .. 0, layer 0's memory in rows, the others in heads.  When L < M
     the memories are ring buffers (each segment writes L rows instead of
-    moving M)."""
+    moving M).  The rolls run on a second stream, overlapping the attention."""
     import transformer_xl_relative_attn_gb300 as txl
     bf = torch.bfloat16
     p = W.make_params(wl)
@@ -586,7 +586,8 @@ def build_stack(wl, dev, stream):
         mems = [m0[0].to(dev, bf)] + [W._split_heads(m, H).to(dev, bf) for m in m0[1:]]
     stream.synchronize()
     ring = wl.L < wl.M and wl.L % 128 == 0 and wl.M % 128 == 0
-    return txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, wl.L, stream=stream, ring=ring)
+    return txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, wl.L, stream=stream, ring=ring,
+                         mem_stream=torch.cuda.Stream(device=dev))
 
 
 def measure_e2e_stack(args, wl, dev, flops_step, ws):

@@ -65,7 +65,7 @@ def test_ring_rejects_unaligned_start():
         txl.qkv_proj(z, m, w, H, mem_start=64)
 
 
-def make(ring):
+def make(ring, mem_stream=None):
     wl = W.WORKLOADS["seg128_bf16"].with_(B=2, H=4, L=128, M=384, layers=2, segments=5)
     dev = torch.device("cuda")
     p = W.make_params(wl)
@@ -76,7 +76,7 @@ def make(ring):
     u, vb = [p.u.to(dev, BF)] * wl.layers, [p.v.to(dev, BF)] * wl.layers
     m0 = W.initial_memories(wl)
     mems = [m0[0].to(dev, BF)] + [W._split_heads(m, H).to(dev, BF) for m in m0[1:]]
-    return wl, txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, L, ring=ring)
+    return wl, txl.AttnStack(w_qkv, r_k, u, vb, mems, wl.scale, H, L, ring=ring, mem_stream=mem_stream)
 
 
 def test_ring_stack_reproduces_the_copying_stack():
@@ -91,3 +91,19 @@ def test_ring_stack_reproduces_the_copying_stack():
         for x, y in zip(a.logical_mems(), b.logical_mems()):
             assert torch.equal(x, y)
     assert b.start == (wl.segments * wl.L) % wl.M
+
+
+@pytest.mark.parametrize("ring", [False, True])
+def test_rolls_on_a_second_stream_change_nothing(ring):
+    """The rolls (or ring pushes) on their own stream, overlapping the
+    attention, give bit-identical outputs and memories."""
+    wl, a = make(ring)
+    _, b = make(ring, mem_stream=torch.cuda.Stream())
+    for s in range(wl.segments):
+        h0 = W.segment_input(wl, s).cuda().to(BF)
+        oa = a.run_segment(h0).clone()
+        ob = b.run_segment(h0).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), s
+    for x, y in zip(a.logical_mems(), b.logical_mems()):
+        assert torch.equal(x, y)

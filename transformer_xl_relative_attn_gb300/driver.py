@@ -151,9 +151,13 @@ class AttnStack:
     the oldest ones instead of moving all M (``logical_mems`` gives the
     unrotated view; ring needs M and L multiples of 128 and ext_len = 0).
 
-    The roll of mems[n] reads h after its projection has read mems[n]; all
-    launches go to one stream, which orders every dependency of the
-    recurrence.  q, k and v are one set of buffers reused by every layer; each
+    The roll of mems[n] reads h after its projection has read mems[n].  On
+    one stream that order is the launch order; with ``mem_stream`` each roll
+    runs there, after an event recorded behind its projection, overlapping
+    the layer's attention, and the stream waits for all rolls at the end of
+    the segment (so the next segment, and whatever the caller launches after
+    run_segment, sees the rolled memories and may reuse h0).  q, k and v are
+    one set of buffers reused by every layer; each
     layer's output has its own buffer (the next layer's input and the source
     of its memory roll).
     """
@@ -162,7 +166,7 @@ class AttnStack:
                  u: Sequence[torch.Tensor], v_bias: Sequence[torch.Tensor],
                  mems: Sequence[torch.Tensor], scale: float, n_head: int, seg_len: int,
                  stream: torch.cuda.Stream | None = None, same_length: bool = False,
-                 ext_len: int = 0, ring: bool = False):
+                 ext_len: int = 0, ring: bool = False, mem_stream: torch.cuda.Stream | None = None):
         n = len(mems)
         if not (len(w_qkv) == len(r_k) == len(u) == len(v_bias) == n) or n == 0:
             raise ValueError("need one weight, r_k, u, v and memory per layer")
@@ -185,6 +189,7 @@ class AttnStack:
         self.scale, self.H, self.L = float(scale), H, int(seg_len)
         self.same_length, self.ext_len = bool(same_length), int(ext_len)
         self.ring, self.start = bool(ring), 0
+        self.mem_stream = mem_stream
         if self.ring and (self.ext_len or int(seg_len) % 128 or m0.shape[1] % 128):
             raise ValueError("ring memories need ext_len = 0 and M, L multiples of 128")
         self.B, self.M, self.d, self.dh = B, M, d, dh
@@ -219,10 +224,18 @@ class AttnStack:
                     rec = {"n": n, "h": h.clone(), "mem": mem.clone()}
                 _lib.qkv_proj(h, mem, self.w_qkv[n], self.H, q=self.q, k=self.k, v=self.v,
                               stream=self.stream, mem_start=self.start if self.ring else 0)
+                rs = self.stream
+                if self.mem_stream is not None:
+                    projected = torch.cuda.Event()
+                    projected.record(self.stream)
+                    self.mem_stream.wait_event(projected)
+                    rs = self.mem_stream
                 if self.ring:
-                    new_start = _push(mem, h, self.start, self.stream)
+                    new_start = _push(mem, h, self.start, rs)
                 else:
-                    _roll(mem, h, self.stream, self.ext_len)
+                    _roll(mem, h, rs, self.ext_len)
+                if self.mem_stream is not None and n == 0:
+                    h.record_stream(self.mem_stream)  # the caller's h0 stays allocated for the roll
                 dst = out if (out is not None and n == len(self.mems) - 1) else self.outs[n]
                 o = _lib.attn_fwd(self.q, self.k, self.v, self.r_k[n], self.u[n], self.v_bias[n],
                                   self.scale, out=dst, stream=self.stream,
@@ -231,6 +244,10 @@ class AttnStack:
                     rec.update(q=self.q.clone(), k=self.k.clone(), v=self.v.clone(), out=o.clone())
                     trace.append(rec)
                 h = o
+            if self.mem_stream is not None:
+                rolled = torch.cuda.Event()
+                rolled.record(self.mem_stream)
+                self.stream.wait_event(rolled)
         if self.ring:
             self.start = new_start
         self.segments_done += 1
