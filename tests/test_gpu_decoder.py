@@ -33,6 +33,8 @@ def rnd(*shape, std=1.0, seed=0):
     (2, 256, 512, 1024, False, True, True, False),    # first feed-forward layer
     (1, 384, 1024, 512, False, True, False, True),    # second layer with the residual
     (2, 128, 512, 512, True, False, False, False),    # o_net on a head-split attention output
+    (8, 1024, 256, 2048, False, True, True, True),    # enough tiles for the 256-column tile width
+    (8, 1024, 512, 512, True, False, False, True),    # 256 tiles of 128 x 128: the narrow width
 ])
 def test_linear_matches_oracle(B, T, K, N, heads, bias, relu, resid):
     x = rnd(B, T, K, seed=1)

@@ -43,19 +43,27 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
 
 namespace pg {
 constexpr int BM = 128;     // rows per tile (TMEM lanes)
-constexpr int BN = 256;     // columns per tile (MMA N)
 constexpr int BK = 64;      // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
 constexpr int NTHREADS = 384;  // warp 0 TMA, 1 MMA, 2-3 idle, 4-11 epilogue
 constexpr uint32_t SZ_A = BM * BK * 2;  // 16 KB
-constexpr uint32_t SZ_B = BN * BK * 2;  // 32 KB
 constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * SZ_A;
-constexpr uint32_t OFF_BAR = OFF_B + STAGES * SZ_B;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one sm_103a CTA");
-constexpr uint32_t TMEM_COLS = 512;     // two accumulators of BN columns
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0);
+constexpr int MAX_STAGES = 6;
+
+// Tile width BN (MMA N): 256 for the projections and wide outputs; 128 when
+// the 256-wide tiles would leave most SMs with one tile and some with two.
+template <int BN_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = BN_ == 256 ? 4 : 6;
+    static constexpr uint32_t SZ_B = BN_ * BK * 2;   // 32 or 16 KB
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * SZ_A;
+    static constexpr uint32_t OFF_BAR = OFF_B + STAGES * SZ_B;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * BN_;  // two accumulators
+    static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_, 0);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget of one sm_103a CTA");
+    static_assert(STAGES <= MAX_STAGES, "barrier arrays");
+};
 }  // namespace pg
 
 // One GEMM of the launch: per batch row, Ta rows of source a (the memory)
@@ -85,8 +93,8 @@ struct PgParams {
 };
 
 struct PgShared {
-    uint64_t full[pg::STAGES];
-    uint64_t empty[pg::STAGES];
+    uint64_t full[pg::MAX_STAGES];
+    uint64_t empty[pg::MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -96,23 +104,29 @@ struct PgShared {
 
 // Tile w of the launch: problem 0's tiles, then problem 1's; within a
 // problem the column tile runs fastest, then the row tile, then the batch row.
+template <int BN>
 __device__ __forceinline__ int pg_tile(const PgParams& p, int w, int& b, int& t0, int& n0) {
     const int g = w < p.pr[0].tiles ? 0 : 1;
     const PgProblem& pr = p.pr[g];
     if (g) w -= p.pr[0].tiles;
     const int nt = w % pr.n_nt, rest = w / pr.n_nt;
-    n0 = nt * pg::BN;
+    n0 = nt * BN;
     t0 = (rest % pr.n_rt) * pg::BM;
     b = rest / pr.n_rt;
     return g;
 }
 
+template <int BN_>
 __global__ void __launch_bounds__(pg::NTHREADS, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                  const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmA1,
                  const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmW1,
                  const PgParams p) {
     using namespace pg;
+    using C = Cfg<BN_>;
+    constexpr int BN = C::BN, STAGES = C::STAGES;
+    constexpr uint32_t SZ_B = C::SZ_B, OFF_B = C::OFF_B, OFF_BAR = C::OFF_BAR, TMEM_COLS = C::TMEM_COLS,
+                       IDESC = C::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -157,7 +171,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
             int c = 0;  // loads issued into the ring
             for (int w = blockIdx.x; ok && w < p.n_tiles; w += gridDim.x) {
                 int b, t0, n0;
-                const int g = pg_tile(p, w, b, t0, n0);
+                const int g = pg_tile<BN>(p, w, b, t0, n0);
                 const int Ta = p.pr[g].Ta;
                 // a row tile lies wholly in one source (Ta is a multiple of BM)
                 const CUtensorMap* mA = t0 < Ta ? (g ? &tmA1 : &tmA0) : (g ? &tmB1 : &tmB0);
@@ -231,7 +245,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     } else if (warp >= 4) {
         // ---------------------------------------------------- epilogue
         const int wq = warp & 3;
-        const int chalf = (warp - 4) >> 2;  // columns 128 * chalf .. +127 of the tile
+        const int chalf = (warp - 4) >> 2;  // columns (BN / 2) chalf .. of the tile
+        constexpr int CPW = BN / 64;         // 32-column chunks per epilogue warp
         const int row = wq * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         bool ok = true;
@@ -243,15 +258,15 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
             if (!ok) break;
             tc_fence_after();
             int b, t0, n0;
-            const int g = pg_tile(p, w, b, t0, n0);
+            const int g = pg_tile<BN>(p, w, b, t0, n0);
             const PgProblem& pr = p.pr[g];
             const int t = t0 + row;
 #pragma unroll 1
-            for (int cc = 4 * chalf; cc < 4 * chalf + 4; ++cc) {
+            for (int cc = CPW * chalf; cc < CPW * chalf + CPW; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_off + acc * BN + 32 * cc, v);
                 tmem_wait_ld();
-                if (cc == 4 * chalf + 3) {
+                if (cc == CPW * chalf + CPW - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
@@ -372,10 +387,12 @@ static int pg_num_sms() {
 cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
                              int plain, int* status, cudaStream_t stream) {
     using namespace pg;
+    using C = Cfg<256>;
+    constexpr int BN = C::BN;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -434,21 +451,24 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_tiles = (int)total;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(maps[0][0], maps[0][1], maps[0][2], maps[1][0],
+    proj_gemm_kernel<256><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(maps[0][0], maps[0][1], maps[0][2], maps[1][0],
                                                             maps[1][1], maps[1][2], p);
     return cudaGetLastError();
 }
 
 // A plain Linear over rows of x (layout 0: [B, T, K]; 1: [B, K / 64, T, 64]):
 // out [B, T, N] = relu?(x W^T + bias) + resid, all bf16, fp32 accumulation.
-cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const void* w, int N,
-                          const void* bias, const void* resid, int relu, void* out, int* status,
-                          cudaStream_t stream) {
+template <int BN_>
+static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, int K, const void* w, int N,
+                                   const void* bias, const void* resid, int relu, void* out, int* status,
+                                   cudaStream_t stream) {
     using namespace pg;
+    using C = Cfg<BN_>;
+    constexpr int BN = C::BN;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<BN_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -496,9 +516,20 @@ cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const
     p.pr[1].tiles = 0;
     p.n_tiles = (int)tiles;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    proj_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[0], maps[1],
+    proj_gemm_kernel<BN_><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[0], maps[1],
                                                             maps[2], p);
     return cudaGetLastError();
+}
+
+// 256-column tiles unless that leaves fewer than two tiles per SM (then
+// 128-column tiles: twice the tiles, each half the work, for a better fill).
+cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const void* w, int N,
+                          const void* bias, const void* resid, int relu, void* out, int* status,
+                          cudaStream_t stream) {
+    const long long wide = (long long)B * (T / pg::BM) * (N / 256);
+    if (wide < 2ll * pg_num_sms())
+        return launch_linear_bn<128>(x, x_heads, B, T, K, w, N, bias, resid, relu, out, status, stream);
+    return launch_linear_bn<256>(x, x_heads, B, T, K, w, N, bias, resid, relu, out, status, stream);
 }
 
 }  // namespace txl
