@@ -55,7 +55,12 @@
 // tile by TMA, then rewritten in place), P x2, K/V ring, R ring.  A group's P
 // buffer is also the scratch of its per-row shift: after the group's previous
 // P V finished and before the new P is written, each warp moves its rows'
-// band windows through its 4 KB quarter of it.
+// band windows through its 4 KB quarter of it, two band columns (c, c+32)
+// per 32-bit word as f16x2 (the position term is rounded to f16 there and
+// added to the f32 content term in f32).
+//
+// Registers: warps 8-11 give up registers (setmaxnreg) so that each softmax
+// thread can hold its row's 64 content terms and 96 band columns at once.
 //
 // Ordering facts relied on: tcgen05.mma operations from one thread execute in
 // issue order, and a tcgen05.commit arrives only when every MMA issued before
@@ -238,6 +243,24 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+// Two f32 values rounded to f16 (finite: out-of-range values saturate to
+// +-65504) in one 32-bit word, lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// (lo(h) + a, hi(h) + b): each f16 half of h added in f32 to an f32 value
+__device__ __forceinline__ float2 add_h2_f32(uint32_t h, float a, float b) {
+    float d, e;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+        : "=f"(d), "=f"(e)
+        : "r"(h), "f"(a), "f"(b));
+    return make_float2(d, e);
+}
+
 // (a.x + b.x, a.y + b.y) in one packed instruction
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     uint64_t r;
@@ -354,6 +377,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
+    // Register split: the softmax warpgroups hold a whole tile's scores and
+    // band (160 values) at once.  Launched with 168 per thread (384 x 168 =
+    // 64,512); 2 x 128 x 200 + 128 x 96 = 63,488 fits in that.
+    if (warp >= 8)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
 
     if (warp < 8) {
         // ------------------------------------------------------ softmax groups
@@ -465,47 +495,56 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const int jlim = p.M + i - j0;       // keys jj > jlim are masked
                 const int jlo = i + 1 - p.lo_shift - j0;  // and keys jj < jlo
                 float sc[BN];
-                float tmax = -INFINITY;
+                {
+                    // the tile's AC (64 columns) and band columns c0 .. c0+95,
+                    // c0 = 96 - 32*wq: row ii's window starts at band column
+                    // 127 - ii = c0 + (31 - lane).  Band column c lives in ring
+                    // slot (global slot of t) + c/64 (item slot t + c/64 is
+                    // global slot gbase + t + c/64).  One wait, then the
+                    // scores are released to the next pair's MMAs.
+                    uint32_t ac[BN], bw[96];
+                    tmem_ld32(tmem + lane_off + col_ac, *reinterpret_cast<uint32_t(*)[32]>(&ac[0]));
+                    tmem_ld32(tmem + lane_off + col_ac + 32, *reinterpret_cast<uint32_t(*)[32]>(&ac[32]));
 #pragma unroll
-                for (int q2 = 0; q2 < BN / 32; ++q2) {
-                    uint32_t ac[32], w0[32], w1[32];
-                    tmem_ld32(tmem + lane_off + col_ac + 32 * q2, ac);
-                    // band columns c0 .. c0+63 of this tile, c0 = 96 - 32*wq + 32*q2;
-                    // band column c lives in ring slot (global slot of t) + c/64
-                    // (item slot t + c/64 is global slot gbase + t + c/64)
-                    const int cA = 96 - 32 * wq + 32 * q2, cB = cA + 32;
-                    const uint32_t rA =
-                        COL_RING + 64 * ((gbase + t + (cA >> 6)) & (RING - 1)) + (cA & 63);
-                    const uint32_t rB =
-                        COL_RING + 64 * ((gbase + t + (cB >> 6)) & (RING - 1)) + (cB & 63);
-                    tmem_ld32(tmem + lane_off + rA, w0);
-                    tmem_ld32(tmem + lane_off + rB, w1);
-                    tmem_wait_ld();
-                    if (q2 == BN / 32 - 1) {
-                        tc_fence_before();
-                        warp_arrive(&sh->s_free[grp]);
+                    for (int kc = 0; kc < 3; ++kc) {
+                        const int c = 96 - 32 * wq + 32 * kc;
+                        const uint32_t rc = COL_RING + 64 * ((gbase + t + (c >> 6)) & (RING - 1)) + (c & 63);
+                        tmem_ld32(tmem + lane_off + rc, *reinterpret_cast<uint32_t(*)[32]>(&bw[32 * kc]));
                     }
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    warp_arrive(&sh->s_free[grp]);
+                    // The shift moves band pairs (c, c+32) packed as f16x2, so
+                    // one pass through the warp's scratch aligns both halves of
+                    // the window: word K = (band c0+K, band c0+K+32), and
+                    // position x of the shifted row is word (31 - lane) + x =
+                    // the terms of keys x and x+32.  Half the shared-memory
+                    // traffic of moving f32 values; the f16 rounding of the
+                    // position term is bounded in the design notes.
+                    uint32_t hp[64];
+#pragma unroll
+                    for (int K = 0; K < 64; ++K)
+                        hp[K] = pack_f16x2_sat(__uint_as_float(bw[K]), __uint_as_float(bw[K + 32]));
                     float win[32];
-                    st_shift_all<0>(31 - lane, t_st, w0, w1);
+                    st_shift_all<0>(31 - lane, t_st, *reinterpret_cast<uint32_t(*)[32]>(&hp[0]),
+                                    *reinterpret_cast<uint32_t(*)[32]>(&hp[32]));
                     ld_shift_all<0>(t_ld, win);
 #pragma unroll
-                    for (int x = 0; x < 32; x += 2) {
-                        const float2 s2 =
-                            add2(make_float2(__uint_as_float(ac[x]), __uint_as_float(ac[x + 1])),
-                                 make_float2(win[x], win[x + 1]));
-                        sc[32 * q2 + x] = s2.x;
-                        sc[32 * q2 + x + 1] = s2.y;
+                    for (int x = 0; x < 32; ++x) {
+                        const float2 s2 = add_h2_f32(__float_as_uint(win[x]), __uint_as_float(ac[x]),
+                                                     __uint_as_float(ac[x + 32]));
+                        sc[x] = s2.x;
+                        sc[x + 32] = s2.y;
                     }
-                    if (need_mask) {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            if (32 * q2 + x > jlim || (LOWER && 32 * q2 + x < jlo))
-                                sc[32 * q2 + x] = -INFINITY;
-                    }
-#pragma unroll
-                    for (int x = 0; x < 32; x += 2)
-                        tmax = max3(tmax, sc[32 * q2 + x], sc[32 * q2 + x + 1]);
                 }
+                if (need_mask) {
+#pragma unroll
+                    for (int x = 0; x < BN; ++x)
+                        if (x > jlim || (LOWER && x < jlo)) sc[x] = -INFINITY;
+                }
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int x = 0; x < BN; x += 2) tmax = max3(tmax, sc[x], sc[x + 1]);
                 // Conditional rescale: keep the running max unless the tile's max
                 // exceeds it by more than the threshold (then p <= 2^threshold).
                 const float m_new = (tmax > m_run + kRescaleThreshold) ? tmax : m_run;
