@@ -45,7 +45,9 @@
 //   warp 9     lane 0 issues the TMA loads (128-row boxes: per-SM TMA
 //              throughput grows with the box size) and L2 prefetches
 //   warp 10    issues the P V MMAs
-//   warp 11    idle (keeps every sub-partition at three warps)
+//   warp 11    prepares the score MMAs' A operands of each item: loads the
+//              raw q tile by TMA into both slots of the item's Q buffer and
+//              rewrites them in place as (q+u)c and (q+v)c
 // The score and P V chains are issued from different sub-partitions so that
 // neither waits behind the other or behind the softmax warps' instruction
 // streams.
@@ -145,7 +147,7 @@ struct TcShared {
     uint64_t r_full[tc::R_STAGES];
     uint64_t r_empty[tc::R_STAGES];
     uint64_t q_ready;     // (q+u)c and (q+v)c of the next item are in shared memory
-    uint64_t q_full[2];   // the raw q tile of the next item landed in group g's slot
+    uint64_t q_full;      // the raw q tile of the next item landed in both slots
     uint64_t s_full[2];   // scores of the group's next tile are in TMEM
     uint64_t s_free[2];   // the group has read them into registers
     uint64_t p_full[2];   // the group's P tile is in shared memory
@@ -153,6 +155,7 @@ struct TcShared {
     uint64_t o_done;      // every MMA of the item finished: O may be read
     uint64_t o_free;      // the merge has read both O accumulators
     uint64_t drain;
+    uint64_t q_free;      // the first score pair of an item (and all before it) completed
     uint32_t tmem_base;
     int abort;
 };
@@ -352,9 +355,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&sh->r_empty[s], 1);
         }
         // softmax-side barriers count warps: one elected lane per warp arrives
-        mbar_init(&sh->q_ready, 8);
+        mbar_init(&sh->q_ready, 1);
+        mbar_init(&sh->q_full, 1);
+        mbar_init(&sh->q_free, 1);
         for (int g = 0; g < 2; ++g) {
-            mbar_init(&sh->q_full[g], 1);
             mbar_init(&sh->s_full[g], 1);
             mbar_init(&sh->s_free[g], 4);
             mbar_init(&sh->p_full[g], 4);
@@ -397,75 +401,12 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // scratch T[pos][lane] (word pos * 32 + lane) before P is written
         const uint32_t t_ld = p_tile + wq * 4096 + 4 * lane;
         const uint32_t t_st = t_ld - 128u * (uint32_t)(31 - lane);
-        const float qscale = p.scale_log2;
-
-        // (q+u)c (group 0) or (q+v)c (group 1) of an item, rounded to bf16, in
-        // the group's slot of Q buffer kbuf.  One thread of the group loads the
-        // raw q tile there by TMA (128B swizzle: chunk c of row ii at chunk
-        // c ^ (ii & 7); rows past L arrive as zeros); later each thread turns
-        // its own row into (q+bias)c in place.  The buffer is free when the
-        // load is issued: its last readers were the score MMAs of the item
-        // before the current one, which completed before the current item's
-        // first scores.
         bool ok = true;
-        auto issue_q = [&](const Item& it, int kbuf) {
-            if (ii == 0) {
-                mbar_expect_tx(&sh->q_full[grp], SZ_Q);
-                tma_load_3d(smem + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q, &tmQ, &sh->q_full[grp], 0,
-                            it.i0, it.bh);
-            }
-            const void* brow = (grp == 0 ? p.ub : p.vb) + (size_t)it.h * DH;
-            if ((ii & 31) == 0) asm volatile("prefetch.global.L1 [%0];" ::"l"(brow));
-        };
-        auto write_q = [&](const Item& it, int kbuf, int kq) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full[grp], kq & 1, kDevTimeoutSoftmax,
-                                                   abort, p.status));
-            if (!ok) return;
-            const uint4* brow =
-                reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)it.h * DH);
-            const uint32_t row = s_base + OFF_Q + kbuf * 2 * SZ_Q + grp * SZ_Q + ii * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint32_t a = row + ((ch ^ (ii & 7)) << 4);
-                float raw[4];
-                ld_shared_v4(a, raw);
-                const uint4 b4 = __ldg(brow + ch);
-                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b4);
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 qf = __bfloat1622float2(q2[e]);
-                    const float2 bf = __bfloat1622float2(b2[e]);
-                    w[e] = pack_bf16x2((qf.x + bf.x) * qscale, (qf.y + bf.y) * qscale);
-                }
-                st_shared_v4(a, w[0], w[1], w[2], w[3]);
-            }
-            fence_proxy_async_smem();
-            warp_arrive(&sh->q_ready);
-        };
 
         Item cur;
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
         for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, cur); ++k) {
-            // the first item's q tile; a failed wait leaves ok false, and the
-            // group still reaches this item's merge barriers below
-            if (k == 0) {
-                issue_q(cur, 0);
-                write_q(cur, 0, 0);
-            }
-            Item nxt;
-            const bool has_next = item_of<SPLIT, LOWER>(p, k + 1, nxt);
-            // the next item's q tile: loaded once this group holds the current
-            // item's first scores, turned into (q+bias)c after that tile
-            bool next_issued = !has_next, next_written = !has_next;
-            auto write_next_q = [&]() {
-                if (!next_issued) issue_q(nxt, (k + 1) & 1);
-                next_issued = true;
-                write_q(nxt, (k + 1) & 1, k + 1);
-                next_written = true;
-            };
             const int i = cur.i0 + ii;
             float m_run = -INFINITY;  // running max (log2 domain), may lag the true max by < 8
             float l_run = 0.f;
@@ -475,10 +416,6 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                                        kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
                 tc_fence_after();
-                if (!next_issued) {
-                    issue_q(nxt, (k + 1) & 1);
-                    next_issued = true;
-                }
                 if (it_g > 0) {
                     // the group's previous P V must be done before its P buffer
                     // is reused (shift scratch, then P) or O is rescaled
@@ -588,9 +525,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 warp_arrive(&sh->p_full[grp]);
                 ++it_g;
                 ++seen;
-                if (!next_written) write_next_q();
             }
-            if (ok && !next_written) write_next_q();
             // ---------------------------------------------- merge + store
             if (ok)
                 ok = __all_sync(0xffffffffu,
@@ -756,6 +691,9 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             mma_ss_elect(d_r, a_qv + 2 * k, b_r + 2 * k, IDESC_N128, k > 0, leader);
                     }
                     if (leader) {
+                        // the first pair of item ks: issued after q_ready of item
+                        // ks and after every MMA of item ks-1
+                        if (pp == 0) mma_commit(&sh->q_free);
                         if (!(p.inject == 1 && ks == 0 && pp == 0)) mma_commit(&sh->s_full[0]);
                         if (two) mma_commit(&sh->s_full[1]);
                         // R boxes 0 .. pp+1 are not read again
@@ -828,6 +766,67 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (leader) mma_commit(&sh->drain);
             drain_wait(&sh->drain, 0, p.status);
         }
+        __syncwarp();
+    } else if (warp == 11) {
+        // ------------------------------------------------ q+u, q+v operands
+        // Item k's operands live in Q buffer k & 1: (q+u)c in slot 0, (q+v)c in
+        // slot 1, c = scale * log2 e, rounded to bf16.  The raw q tile arrives
+        // by TMA in both slots (128B swizzle: chunk ch of row r at chunk
+        // ch ^ (r & 7); rows past L arrive as zeros) and is rewritten in place.
+        // Item k >= 1 waits for q_free completion k-1 (the first pair of item
+        // k-1 and everything before it completed): the issuer has consumed
+        // q_ready of item k-1, so q_ready never runs two phases ahead of its
+        // waits, and the score MMAs of item k-2, the last readers of buffer
+        // k & 1, are done.  Likewise q_free completion k needs q_ready of item
+        // k, so it never runs two phases ahead of this warp's waits.
+        const float qscale = p.scale_log2;
+        const int ch = lane & 7;  // the lane's 16-byte chunk of every row it converts
+        bool ok = true;
+        int issued = 0, landed = 0;  // q tiles loaded / observed in shared memory
+        Item it;
+        for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
+            if (k >= 1)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&sh->q_free, (k - 1) & 1, kDevTimeoutMma, abort, p.status));
+            if (!ok) break;
+            const uint32_t qb = OFF_Q + (k & 1) * 2 * SZ_Q;
+            if (lane == 0) {
+                mbar_expect_tx(&sh->q_full, 2 * SZ_Q);
+                tma_load_3d(smem + qb, &tmQ, &sh->q_full, 0, it.i0, it.bh);
+                tma_load_3d(smem + qb + SZ_Q, &tmQ, &sh->q_full, 0, it.i0, it.bh);
+            }
+            ++issued;
+            const uint4 bu = __ldg(reinterpret_cast<const uint4*>(p.ub + (size_t)it.h * DH) + ch);
+            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.vb + (size_t)it.h * DH) + ch);
+            ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full, k & 1, kDevTimeoutMma, abort, p.status));
+            if (!ok) break;
+            ++landed;
+#pragma unroll 4
+            for (int r = lane >> 3; r < BM; r += 4) {
+                const uint32_t a = s_base + qb + r * 128 + ((ch ^ (r & 7)) << 4);
+#pragma unroll
+                for (int slot = 0; slot < 2; ++slot) {
+                    const uint4& b4 = slot ? bv : bu;
+                    float raw[4];
+                    ld_shared_v4(a + slot * SZ_Q, raw);
+                    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b4);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 qf = __bfloat1622float2(q2[e]);
+                        const float2 bf = __bfloat1622float2(b2[e]);
+                        w[e] = pack_bf16x2((qf.x + bf.x) * qscale, (qf.y + bf.y) * qscale);
+                    }
+                    st_shared_v4(a + slot * SZ_Q, w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->q_ready);
+        }
+        // drain: a q tile still in flight lands before the CTA exits
+        if (landed < issued) drain_wait(&sh->q_full, (issued - 1) & 1, p.status);
         __syncwarp();
     } else if (warp == 9) {
         // ------------------------------------------------------ TMA producer
