@@ -158,6 +158,7 @@ struct TcShared {
     uint64_t q_free;      // the first score pair of an item (and all before it) completed
     uint32_t tmem_base;
     int abort;
+    int merge_abort;      // the abort flag as seen once per item by the merge
 };
 
 // One work unit and the quantities every role derives from it: the key tiles
@@ -264,6 +265,32 @@ __device__ __forceinline__ float2 add_h2_f32(uint32_t h, float a, float b) {
     return make_float2(d, e);
 }
 
+// TMA store of a shared-memory box to a 3-D tensor (out-of-range rows are
+// clipped), committed as one bulk group of the issuing thread
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// the issuing thread's bulk stores have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the issuing thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// one arrival on an mbarrier that counts as n
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n)
+                 : "memory");
+}
+
 // (a.x + b.x, a.y + b.y) in one packed instruction
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     uint64_t r;
@@ -329,7 +356,7 @@ template <bool SPLIT, bool LOWER>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
 attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
-                    const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmO, const TcParams p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -355,7 +382,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&sh->r_empty[s], 1);
         }
         // softmax-side barriers count warps: one elected lane per warp arrives
-        mbar_init(&sh->q_ready, 1);
+        mbar_init(&sh->q_ready, 8);  // 8 warp arrivals, or one arrival counting 8
         mbar_init(&sh->q_full, 1);
         mbar_init(&sh->q_free, 1);
         for (int g = 0; g < 2; ++g) {
@@ -407,6 +434,43 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
         for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, cur); ++k) {
+            if (k == 0) {
+                // the first item's operands: the groups are idle until its first
+                // scores, so they convert it themselves (warp 11 takes the rest)
+                if (tid == 0) {
+                    mbar_expect_tx(&sh->q_full, 2 * SZ_Q);
+                    tma_load_3d(smem + OFF_Q, &tmQ, &sh->q_full, 0, cur.i0, cur.bh);
+                    tma_load_3d(smem + OFF_Q + SZ_Q, &tmQ, &sh->q_full, 0, cur.i0, cur.bh);
+                }
+                const uint4* brow = reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)cur.h * DH);
+                uint4 b4[8];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) b4[ch] = __ldg(brow + ch);
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full, 0, kDevTimeoutSoftmax, abort, p.status));
+                if (!ok && tid == 0) drain_wait(&sh->q_full, 0, p.status);
+                if (ok) {
+                    const uint32_t row = s_base + OFF_Q + grp * SZ_Q + ii * 128;
+                    const float qscale = p.scale_log2;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t a = row + ((ch ^ (ii & 7)) << 4);
+                        float raw[4];
+                        ld_shared_v4(a, raw);
+                        const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
+                        const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(&b4[ch]);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 qf = __bfloat1622float2(q2[e]);
+                            const float2 bf = __bfloat1622float2(bb[e]);
+                            w[e] = pack_bf16x2((qf.x + bf.x) * qscale, (qf.y + bf.y) * qscale);
+                        }
+                        st_shared_v4(a, w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async_smem();
+                    warp_arrive(&sh->q_ready);
+                }
+            }
             const int i = cur.i0 + ii;
             float m_run = -INFINITY;  // running max (log2 domain), may lag the true max by < 8
             float l_run = 0.f;
@@ -550,10 +614,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mo = ml_in[2 * ii];
                 lo = ml_in[2 * ii + 1];
             }
+            // One snapshot of the abort flag decides for all 256 threads, so
+            // that either every softmax warp runs the merge (with its group
+            // barriers) and the next item, or none does.  A warp whose wait
+            // failed set the flag before it reached the first barrier.
+            if (tid == 0) sh->merge_abort = *abort;
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            // a failed wait anywhere sets the abort flag: both groups leave
-            // together, so neither waits alone at a later named barrier
-            if (*abort) ok = false;
+            if (*reinterpret_cast<volatile int*>(&sh->merge_abort)) ok = false;
             if (ok) {
                 tc_fence_after();
                 // (m, l) of group 0 and group 1
@@ -573,8 +640,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
                     const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
                     const float a0 = f0 * inv, a1 = f1 * inv;
-                    uint4* orow =
-                        reinterpret_cast<uint4*>(p.out + ((size_t)cur.bh * p.L + i) * DH) + 4 * grp;
+                    // the group's 32 output columns of the tile go out as one TMA
+                    // store of a 128 x 32 box, staged in the upper half of the
+                    // group's P buffer (free: its last P V finished; the merge
+                    // exchange uses the lower 1 KB) in the 64-byte swizzle the
+                    // store expects: chunk c of row ii at chunk c ^ ((ii >> 1) & 3),
+                    // which also spreads each 8-thread phase over all banks
+                    const uint32_t stage = p_tile + 8192;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float y[8];
@@ -583,13 +655,17 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
                             y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
                         }
-                        uint4 w;
-                        w.x = pack_bf16x2(y[0], y[1]);
-                        w.y = pack_bf16x2(y[2], y[3]);
-                        w.z = pack_bf16x2(y[4], y[5]);
-                        w.w = pack_bf16x2(y[6], y[7]);
-                        if (i < p.L) orow[c] = w;
+                        st_shared_v4(stage + ii * 64 + ((c ^ ((ii >> 1) & 3)) << 4), pack_bf16x2(y[0], y[1]),
+                                     pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                     }
+                    fence_proxy_async_smem();
+                    named_bar_sync(2 + grp, 128);
+                    if (ii == 0) {
+                        tma_store_3d(&tmO, stage, 32 * grp, cur.i0, cur.bh);
+                        bulk_wait_read();
+                    }
+                    // nobody reuses the staging rows before the store has read them
+                    named_bar_sync(2 + grp, 128);
                 } else {
                     // this unit's share: O relative to the row max m, and
                     // (m, l); a split unit may hold no visible key of a row
@@ -616,6 +692,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             gbase += slots_of(cur.ntiles);
         }
+        if (!SPLIT && ii == 0) bulk_wait_all();
         tc_fence_before();
     } else if (warp == 8) {
         // ------------------------------------------------ score MMA issuer
@@ -782,12 +859,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const float qscale = p.scale_log2;
         const int ch = lane & 7;  // the lane's 16-byte chunk of every row it converts
         bool ok = true;
-        int issued = 0, landed = 0;  // q tiles loaded / observed in shared memory
+        int issued = 1, landed = 1;  // q tiles loaded / observed (item 0: by the groups)
         Item it;
-        for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
-            if (k >= 1)
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&sh->q_free, (k - 1) & 1, kDevTimeoutMma, abort, p.status));
+        for (int k = 1; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&sh->q_free, (k - 1) & 1, kDevTimeoutMma, abort, p.status));
             if (!ok) break;
             const uint32_t qb = OFF_Q + (k & 1) * 2 * SZ_Q;
             if (lane == 0) {
@@ -823,7 +899,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->q_ready);
+            if (lane == 0) mbar_arrive_cnt(&sh->q_ready, 8);
         }
         // drain: a q tile still in flight lands before the CTA exits
         if (landed < issued) drain_wait(&sh->q_full, (issued - 1) & 1, p.status);
@@ -947,13 +1023,14 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                        const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                        const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                     strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1030,13 +1107,17 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
         attr_set = true;
     }
     const int K = M + L;
-    CUtensorMap mQ, mK, mV, mR;
+    CUtensorMap mQ, mK, mV, mR, mO;
     {
         // q tile of an item: 128 rows of one (b, h); rows past L read as zeros
         cuuint64_t dims[3] = {(cuuint64_t)DH, (cuuint64_t)L, (cuuint64_t)B * H};
         cuuint64_t strides[2] = {(cuuint64_t)DH * 2, (cuuint64_t)L * DH * 2};
         cuuint32_t box[3] = {DH, BM, 1};
         if (!encode_bf16(&mQ, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        // output: one group's 32 columns of a tile per store (rows past L clipped)
+        cuuint32_t obox[3] = {DH / 2, BM, 1};
+        if (!encode_bf16(&mO, out, 3, dims, strides, obox, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)DH, (cuuint64_t)K, (cuuint64_t)B * H};
@@ -1079,11 +1160,11 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
     if (p.nsplit > 1)
-        attn_tc_bf16_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+        attn_tc_bf16_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
     else if (lower)
-        attn_tc_bf16_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+        attn_tc_bf16_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
     else
-        attn_tc_bf16_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, p);
+        attn_tc_bf16_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const long long threads = (long long)B * H * L * 8;
