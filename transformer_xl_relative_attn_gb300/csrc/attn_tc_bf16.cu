@@ -372,7 +372,15 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
-    if (tid == 0) {
+    // The TMA producer thread initialises the barriers and issues the first
+    // item's loads (its q tile, K/V stage 0, R boxes 0 and 1) before the block
+    // synchronises, so that their DRAM latency overlaps the prologue.
+    int pre_kv = 0, pre_r = 0;  // loads of item 0 issued here
+    if (warp == 9 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmR);
         for (int s = 0; s < KV_STAGES; ++s) {
             mbar_init(&sh->kv_full[s], 1);
             mbar_init(&sh->kv_empty[s], 1);
@@ -396,12 +404,22 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(&sh->drain, 2);  // one commit from each MMA issuer
         sh->abort = 0;
         fence_mbar_init();
-    }
-    if (warp == 9 && lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmR);
+        Item it0;
+        if (item_of<SPLIT, LOWER>(p, 0, it0)) {
+            mbar_expect_tx(&sh->q_full, 2 * SZ_Q);
+            tma_load_3d(smem + OFF_Q, &tmQ, &sh->q_full, 0, it0.i0, it0.bh);
+            tma_load_3d(smem + OFF_Q + SZ_Q, &tmQ, &sh->q_full, 0, it0.i0, it0.bh);
+            mbar_expect_tx(&sh->kv_full[0], 2 * SZ_BOX);
+            tma_load_3d(smem + OFF_KV, &tmK, &sh->kv_full[0], 0, it0.t0 * BN, it0.bh);
+            tma_load_3d(smem + OFF_KV + SZ_BOX, &tmV, &sh->kv_full[0], 0, it0.t0 * BN, it0.bh);
+            pre_kv = 1;
+            const int nrb = (it0.ntiles + 3) >> 1;
+            for (; pre_r < 2 && pre_r < nrb; ++pre_r) {
+                mbar_expect_tx(&sh->r_full[pre_r], SZ_BOX);
+                tma_load_2d(smem + OFF_R + pre_r * SZ_BOX, &tmR, &sh->r_full[pre_r], it0.h * DH,
+                            it0.rbase + SLOT * 2 * pre_r);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -436,12 +454,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, cur); ++k) {
             if (k == 0) {
                 // the first item's operands: the groups are idle until its first
-                // scores, so they convert it themselves (warp 11 takes the rest)
-                if (tid == 0) {
-                    mbar_expect_tx(&sh->q_full, 2 * SZ_Q);
-                    tma_load_3d(smem + OFF_Q, &tmQ, &sh->q_full, 0, cur.i0, cur.bh);
-                    tma_load_3d(smem + OFF_Q + SZ_Q, &tmQ, &sh->q_full, 0, cur.i0, cur.bh);
-                }
+                // scores, so they convert it themselves (warp 11 takes the rest);
+                // its q tile was loaded in the prologue
                 const uint4* brow = reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)cur.h * DH);
                 uint4 b4[8];
 #pragma unroll
@@ -907,13 +921,13 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     } else if (warp == 9) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int kvc = 0, rc = 0;  // loads issued into each ring
+            int kvc = pre_kv, rc = pre_r;  // loads issued into each ring (item 0's first in the prologue)
             bool ok = true;
             Item it;
             for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
                 const int nkv = (it.ntiles + 1) >> 1;  // K/V stages of this item
                 const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
-                int rb = 0;
+                int rb = k == 0 ? pre_r : 0;
                 for (int u = 0; ok && u < nkv; ++u) {
                     // R boxes that S(2u) and S(2u+1) read, then the K/V stage
                     for (; rb <= u + 1 && rb < nrb; ++rb, ++rc) {
@@ -928,6 +942,15 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                     it.rbase + SLOT * 2 * rb);
                     }
                     if (!ok) break;
+                    if (k == 0 && u < pre_kv) {
+                        // issued in the prologue; warm L2 for the next stages
+                        for (int w = 1; w <= PREFETCH && w < nkv; ++w) {
+                            tma_prefetch_l2_3d(&tmK, 0, (it.t0 + 2 * w) * BN, it.bh);
+                            tma_prefetch_l2_3d(&tmV, 0, (it.t0 + 2 * w) * BN, it.bh);
+                            tma_prefetch_l2_2d(&tmR, it.h * DH, it.rbase + SLOT * 2 * (w + 1));
+                        }
+                        continue;
+                    }
                     const int s = kvc % KV_STAGES;
                     if (kvc >= KV_STAGES && !mbar_wait(&sh->kv_empty[s], ((kvc / KV_STAGES) & 1) ^ 1,
                                                        kDevTimeoutProducer, abort, p.status)) {
