@@ -42,19 +42,24 @@
 //              keeps its own running max, sum and O accumulator, and the two
 //              partial results are merged per item
 //   warp 8     TMEM allocation; issues the score MMAs (AC and position slots)
-//   warp 9     lane 0 issues the TMA loads (128-row boxes: per-SM TMA
-//              throughput grows with the box size) and L2 prefetches
+//   warp 9     lane 0 initialises the barriers, issues the first item's
+//              loads before the block synchronises, then all TMA loads
+//              (128-row boxes: per-SM TMA throughput grows with the box
+//              size) and L2 prefetches
 //   warp 10    issues the P V MMAs
-//   warp 11    prepares the score MMAs' A operands of each item: loads the
-//              raw q tile by TMA into both slots of the item's Q buffer and
-//              rewrites them in place as (q+u)c and (q+v)c
+//   warp 11    prepares the score MMAs' A operands of each item after the
+//              first: loads the raw q tile by TMA into both slots of the
+//              item's Q buffer and rewrites them in place as (q+u)c and
+//              (q+v)c (the softmax groups do the first item's)
 // The score and P V chains are issued from different sub-partitions so that
 // neither waits behind the other or behind the softmax warps' instruction
 // streams.
 //
 // TMEM columns: O0 0-63, O1 64-127, AC0 128-191, AC1 192-255, position ring
 // 256-511.  Shared memory: (q+u)c,(q+v)c x2 (each first filled with the raw q
-// tile by TMA, then rewritten in place), P x2, K/V ring, R ring.  A group's P
+// tile by TMA, then rewritten in place), P x2, K/V ring, R ring.  At the end
+// of an item each group stages its 32 output columns in the upper half of its
+// P buffer and writes them with one TMA store.  A group's P
 // buffer is also the scratch of its per-row shift: after the group's previous
 // P V finished and before the new P is written, each warp moves its rows'
 // band windows through its 4 KB quarter of it, two band columns (c, c+32)
@@ -68,8 +73,11 @@
 // issue order, and a tcgen05.commit arrives only when every MMA issued before
 // it by the same thread has completed.
 //
-// Every wait is bounded (1 s); on expiry the CTA records a status, drains its
-// in-flight copies and MMAs, frees TMEM and exits.
+// Every mbarrier wait is bounded (1 s); on expiry the CTA records a status,
+// drains its in-flight copies and MMAs, frees TMEM and exits.  The named
+// barriers of the per-item merge have no time limit: one snapshot of the
+// abort flag taken between the first two decides, for all 256 softmax
+// threads at once, whether the merge and the next item run.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
