@@ -58,8 +58,9 @@
 // TMEM columns: O0 0-63, O1 64-127, AC0 128-191, AC1 192-255, position ring
 // 256-511.  Shared memory: (q+u)c,(q+v)c x2 (each first filled with the raw q
 // tile by TMA, then rewritten in place), P x2, K/V ring, R ring.  At the end
-// of an item each group stages its 32 output columns in the upper half of its
-// P buffer and writes them with one TMA store.  A group's P
+// of an item each softmax warp stages its 32 rows of its group's 32 output
+// columns in its own quarter of the P buffer and writes them with one TMA
+// store.  A group's P
 // buffer is also the scratch of its per-row shift: after the group's previous
 // P V finished and before the new P is written, each warp moves its rows'
 // band windows through its 4 KB quarter of it, two band columns (c, c+32)
@@ -75,9 +76,10 @@
 //
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records a status,
 // drains its in-flight copies and MMAs, frees TMEM and exits.  The named
-// barriers of the per-item merge have no time limit: one snapshot of the
-// abort flag taken between the first two decides, for all 256 softmax
-// threads at once, whether the merge and the next item run.
+// barriers of the per-item merge (bar 1, all 256 softmax threads) have no
+// time limit: one snapshot of the abort flag taken between the first two
+// decides, for all 256 threads at once, whether the merge and the next item
+// run.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -289,10 +291,6 @@ __device__ __forceinline__ void bulk_wait_read() {
 // the issuing thread's bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // one arrival on an mbarrier that counts as n
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n)
@@ -457,6 +455,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         bool ok = true;
 
         Item cur;
+        bool store_pending = false;  // lane 0: this warp's output box may still be being read
         int it_g = 0;      // tiles this group has processed (all items)
         int gbase = 0;     // global position-slot counter of the item's slot 0 (even)
         for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, cur); ++k) {
@@ -549,6 +548,12 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     for (int K = 0; K < 64; ++K)
                         hp[K] = pack_f16x2_sat(__uint_as_float(bw[K]), __uint_as_float(bw[K + 32]));
                     float win[32];
+                    if (store_pending) {
+                        // the previous item's output box has been read
+                        bulk_wait_read();
+                        store_pending = false;
+                    }
+                    __syncwarp();
                     st_shift_all<0>(31 - lane, t_st, *reinterpret_cast<uint32_t(*)[32]>(&hp[0]),
                                     *reinterpret_cast<uint32_t(*)[32]>(&hp[32]));
                     ld_shift_all<0>(t_ld, win);
@@ -662,13 +667,16 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
                     const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
                     const float a0 = f0 * inv, a1 = f1 * inv;
-                    // the group's 32 output columns of the tile go out as one TMA
-                    // store of a 128 x 32 box, staged in the upper half of the
-                    // group's P buffer (free: its last P V finished; the merge
-                    // exchange uses the lower 1 KB) in the 64-byte swizzle the
-                    // store expects: chunk c of row ii at chunk c ^ ((ii >> 1) & 3),
-                    // which also spreads each 8-thread phase over all banks
-                    const uint32_t stage = p_tile + 8192;
+                    // Each warp writes its 32 rows of the group's 32 output columns
+                    // with one TMA store of a 32 x 32 box, staged in the upper
+                    // 2 KB of the warp's own quarter of the P buffer (free: the
+                    // group's last P V finished; the merge exchange uses the
+                    // lower 1 KB of quarter 0) in the 64-byte swizzle the store
+                    // expects: chunk c of row r at chunk c ^ ((r >> 1) & 3), which
+                    // also spreads each 8-thread phase over all banks.  Only this
+                    // warp writes its quarter again (scratch, P rows), after its
+                    // lane 0 has seen the store read the box.
+                    const uint32_t stage = p_tile + wq * 4096 + 2048;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float y[8];
@@ -677,17 +685,15 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
                             y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
                         }
-                        st_shared_v4(stage + ii * 64 + ((c ^ ((ii >> 1) & 3)) << 4), pack_bf16x2(y[0], y[1]),
+                        st_shared_v4(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(y[0], y[1]),
                                      pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                     }
                     fence_proxy_async_smem();
-                    named_bar_sync(2 + grp, 128);
-                    if (ii == 0) {
-                        tma_store_3d(&tmO, stage, 32 * grp, cur.i0, cur.bh);
-                        bulk_wait_read();
+                    __syncwarp();
+                    if (lane == 0 && cur.i0 + 32 * wq < p.L) {
+                        tma_store_3d(&tmO, stage, 32 * grp, cur.i0 + 32 * wq, cur.bh);
+                        store_pending = true;
                     }
-                    // nobody reuses the staging rows before the store has read them
-                    named_bar_sync(2 + grp, 128);
                 } else {
                     // this unit's share: O relative to the row max m, and
                     // (m, l); a split unit may hold no visible key of a row
@@ -714,7 +720,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             gbase += slots_of(cur.ntiles);
         }
-        if (!SPLIT && ii == 0) bulk_wait_all();
+        if (!SPLIT && lane == 0) bulk_wait_all();
         tc_fence_before();
     } else if (warp == 8) {
         // ------------------------------------------------ score MMA issuer
@@ -1145,8 +1151,9 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
         cuuint64_t strides[2] = {(cuuint64_t)DH * 2, (cuuint64_t)L * DH * 2};
         cuuint32_t box[3] = {DH, BM, 1};
         if (!encode_bf16(&mQ, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
-        // output: one group's 32 columns of a tile per store (rows past L clipped)
-        cuuint32_t obox[3] = {DH / 2, BM, 1};
+        // output: one warp's 32 rows x one group's 32 columns per store (rows
+        // past L clipped)
+        cuuint32_t obox[3] = {DH / 2, 32, 1};
         if (!encode_bf16(&mO, out, 3, dims, strides, obox, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
