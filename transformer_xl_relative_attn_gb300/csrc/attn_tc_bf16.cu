@@ -37,7 +37,8 @@
 // item's scores can start while the current item is finished and stored.
 //
 // Roles (384 threads; warp w runs on SM sub-partition w % 4):
-//   warps 0-7  two softmax groups of 128 threads (one query row per thread);
+//   warps 0-7  two softmax groups of 128 threads (one query row per thread;
+//              group 0 = warps 0, 2, 5, 7, group 1 = warps 1, 3, 4, 6);
 //              group g takes the item's key tiles t = g (mod 2),
 //              keeps its own running max, sum and O accumulator, and the two
 //              partial results are merged per item
@@ -442,7 +443,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     if (warp < 8) {
         // ------------------------------------------------------ softmax groups
-        const int grp = warp >> 2;
+        // Groups {0, 2, 5, 7} and {1, 3, 4, 6}: each covers the four TMEM lane
+        // quarters (warp w reads lanes 32 (w % 4) ..) and holds two of the four
+        // lower warp ids the schedulers favour, so neither group lags by design
+        const int grp = ((warp >> 2) ^ warp) & 1;
         const int wq = warp & 3;            // TMEM lane quarter
         const int ii = tid & 127;           // query row within the item
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
