@@ -170,8 +170,12 @@ constexpr int kPS = 33;         // padded row of the P and dS tiles
 constexpr size_t kTiledSmem =
     (size_t)(3 * kQR * kDT + 2 * kQR * kPad + kSpan * kPad + 2 * kQR * kPS) * sizeof(float);
 
+// Three CTAs per SM (80 registers a thread, 28 bytes of spills; 3 x 66 KB of
+// shared memory): one CTA's 8 warps alone left the SM waiting on
+// shared-memory latency; base512 call 9.9 ms with one CTA, 8.6 with two,
+// 8.25 with three.
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 3)
 attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                       const T* __restrict__ r, const T* __restrict__ ub, const T* __restrict__ vb,
                       const T* __restrict__ dout, int B, int H, int L, int M, int dh, float scale,
