@@ -374,6 +374,12 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // Launched with programmatic stream serialisation: the next kernel of the
+    // stream may start its prologue while this grid's CTAs finish (none of
+    // its CTAs fits beside one of these, so it only takes SMs as they free
+    // up); every global access here comes after the wait for the previous
+    // kernel of the stream to complete.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 8) {
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
@@ -411,6 +417,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(&sh->drain, 2);  // one commit from each MMA issuer
         sh->abort = 0;
         fence_mbar_init();
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         Item it0;
         if (item_of<SPLIT, LOWER>(p, 0, it0)) {
             mbar_expect_tx(&sh->q_full, 2 * SZ_Q);
@@ -431,6 +438,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
     // Register split: the softmax warpgroups hold a whole tile's scores and
@@ -1087,6 +1095,24 @@ static int num_sms() {
     return n;
 }
 
+// Launch with programmatic stream serialisation (the kernel waits for the
+// previous kernel of the stream before its first global access).
+template <typename Kern>
+static void launch_pdl(Kern kern, int grid, cudaStream_t stream, const CUtensorMap& a, const CUtensorMap& b,
+                       const CUtensorMap& c, const CUtensorMap& d, const CUtensorMap& e, const TcParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc::NTHREADS);
+    cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kern, a, b, c, d, e, p);
+}
+
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 // Key splits per item when a workspace is available.  With fewer items than
 // SMs, whole items leave SMs idle; splitting each item's key tiles over
@@ -1202,11 +1228,11 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
     if (p.nsplit > 1)
-        attn_tc_bf16_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
+        launch_pdl(attn_tc_bf16_kernel<true, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     else if (lower)
-        attn_tc_bf16_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
+        launch_pdl(attn_tc_bf16_kernel<false, true>, grid, stream, mQ, mK, mV, mR, mO, p);
     else
-        attn_tc_bf16_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mR, mO, p);
+        launch_pdl(attn_tc_bf16_kernel<false, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nsplit == 1) return e;
     const long long threads = (long long)B * H * L * 8;
