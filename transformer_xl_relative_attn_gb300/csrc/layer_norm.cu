@@ -21,6 +21,10 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const __nv_bfloat16* x,
                                                          const __nv_bfloat16* __restrict__ beta,
                                                          long long rows, float eps, __nv_bfloat16* out) {
     constexpr int d = 256 * VPL;
+    // programmatic stream serialisation: let the next kernel launch, wait for
+    // the previous one before touching global memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
@@ -96,16 +100,24 @@ cudaError_t launch_layer_norm(const void* x, const void* y, const void* gamma, c
     const auto* bb = static_cast<const __nv_bfloat16*>(beta);
     auto* oo = static_cast<__nv_bfloat16*>(out);
     const unsigned g = (unsigned)blocks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     switch (d) {
-        case 256: layer_norm_kernel<1><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
-        case 512: layer_norm_kernel<2><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
-        case 768: layer_norm_kernel<3><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
-        case 1024: layer_norm_kernel<4><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
-        case 1536: layer_norm_kernel<6><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
-        case 2048: layer_norm_kernel<8><<<g, 256, 0, stream>>>(xx, yy, gg, bb, rows, eps, oo); break;
+        case 256: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<1>, xx, yy, gg, bb, rows, eps, oo);
+        case 512: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<2>, xx, yy, gg, bb, rows, eps, oo);
+        case 768: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<3>, xx, yy, gg, bb, rows, eps, oo);
+        case 1024: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<4>, xx, yy, gg, bb, rows, eps, oo);
+        case 1536: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<6>, xx, yy, gg, bb, rows, eps, oo);
+        case 2048: return cudaLaunchKernelEx(&cfg, layer_norm_kernel<8>, xx, yy, gg, bb, rows, eps, oo);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace txl

@@ -134,6 +134,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     const uint32_t s_base = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ksteps = p.K / BK;
+    // programmatic stream serialisation: the next kernel may launch now; this
+    // one waits for the previous kernel of the stream before any global access
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 1) {
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
@@ -161,6 +164,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
 
@@ -372,6 +376,25 @@ static bool pg_encode(CUtensorMap* map, const void* base, int rank, const cuuint
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialisation (the kernel waits for the
+// previous kernel of the stream before its first global access).
+template <typename Kern>
+static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_t stream, const CUtensorMap& a0,
+                                 const CUtensorMap& b0, const CUtensorMap& w0, const CUtensorMap& a1,
+                                 const CUtensorMap& b1, const CUtensorMap& w1, const PgParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(pg::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a0, b0, w0, a1, b1, w1, p);
+}
+
 static int pg_num_sms() {
     static int n = 0;
     if (!n) {
@@ -451,9 +474,8 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_tiles = (int)total;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    proj_gemm_kernel<256><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(maps[0][0], maps[0][1], maps[0][2], maps[1][0],
-                                                            maps[1][1], maps[1][2], p);
-    return cudaGetLastError();
+    return launch_pg_pdl(proj_gemm_kernel<256>, grid, C::SMEM_BYTES, stream, maps[0][0], maps[0][1], maps[0][2],
+                         maps[1][0], maps[1][1], maps[1][2], p);
 }
 
 // A plain Linear over rows of x (layout 0: [B, T, K]; 1: [B, K / 64, T, 64]):
@@ -516,9 +538,8 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
     p.pr[1].tiles = 0;
     p.n_tiles = (int)tiles;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    proj_gemm_kernel<BN_><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[0], maps[1],
-                                                            maps[2], p);
-    return cudaGetLastError();
+    return launch_pg_pdl(proj_gemm_kernel<BN_>, grid, C::SMEM_BYTES, stream, maps[0], maps[1], maps[2], maps[0],
+                         maps[1], maps[2], p);
 }
 
 // 256-column tiles unless that leaves fewer than two tiles per SM (then
