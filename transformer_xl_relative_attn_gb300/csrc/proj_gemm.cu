@@ -41,6 +41,19 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// the issuing thread's bulk stores have read / completed
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 namespace pg {
 constexpr int BM = 128;     // rows per tile (TMEM lanes)
 constexpr int BK = 64;      // K per stage: one 128-byte swizzle row of bf16
@@ -59,7 +72,10 @@ struct Cfg {
     static constexpr int STAGES = BN_ == 256 ? 3 : 6;
     static constexpr uint32_t SZ_B = BN_ * BK * 2;   // 32 or 16 KB
     static constexpr uint32_t OFF_B = OFF_A + STAGES * SZ_A;
-    static constexpr uint32_t OFF_BAR = OFF_B + STAGES * SZ_B;
+    // output staging: each of the 8 epilogue warps, 32 rows x BN / 2 columns
+    // in 64-column slices of 4 KB (128-byte rows, 128-byte swizzle)
+    static constexpr uint32_t OFF_STG = OFF_B + STAGES * SZ_B;
+    static constexpr uint32_t OFF_BAR = OFF_STG + 8 * 32 * (BN_ / 2) * 2;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 2 * BN_;  // two accumulators
     static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_, 0);
@@ -94,6 +110,13 @@ struct PgParams {
     int relu;
 };
 
+// Output tensor maps: problem g, output tensor o, viewed as (element of a
+// 64-column slice, row t, slice (head, or 64-column chunk of a row-major
+// output), batch row b); box 64 x 32 rows.
+struct PgOut {
+    CUtensorMap m[2][3];
+};
+
 struct PgShared {
     uint64_t full[pg::MAX_STAGES];
     uint64_t empty[pg::MAX_STAGES];
@@ -123,7 +146,7 @@ __global__ void __launch_bounds__(pg::NTHREADS, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                  const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmA1,
                  const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmW1,
-                 const PgParams p) {
+                 const __grid_constant__ PgOut outm, const PgParams p) {
     using namespace pg;
     using C = Cfg<BN_>;
     constexpr int BN = C::BN, STAGES = C::STAGES;
@@ -255,6 +278,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
         constexpr int CPW = BN / 64;         // 32-column chunks per epilogue warp
         const int row = wq * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t stg = s_base + C::OFF_STG + (uint32_t)(warp - 4) * 32 * (BN / 2) * 2;
+        bool store_pending = false;  // lane 0: this warp's last stores may still read the staging
         bool ok = true;
         int j = 0;
         for (int w = blockIdx.x; ok && w < p.n_tiles; w += gridDim.x, ++j) {
@@ -267,6 +292,11 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
             const int g = pg_tile<BN>(p, w, b, t0, n0);
             const PgProblem& pr = p.pr[g];
             const int t = t0 + row;
+            if (store_pending) {
+                bulk_wait_read();  // the previous tile's slices have been read
+                store_pending = false;
+            }
+            __syncwarp();
 #pragma unroll 1
             for (int cc = CPW * chalf; cc < CPW * chalf + CPW; ++cc) {
                 uint32_t v[32];
@@ -327,18 +357,32 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
 #pragma unroll
                     for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(f[x]);
                 }
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
+                // stage the 32 columns in the warp's 64-column slice (row = lane,
+                // 16-byte chunk c at c ^ (lane & 7)); a full slice goes out as one
+                // TMA store of 32 rows
+                const uint32_t slice = stg + (uint32_t)((cc - CPW * chalf) >> 1) * 4096;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint4 w4;
-                    w4.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                    w4.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                    w4.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                    w4.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                    d4[q] = w4;
+                    const int c16 = 4 * (cc & 1) + q;
+                    st_shared_v4(slice + lane * 128 + ((c16 ^ (lane & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+                if (cc & 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int ns = n - 32;  // the slice's first column
+                        const int os = ns / p.d, nds = ns - os * p.d;
+                        tma_store_4d(&outm.m[g][os], slice, 0, t0 + 32 * wq, p.plain ? nds / 64 : nds / p.dh, b);
+                        store_pending = true;
+                    }
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();  // the stores complete before the CTA exits
     }
 
     tc_fence_before();
@@ -383,7 +427,8 @@ static bool pg_encode(CUtensorMap* map, const void* base, int rank, const cuuint
 template <typename Kern>
 static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_t stream, const CUtensorMap& a0,
                                  const CUtensorMap& b0, const CUtensorMap& w0, const CUtensorMap& a1,
-                                 const CUtensorMap& b1, const CUtensorMap& w1, const PgParams& p) {
+                                 const CUtensorMap& b1, const CUtensorMap& w1, const PgOut& outm,
+                                 const PgParams& p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(pg::NTHREADS);
@@ -394,7 +439,19 @@ static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a0, b0, w0, a1, b1, w1, p);
+    return cudaLaunchKernelEx(&cfg, kern, a0, b0, w0, a1, b1, w1, outm, p);
+}
+
+// Output map of one bf16 tensor: heads [B, H, T, dh] (dh = 64) or row-major
+// [B, T, width], as (element of a 64-column slice, row, slice, batch).
+static bool pg_encode_out(CUtensorMap* map, void* base, int B, int T, int width, int heads_layout) {
+    const int slices = width / 64;
+    const cuuint64_t dims[4] = {64, (cuuint64_t)T, (cuuint64_t)slices, (cuuint64_t)B};
+    const cuuint64_t row = heads_layout ? 128 : (cuuint64_t)width * 2;
+    const cuuint64_t slice = heads_layout ? (cuuint64_t)T * 128 : 128;
+    const cuuint64_t strides[3] = {row, slice, (cuuint64_t)T * width * 2};
+    const cuuint32_t box[4] = {64, 32, 1, 1};
+    return pg_encode(map, base, 4, dims, strides, box);
 }
 
 static int pg_num_sms() {
@@ -423,6 +480,7 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     }
     if (n_gemm < 1 || n_gemm > 2) return cudaErrorInvalidValue;
     CUtensorMap maps[2][3];  // per problem: source a, source b, weights
+    PgOut outm;
     PgParams p;
     p.B = B;
     p.K = K;
@@ -472,12 +530,22 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         pr.tiles = (int)(tiles > 0x7FFFFFFFll ? 0 : tiles);
         total += tiles;
         for (int o = 0; o < 3; ++o) pr.out[o] = static_cast<__nv_bfloat16*>(q.out[o]);
+        // one map per output tensor of the problem (N / d of them); unused
+        // entries repeat the first
+        const int n_out = q.N / d;
+        for (int o = 0; o < 3; ++o) {
+            if (o < n_out) {
+                if (!pg_encode_out(&outm.m[g][o], q.out[o], B, q.T_out, d, !plain)) return cudaErrorInvalidValue;
+            } else {
+                outm.m[g][o] = outm.m[g][0];
+            }
+        }
     }
     if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_tiles = (int)total;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
     return launch_pg_pdl(proj_gemm_kernel<256>, grid, C::SMEM_BYTES, stream, maps[0][0], maps[0][1], maps[0][2],
-                         maps[1][0], maps[1][1], maps[1][2], p);
+                         maps[1][0], maps[1][1], maps[1][2], outm, p);
 }
 
 // A plain Linear over rows of x (layout 0: [B, T, K]; 1: [B, K / 64, T, 64]):
@@ -536,12 +604,15 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
     pr.tiles = (int)tiles;
     pr.out[0] = static_cast<__nv_bfloat16*>(out);
     pr.out[1] = pr.out[2] = nullptr;
+    PgOut outm;
+    if (!pg_encode_out(&outm.m[0][0], out, B, T, N, 0)) return cudaErrorInvalidValue;
+    for (int i = 0; i < 6; ++i) (&outm.m[0][0])[i] = outm.m[0][0];
     p.pr[1] = pr;
     p.pr[1].tiles = 0;
     p.n_tiles = (int)tiles;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
     return launch_pg_pdl(proj_gemm_kernel<BN_>, grid, C::SMEM_BYTES, stream, maps[0], maps[1], maps[2], maps[0],
-                         maps[1], maps[2], p);
+                         maps[1], maps[2], outm, p);
 }
 
 // 256-column tiles unless that leaves fewer than two tiles per SM (then
