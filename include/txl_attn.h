@@ -44,7 +44,7 @@ enum txl_dtype {
 enum txl_status {
     TXL_OK = 0,
     TXL_ERR_INVALID_ARG = -1,    /* null pointer, B/H/L <= 0, M < 0, bad dtype */
-    TXL_ERR_UNSUPPORTED = -2,    /* a size this build has no kernel for (see each call) */
+    TXL_ERR_UNSUPPORTED = -2,    /* a size the library has no kernel for (see each call) */
     TXL_ERR_MISALIGNED = -3,     /* a base pointer is not 16-byte aligned */
     TXL_ERR_ALIAS = -4,          /* an output overlaps an input it must not overlap */
     TXL_ERR_LAUNCH = -5,         /* the CUDA launch itself failed */
@@ -199,7 +199,7 @@ int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout
                     void* v, void* stream);
 
 /*
- * Ring-buffer memory (the survey's alternative to the Tail_M copy): a memory
+ * Ring-buffer memory (an alternative to the Tail_M copy): a memory
  * of M rows whose logical row t is stored at row (start + t) mod M.
  *
  * txl_qkv_proj_ring: txl_qkv_proj_ex reading mem as a ring starting at
