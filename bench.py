@@ -299,7 +299,8 @@ def run_ours(args, wl: W.Workload):
     sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]  # last replay of the timed region
-    roll_ms = time_rolls(calls, mems, stream)
+    roll_avg_ms = time_rolls(calls, mems, stream)
+    roll_long = time_longmem_rolls(dev, stream, peaks)
     proj = time_projections(wl, dev, stream, peaks)
     bwd = time_backward(wl, calls, rks, u, vb, dev) if wl.dh <= 256 else None
     txl.check_status()
@@ -311,7 +312,9 @@ def run_ours(args, wl: W.Workload):
     ms_per_step = elapsed_max / args.steps
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = flops_call / (attn_avg_ms * 1e-3) / 1e12
-    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # the timed region is tens of milliseconds at the maximum SM clock (the
+    # clock record below shows it): burst conditions, so the burst peak
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     result = {
         "metric": METRIC,
@@ -347,7 +350,7 @@ def run_ours(args, wl: W.Workload):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4),
             "traffic": measured_traffic(wl.name),
-            "peak_source": f"bf16_tflops_sustained ({peak_src})",
+            "peak_source": f"bf16_tflops, burst ({peak_src}): the timed region is tens of ms at max clock",
             "flops_per_launch": flops_call,
             "avg_launch_ms": round(attn_avg_ms, 5),
             "launches_averaged": len(attn_ms),
@@ -360,17 +363,19 @@ def run_ours(args, wl: W.Workload):
         "backward": bwd,
         "roofline_mem_update": {
             "kernel": "tail_copy_kernel" if wl.L >= wl.M else "tail_chain_kernel",
+            "workload": wl.name,
             "bound": "hbm",
-            "achieved": round(wl.mem_update_bytes() / (sum(roll_ms) / len(roll_ms) * 1e-3) / 1e9, 1),
+            "achieved": round(wl.mem_update_bytes() / (roll_avg_ms * 1e-3) / 1e9, 1),
             "peak": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
             "unit": "GB/s",
-            "frac": round(wl.mem_update_bytes() / (sum(roll_ms) / len(roll_ms) * 1e-3) / 1e9
+            "frac": round(wl.mem_update_bytes() / (roll_avg_ms * 1e-3) / 1e9
                           / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), 4),
             "bytes_per_launch": wl.mem_update_bytes(),
-            "avg_launch_ms": round(sum(roll_ms) / len(roll_ms), 5),
-            "measured": "each call's roll once, in step order, alone on one stream, as a CUDA graph "
-                        "with CUDA events between the rolls",
+            "avg_launch_ms": round(roll_avg_ms, 5),
+            "measured": f"the step's {n_calls} rolls in step order, back to back in one CUDA graph, "
+                        "events around the graph only (total / rolls, median of 5 replays)",
         },
+        "roofline_mem_update_longmem3200": roll_long,
         "gpu_launches": (3 if scratch is not None else 2) * n_calls * args.steps,
         "clocks": sampler.summary(),
     }
@@ -477,25 +482,79 @@ def time_projections(wl, dev, stream, peaks):
     }
 
 
-def time_rolls(calls, mems, stream):
-    """Durations (ms) of every call's Tail_M roll, each alone on `stream`, in
-    step order (so consecutive rolls touch different layers' memories).  The
-    rolls and their events are captured in a CUDA graph first, so the events
-    time the device, not the host's launch path."""
+def time_rolls(calls, mems, stream, reps=5):
+    """Average duration (ms) of one Tail_M roll: every call's roll of the step,
+    in step order (consecutive rolls touch different layers' memories and
+    different hidden states), back to back on `stream` as one CUDA graph with
+    CUDA events only around the whole sequence; the graph is replayed
+    ``reps`` times and the median replay is divided by the number of rolls."""
     import transformer_xl_relative_attn_gb300 as txl
 
-    evs = [(torch.cuda.Event(enable_timing=True, external=True),
-            torch.cuda.Event(enable_timing=True, external=True)) for _ in calls]
+    t0 = torch.cuda.Event(enable_timing=True, external=True)
+    t1 = torch.cuda.Event(enable_timing=True, external=True)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for c, (a, b) in zip(calls, evs):
-            a.record()
+        t0.record()
+        for c in calls:
             txl.mem_update(mems[c["n"]], c["h"])
-            b.record()
-    g.replay()
-    torch.cuda.synchronize()
+        t1.record()
+    times = []
+    for _ in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1) / len(calls))
     txl.check_status()
-    return [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(times)
+
+
+def time_longmem_rolls(dev, stream, peaks, n_sets=6, reps=5):
+    """The Tail_M roll of the long-memory configuration (B=8, L=128, M=3200,
+    d=1024, bf16: 52.4 MB read + 52.4 MB written per roll), measured where its
+    HBM target is quoted.  ``n_sets`` distinct (memory, hidden state) pairs
+    (6 x 54.5 MB, well beyond the 126 MB L2) are rolled in rotation, 4 passes
+    over the sets in one CUDA graph, so every roll reads memory that the L2
+    no longer holds and its writes must reach DRAM; events bracket the whole
+    graph only."""
+    import transformer_xl_relative_attn_gb300 as txl
+
+    wl = W.WORKLOADS["longmem3200_bf16"]
+    B, L, M, d = wl.B, wl.L, wl.M, wl.d
+    g = torch.Generator(device="cpu").manual_seed(29)
+    mems = [torch.randn(B, M, d, generator=g).to(device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
+    hids = [torch.randn(B, L, d, generator=g).to(device=dev, dtype=torch.bfloat16) for _ in range(n_sets)]
+    passes = 4
+    t0 = torch.cuda.Event(enable_timing=True, external=True)
+    t1 = torch.cuda.Event(enable_timing=True, external=True)
+    with torch.cuda.stream(stream):
+        for m, h in zip(mems, hids):
+            txl.mem_update(m, h, stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        t0.record()
+        for _ in range(passes):
+            for m, h in zip(mems, hids):
+                txl.mem_update(m, h)
+        t1.record()
+    times = []
+    for _ in range(reps):
+        graph.replay()
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1) / (passes * n_sets))
+    txl.check_status()
+    ms = statistics.median(times)
+    nbytes = wl.mem_update_bytes()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del mems, hids
+    return {
+        "kernel": "tail_chain_kernel", "workload": wl.name, "bound": "hbm",
+        "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+        "peak_source": "hbm_gbs (measured copy bandwidth)",
+        "bytes_per_launch": nbytes, "avg_launch_ms": round(ms, 5),
+        "measured": f"{passes} passes over {n_sets} distinct memories (6 x 54.5 MB > L2) in one CUDA "
+                    f"graph, events around the graph only; median of {reps} replays",
+    }
 
 
 def measure_e2e(args, wl, calls, stream, side, mems, rks, u, vb, scratch, flops_step, ws):

@@ -133,18 +133,22 @@ int txl_attn_fwd_ws(const void* q, const void* k, const void* v, const void* r_k
  * txl_attn_fwd_ws without a caller workspace and without any allocation: the
  * split-key path (see txl_attn_fwd_ws) takes its partial results from one
  * file-scope static device buffer of TXL_NOALLOC_SCRATCH_BYTES (16 MiB) per
- * device, whose address the library looks up once per device on the first
- * call.  The pages have no counterpart of this entry point: it exists for
- * callers that cannot hand out a workspace (for example a fixed launch
- * sequence).
+ * device.  The library looks its device address up (cudaGetSymbolAddress)
+ * on every call that is not inside a stream capture and keeps the last
+ * address per device for calls made during a capture.  The pages have no
+ * counterpart of this entry point: it exists for callers that cannot hand
+ * out a workspace (for example a fixed launch sequence).
  *
  *   - Same arguments, results and errors as txl_attn_fwd_ws; a call whose
  *     txl_attn_workspace_bytes(...) exceeds TXL_NOALLOC_SCRATCH_BYTES returns
  *     TXL_ERR_SCRATCH_LIMIT and launches nothing.
  *   - Nothing in the scratch needs to start at zero: every value read is
  *     written earlier in the same call.
- *   - The first call on each device must not be inside a stream capture (it
- *     looks the buffer up with cudaGetSymbolAddress).
+ *   - The first call on each device that needs scratch must not be inside a
+ *     stream capture (there is no cached address yet: TXL_ERR_CUDA).  After
+ *     cudaDeviceReset (or any teardown of the device's context) the module is
+ *     loaded again at a new address: make one call outside a capture before
+ *     capturing again, or a capture would launch on the stale address.
  *   - Calls that overlap in time on one device (different streams, or
  *     threads) share the buffer and race: order them, e.g. on one stream.
  *   - Calls that need no scratch (txl_attn_workspace_bytes(...) == 0) do not
@@ -319,10 +323,12 @@ int txl_version(void);
 
 /*
  * Test hook for the failure-detection path.  kind = 1 makes the NEXT bf16
- * attention launch withhold one internal completion signal, so its waiting
- * warps hit their time limit, record TXL_ERR_DEVICE_TIMEOUT and exit cleanly
- * (the GPU context stays usable).  kind = 0 clears it.  The hook disarms
- * itself after one launch.  Not for production use.
+ * attention launch made by the calling host thread withhold one internal
+ * completion signal, so its waiting warps hit their time limit, record
+ * TXL_ERR_DEVICE_TIMEOUT and exit cleanly (the GPU context stays usable).
+ * kind = 0 clears it.  The hook is per host thread (launches from other
+ * threads never consume it) and disarms itself after one launch.  Not for
+ * production use.
  */
 int txl_debug_inject(int kind);
 

@@ -85,6 +85,27 @@ def test_binding_refuses_cpu_tensors():
                      torch.zeros(1, 64, dtype=torch.bfloat16), torch.zeros(1, 64, dtype=torch.bfloat16))
 
 
+def test_binding_refuses_tensors_on_another_device():
+    """Every tensor of a call must be on the first tensor's device: the C call
+    runs with that device current, and a pointer from another device would be
+    dereferenced on the wrong GPU.  (On this CPU-only host the check is
+    exercised directly: a tensor whose device differs from the call's.)"""
+    import torch
+    other = torch.device("cuda", 1)
+    with pytest.raises(ValueError, match="cuda:1"):
+        _lib._need(torch.zeros(2, 64), "k", (2, 64), torch.float32, other)
+    with pytest.raises(ValueError, match="on cpu"):
+        _lib._need(torch.zeros(2, 64), "k", (2, 64), torch.float32, other)
+
+
+def test_status_table_covers_every_header_code():
+    """Each TXL_ERR_* code the header defines has a name in the binding."""
+    import re
+    with open(_lib.HEADER, encoding="utf-8") as fh:
+        codes = {int(v) for v in re.findall(r"\bTXL_(?:OK|ERR_\w+)\s*=\s*(-?\d+)", fh.read())}
+    assert codes and codes <= set(_lib.STATUS)
+
+
 # --------------------------------------------------------------------------
 # the entry points added beyond the attention operator: bad arguments are
 # rejected on the host, before any CUDA call

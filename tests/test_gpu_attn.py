@@ -99,6 +99,47 @@ def test_bf16_full_size_sampled(name):
     check_bf16(ci, pairs=pairs)
 
 
+@pytest.mark.parametrize("name,seg,layer", [("base512_bf16", 1, 5), ("base512_bf16", 2, 11),
+                                            ("large384_bf16", 1, 17)])
+def test_bf16_full_size_later_segment_and_layer(name, seg, layer):
+    """A later call of the full-size chain, in the benchmark's launch
+    configuration: segment ``seg`` (memories rolled by Tail_M through every
+    earlier segment) and layer ``layer`` (its input the head-merged output of
+    the layer below), on exactly the inputs that call saw.  The oracle checks
+    a seeded sample of (b, h) pairs."""
+    wl = W.WORKLOADS[name]
+    dev = torch.device("cuda")
+    dt = wl.torch_dtype
+    params = W.make_params(wl)
+    lws = [W.LayerWeights(*(getattr(lw, f).to(dev) for f in ("W_q", "W_k", "W_v", "W_r")))
+           for lw in params.layers]
+    mems = [m.to(device=dev, dtype=dt) for m in W.initial_memories(wl)]
+    rks = [W.project_r(lw, wl.M, wl.L, wl.H, device=dev).to(dt) for lw in lws]
+    u, vb = params.u.to(dev, dt), params.v.to(dev, dt)
+    n_pairs = wl.B * wl.H
+    pairs = sorted({0, n_pairs - 1,
+                    *np.random.default_rng(seg * 100 + layer).choice(n_pairs, size=4, replace=False).tolist()})
+    for s in range(seg + 1):
+        h = W.segment_input(wl, s).to(device=dev, dtype=dt)
+        for n in range(wl.layers):
+            q, k, v = (x.to(dt) for x in W.project_qkv(lws[n], mems[n], h, wl.H))
+            out = txl.attn_fwd(q, k, v, rks[n], u, vb, wl.scale)
+            if (s, n) == (seg, layer):
+                torch.cuda.synchronize()
+                assert txl.sync_status() == 0
+                got = out.float().cpu().double().numpy()
+                ref = oracle.attn(q.cpu(), k.cpu(), v.cpu(), rks[n].cpu(), u.cpu(), vb.cpu(), wl.scale,
+                                  pairs=pairs)
+                g = np.stack([got[p // wl.H, p % wl.H] for p in pairs])
+                r = np.stack([ref[p // wl.H, p % wl.H] for p in pairs])
+                assert np.isfinite(g).all()
+                assert np.abs(g - r).max() <= bf16_tol(r)
+                return
+            txl.mem_update(mems[n], h)
+            h = W.merge_heads(out)
+    raise AssertionError("the requested call was not reached")
+
+
 def test_bf16_one_hot_probe_shows_mask_and_uniform_rows():
     """k = 0, u = 0, r_k = 0 and V_j = e_j: row i of the output is the
     probability row, 1/(M+i+1) on keys 0..M+i and exactly 0 past them."""

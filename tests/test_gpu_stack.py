@@ -132,3 +132,41 @@ def test_heads_layout_projection_matches_rows_layout():
     torch.cuda.synchronize()
     for a, b, c in ((q0, q1, q2), (k0, k1, k2), (v0, v1, v2)):
         assert torch.equal(a, b) and torch.equal(a, c)
+
+
+@pytest.mark.parametrize("clamp_len", [100, 0])
+def test_stack_with_clamp_len_matches_oracle(clamp_len):
+    """clamp_len ("Transformer-XL模型 核心源码阅读笔记", section "Build the model",
+    MemTransformerLM._forward: pos_seq.clamp_(max=clamp_len) before the
+    positional embedding): every distance beyond clamp_len takes the position
+    embedding of clamp_len.  It changes only the position table the layer's
+    r_k is projected from, so the stack runs unchanged on a clamped r_k: its
+    rows for distances >= clamp_len come out bit-identical, and every call
+    matches the oracle on the inputs it saw."""
+    stack, w_qkv, r_k_plain, u, vb = make_stack()
+    p = W.make_params(WL)
+    H, d, L, M = WL.H, WL.d, WL.L, WL.M
+    emb = W.sinusoid(W.position_sequence(M, L, clamp_len), d).cuda().to(BF)
+    r_k = [txl.r_proj(emb, lw.W_r.t().contiguous().cuda().to(BF), H) for lw in p.layers]
+    stack.r_k = r_k
+    torch.cuda.synchronize()
+    far = M + L - 1 - clamp_len          # rows 0..far hold distances >= clamp_len
+    for r in r_k:
+        assert all(torch.equal(r[i], r[far]) for i in range(far + 1))
+        if far + 1 < M + L:
+            assert not torch.equal(r[far], r[far + 1])
+    trace = []
+    for s in range(2):
+        stack.run_segment(W.segment_input(WL, s).cuda().to(BF), trace=trace)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    differs = False
+    for c in trace:
+        n = c["n"]
+        cpu = [t.cpu() for t in (c["q"], c["k"], c["v"], r_k[n], u[n], vb[n])]
+        ref = oracle.attn(*cpu, WL.scale)
+        got = c["out"].float().cpu().double().numpy()
+        assert np.abs(got - ref).max() <= tol(ref), n
+        plain = oracle.attn(*cpu[:3], r_k_plain[n].cpu(), *cpu[4:], WL.scale)
+        differs |= np.abs(plain - ref).max() > tol(ref)
+    assert differs  # the clamp is visible in the result

@@ -262,6 +262,36 @@ def test_closed_form_mean_of_visible_values():
         np.testing.assert_allclose(out[:, :, i], v[:, :, :M + i + 1].mean(axis=2), atol=1e-14)
 
 
+@pytest.mark.parametrize("M,L,clamp_len", [(5, 6, 0), (12, 4, 3), (0, 9, 2)])
+def test_clamped_positions_reduce_to_textbook_attention_beyond_the_clamp(M, L, clamp_len):
+    """clamp_len ("Transformer-XL模型 核心源码阅读笔记", MemTransformerLM._forward:
+    pos_seq.clamp_(max=clamp_len)) makes every distance >= clamp_len share one
+    position row R_c.  With q = 0 and v_bias = e_0 the position term is the
+    first column of that row, so on the keys at distance >= clamp_len the
+    score is the constant a = R_c[0] (plus the content term c = u.k_j); the
+    oracle fed the clamped table must then equal textbook attention (SDPA)
+    with the explicit additive bias scale * R[min(dist, clamp_len)][0]."""
+    H, dh = 2, 4
+    K = M + L
+    q = np.zeros((1, H, L, dh)); k = rnd(1, H, K, dh); v = rnd(1, H, K, dh)
+    u = rnd(H, dh, std=0.5); vb = np.zeros((H, dh)); vb[:, 0] = 1.0
+    table = rnd(K, H, dh)                           # row t <-> position t
+    pos = W.position_sequence(M, L, clamp_len).numpy().astype(int)
+    r = table[pos]                                  # r_k row r <-> pos_seq[r]
+    scale = 0.6
+    out = oracle.attn(q, k, v, r, u, vb, scale)
+    dist = (M + np.arange(L))[:, None] - np.arange(K)[None, :]
+    allow = dist >= 0
+    # explicit bias per head: scale * table[min(dist, clamp_len), h, 0]
+    for h in range(H):
+        bh = np.where(allow, scale * table[np.minimum(np.maximum(dist, 0), clamp_len), h, 0], -np.inf)
+        qq = np.broadcast_to(u[h][None, None, :], (1, 1, L, dh))
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            t(qq), t(k[:, h:h + 1]), t(v[:, h:h + 1]), attn_mask=t(bh), scale=scale).numpy()
+        np.testing.assert_allclose(out[:, h:h + 1], ref, rtol=1e-12, atol=1e-12)
+
+
 def test_pairs_subset_matches_full():
     M, L, B, H, dh = 4, 3, 3, 2, 5
     K = M + L

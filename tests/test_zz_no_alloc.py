@@ -45,12 +45,21 @@ def test_noalloc_without_split_matches_plain_entry():
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
-    """Few heads with a very long memory split into many units; the partial
-    results outgrow the static scratch and the call is refused, not run."""
-    B, H, L, M = 1, 40, 128, 32000
-    need = txl.attn_workspace_bytes(B, H, L, M, 64)
-    if need <= SCRATCH_BYTES:
-        pytest.skip("this GPU's split for these sizes fits the static scratch")
+    """Few items with a very long memory split into many units; once their
+    partial results outgrow the static scratch the call is refused, not run.
+    The split (and so the scratch a call needs) depends on this GPU's SM
+    count, so the shape is searched for here, smallest first; finding none
+    is a failure, not a skip."""
+    found = None
+    for M in (8000, 16000, 32000, 64000):
+        for H in (8, 16, 24, 32, 40, 48, 64, 100, 140):
+            if txl.attn_workspace_bytes(1, H, 128, M, 64) > SCRATCH_BYTES:
+                found = (1, H, 128, M)
+                break
+        if found:
+            break
+    assert found, "no searched shape needs more than the static scratch"
+    B, H, L, M = found
     q = torch.zeros(B, H, L, 64, device="cuda", dtype=torch.bfloat16)
     k = torch.zeros(B, H, M + L, 64, device="cuda", dtype=torch.bfloat16)
     r = torch.zeros(M + L, H, 64, device="cuda", dtype=torch.bfloat16)

@@ -27,6 +27,7 @@ STATUS = {
     -6: "TXL_ERR_DEVICE_TIMEOUT",
     -7: "TXL_ERR_WORKSPACE",
     -8: "TXL_ERR_CUDA",
+    -9: "TXL_ERR_SCRATCH_LIMIT",
 }
 
 _lib = None
@@ -121,15 +122,27 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32 only")
 
 
+def _invoke(device, name: str, *args):
+    """Calls C entry point ``name`` with ``device`` current, so that the
+    library's launches, its status word and its static scratch are those of
+    the device the call's tensors live on."""
+    with torch.cuda.device(device):
+        return getattr(load(), name)(*args)
+
+
 def _stream(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _need(t: torch.Tensor, name: str, shape: tuple, dtype) -> None:
+def _need(t: torch.Tensor, name: str, shape: tuple, dtype, device=None) -> None:
+    """Type, device, dtype, shape and contiguity of one argument.  ``device``:
+    the device every tensor of the call must share (the kernels run there)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
     if t.dtype != dtype:
@@ -150,14 +163,15 @@ def _attn_args(q, k, v, r_k, u, vb, scale, out):
         raise ValueError("k must be [B, H, M+L, d_h] with M >= 0")
     dt = q.dtype
     _need(q, "q", (B, H, L, dh), dt)
-    _need(k, "k", (B, H, K, dh), dt)
-    _need(v, "v", (B, H, K, dh), dt)
-    _need(r_k, "r_k", (K, H, dh), dt)
-    _need(u, "u", (H, dh), dt)
-    _need(vb, "v_bias", (H, dh), dt)
+    dv = q.device
+    _need(k, "k", (B, H, K, dh), dt, dv)
+    _need(v, "v", (B, H, K, dh), dt, dv)
+    _need(r_k, "r_k", (K, H, dh), dt, dv)
+    _need(u, "u", (H, dh), dt, dv)
+    _need(vb, "v_bias", (H, dh), dt, dv)
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", (B, H, L, dh), dt)
+    _need(out, "out", (B, H, L, dh), dt, dv)
     if scale is None:
         scale = dh ** -0.5
     return B, H, L, M, dh, float(scale), out
@@ -172,14 +186,14 @@ def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None, same_length
     configured memory length mem_len (default M).  Returns out [B,H,L,dh]."""
     B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
     if same_length:
-        rc = load().txl_attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+        rc = _invoke(q.device, "txl_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
                                     u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, 1,
                                     M if mem_len is None else int(mem_len), out.data_ptr(),
                                     _dtype_code(q), _stream(stream, q.device))
         if rc != 0:
             raise TxlError(rc, "txl_attn_fwd_ex")
         return out
-    rc = load().txl_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+    rc = _invoke(q.device, "txl_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
                              u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(),
                              _dtype_code(q), _stream(stream, q.device))
     if rc != 0:
@@ -192,12 +206,12 @@ def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=N
     v, r_k, u and vb (stop-gradient memory: the memory rows' dk, dv are
     included and left to the caller).  Returns a dict dq, dk, dv, dr, du, dvb."""
     B, H, L, M, dh, scale, _ = _attn_args(q, k, v, r_k, u, vb, scale, dout)
-    _need(dout, "dout", (B, H, L, dh), q.dtype)
+    _need(dout, "dout", (B, H, L, dh), q.dtype, q.device)
     f32 = dict(dtype=torch.float32, device=q.device)
     g = {"dq": torch.empty((B, H, L, dh), **f32), "dk": torch.empty((B, H, M + L, dh), **f32),
          "dv": torch.empty((B, H, M + L, dh), **f32), "dr": torch.empty((M + L, H, dh), **f32),
          "du": torch.empty((H, dh), **f32), "dvb": torch.empty((H, dh), **f32)}
-    rc = load().txl_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(),
+    rc = _invoke(q.device, "txl_attn_bwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(),
                              vb.data_ptr(), dout.data_ptr(), B, H, L, M, dh, scale, int(bool(same_length)),
                              M if mem_len is None else int(mem_len),
                              *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")],
@@ -207,18 +221,23 @@ def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=N
     return g
 
 
-def attn_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16) -> int:
+def attn_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16, device=None) -> int:
+    """txl_attn_workspace_bytes for a call on ``device`` (default: the current
+    one): the split depends on that device's SM count."""
     code = TXL_BF16 if dtype == torch.bfloat16 else TXL_F32
-    return int(load().txl_attn_workspace_bytes(B, H, L, M, dh, code))
+    dev = device if device is not None else torch.cuda.current_device()
+    return int(_invoke(dev, "txl_attn_workspace_bytes", B, H, L, M, dh, code))
 
 
 def attn_fwd_ws(q, k, v, r_k, u, vb, workspace, scale=None, out=None, stream=None):
     """txl_attn_fwd_ws: like attn_fwd with caller-owned scratch (a uint8 CUDA
     tensor of at least attn_workspace_bytes(...) bytes, or None when 0)."""
     B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    if workspace is not None and (not isinstance(workspace, torch.Tensor) or workspace.device != q.device):
+        raise ValueError(f"workspace must be a tensor on {q.device}")
     wp = workspace.data_ptr() if workspace is not None else 0
     wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load().txl_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+    rc = _invoke(q.device, "txl_attn_fwd_ws", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
                                 u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(),
                                 _dtype_code(q), wp, wn, _stream(stream, q.device))
     if rc != 0:
@@ -231,7 +250,7 @@ def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
     device scratch instead of a caller workspace (calls on one device must not
     overlap in time; the first call on a device must not be captured)."""
     B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
-    rc = load().txl_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+    rc = _invoke(q.device, "txl_attn_fwd_noalloc", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
                                      u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale,
                                      out.data_ptr(), _dtype_code(q), _stream(stream, q.device))
     if rc != 0:
@@ -268,18 +287,18 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0)
         raise ValueError("mem must be [B, M, d] or [B, H, M, d_h]")
     _need(h, "h", (B, L, d) if h_layout == 0 else (B, H, L, dh), torch.bfloat16)
     if M > 0:
-        _need(mem, "mem", mem_shape, torch.bfloat16)
-    _need(w_qkv, "w_qkv", (3 * d, d), torch.bfloat16)
+        _need(mem, "mem", mem_shape, torch.bfloat16, h.device)
+    _need(w_qkv, "w_qkv", (3 * d, d), torch.bfloat16, h.device)
     if q is None:
         q = torch.empty((B, H, L, dh), dtype=torch.bfloat16, device=h.device)
     if k is None:
         k = torch.empty((B, H, M + L, dh), dtype=torch.bfloat16, device=h.device)
     if v is None:
         v = torch.empty((B, H, M + L, dh), dtype=torch.bfloat16, device=h.device)
-    _need(q, "q", (B, H, L, dh), torch.bfloat16)
-    _need(k, "k", (B, H, M + L, dh), torch.bfloat16)
-    _need(v, "v", (B, H, M + L, dh), torch.bfloat16)
-    rc = load().txl_qkv_proj_ring(h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
+    _need(q, "q", (B, H, L, dh), torch.bfloat16, h.device)
+    _need(k, "k", (B, H, M + L, dh), torch.bfloat16, h.device)
+    _need(v, "v", (B, H, M + L, dh), torch.bfloat16, h.device)
+    rc = _invoke(h.device, "txl_qkv_proj_ring", h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
                                   int(mem_start), w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(),
                                   k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
     if rc != 0:
@@ -303,15 +322,15 @@ def linear(x, w, bias=None, resid=None, relu=False, out=None, stream=None):
         raise ValueError("x must be [B, T, K] or [B, H, T, 64]")
     N = w.shape[0]
     _need(x, "x", tuple(x.shape), torch.bfloat16)
-    _need(w, "w", (N, K), torch.bfloat16)
+    _need(w, "w", (N, K), torch.bfloat16, x.device)
     if bias is not None:
-        _need(bias, "bias", (N,), torch.bfloat16)
+        _need(bias, "bias", (N,), torch.bfloat16, x.device)
     if resid is not None:
-        _need(resid, "resid", (B, T, N), torch.bfloat16)
+        _need(resid, "resid", (B, T, N), torch.bfloat16, x.device)
     if out is None:
         out = torch.empty((B, T, N), dtype=torch.bfloat16, device=x.device)
-    _need(out, "out", (B, T, N), torch.bfloat16)
-    rc = load().txl_linear(x.data_ptr(), layout, B, T, K, w.data_ptr(), N,
+    _need(out, "out", (B, T, N), torch.bfloat16, x.device)
+    rc = _invoke(x.device, "txl_linear", x.data_ptr(), layout, B, T, K, w.data_ptr(), N,
                            bias.data_ptr() if bias is not None else 0,
                            resid.data_ptr() if resid is not None else 0, int(bool(relu)),
                            out.data_ptr(), _stream(stream, x.device))
@@ -327,13 +346,13 @@ def layer_norm(x, gamma, beta, y=None, eps=1e-5, out=None, stream=None):
     rows = x.numel() // d
     _need(x, "x", tuple(x.shape), torch.bfloat16)
     if y is not None:
-        _need(y, "y", tuple(x.shape), torch.bfloat16)
-    _need(gamma, "gamma", (d,), torch.bfloat16)
-    _need(beta, "beta", (d,), torch.bfloat16)
+        _need(y, "y", tuple(x.shape), torch.bfloat16, x.device)
+    _need(gamma, "gamma", (d,), torch.bfloat16, x.device)
+    _need(beta, "beta", (d,), torch.bfloat16, x.device)
     if out is None:
         out = torch.empty_like(x)
-    _need(out, "out", tuple(x.shape), torch.bfloat16)
-    rc = load().txl_layer_norm(x.data_ptr(), y.data_ptr() if y is not None else 0, gamma.data_ptr(),
+    _need(out, "out", tuple(x.shape), torch.bfloat16, x.device)
+    rc = _invoke(x.device, "txl_layer_norm", x.data_ptr(), y.data_ptr() if y is not None else 0, gamma.data_ptr(),
                                beta.data_ptr(), rows, d, float(eps), out.data_ptr(),
                                _stream(stream, x.device))
     if rc != 0:
@@ -346,11 +365,11 @@ def r_proj(emb, w_r, H, out=None, stream=None):
     K, d = emb.shape
     dh = d // H
     _need(emb, "emb", (K, d), torch.bfloat16)
-    _need(w_r, "w_r", (d, d), torch.bfloat16)
+    _need(w_r, "w_r", (d, d), torch.bfloat16, emb.device)
     if out is None:
         out = torch.empty((K, H, dh), dtype=torch.bfloat16, device=emb.device)
-    _need(out, "r_k", (K, H, dh), torch.bfloat16)
-    rc = load().txl_r_proj(emb.data_ptr(), w_r.data_ptr(), K, H, dh, out.data_ptr(), _stream(stream, emb.device))
+    _need(out, "r_k", (K, H, dh), torch.bfloat16, emb.device)
+    rc = _invoke(emb.device, "txl_r_proj", emb.data_ptr(), w_r.data_ptr(), K, H, dh, out.data_ptr(), _stream(stream, emb.device))
     if rc != 0:
         raise TxlError(rc, "txl_r_proj")
     return out
@@ -365,14 +384,14 @@ def mem_update(mems: torch.Tensor, hids: torch.Tensor, stream=None, ext_len: int
     B, M, d = mems.shape
     L = hids.shape[1]
     _need(mems, "mems", (B, M, d), mems.dtype)
-    _need(hids, "hids", (B, L, d), mems.dtype)
+    _need(hids, "hids", (B, L, d), mems.dtype, mems.device)
     if ext_len:
-        rc = load().txl_mem_update_ext(mems.data_ptr(), hids.data_ptr(), B, L, M, d, int(ext_len),
+        rc = _invoke(mems.device, "txl_mem_update_ext", mems.data_ptr(), hids.data_ptr(), B, L, M, d, int(ext_len),
                                        _dtype_code(mems), _stream(stream, mems.device))
         if rc != 0:
             raise TxlError(rc, "txl_mem_update_ext")
         return mems
-    rc = load().txl_mem_update(mems.data_ptr(), hids.data_ptr(), B, L, M, d, _dtype_code(mems),
+    rc = _invoke(mems.device, "txl_mem_update", mems.data_ptr(), hids.data_ptr(), B, L, M, d, _dtype_code(mems),
                                _stream(stream, mems.device))
     if rc != 0:
         raise TxlError(rc, "txl_mem_update")
@@ -387,9 +406,9 @@ def mem_ring_push(ring: torch.Tensor, hids: torch.Tensor, start: int, stream=Non
     B, M, d = ring.shape
     L = hids.shape[1]
     _need(ring, "ring", (B, M, d), ring.dtype)
-    _need(hids, "hids", (B, L, d), ring.dtype)
+    _need(hids, "hids", (B, L, d), ring.dtype, ring.device)
     new = ctypes.c_int(0)
-    rc = load().txl_mem_ring_push(ring.data_ptr(), hids.data_ptr(), B, L, M, d, int(start), ctypes.byref(new),
+    rc = _invoke(ring.device, "txl_mem_ring_push", ring.data_ptr(), hids.data_ptr(), B, L, M, d, int(start), ctypes.byref(new),
                                   _dtype_code(ring), _stream(stream, ring.device))
     if rc != 0:
         raise TxlError(rc, "txl_mem_ring_push")
@@ -408,7 +427,7 @@ def mem_reset(mems: torch.Tensor, flags: torch.Tensor, stream=None) -> torch.Ten
     if flags.shape != (B,) or flags.device != mems.device or flags.dtype not in (torch.bool, torch.uint8):
         raise ValueError("flags must be a bool/uint8 tensor [B] on the memory's device")
     f = flags.contiguous()
-    rc = load().txl_mem_reset(mems.data_ptr(), f.data_ptr(), B, rows, d, _dtype_code(mems),
+    rc = _invoke(mems.device, "txl_mem_reset", mems.data_ptr(), f.data_ptr(), B, rows, d, _dtype_code(mems),
                               _stream(stream, mems.device))
     if rc != 0:
         raise TxlError(rc, "txl_mem_reset")
@@ -418,7 +437,7 @@ def mem_reset(mems: torch.Tensor, flags: torch.Tensor, stream=None) -> torch.Ten
 def sync_status(stream=None, device=None) -> int:
     """Waits for the stream and returns (and clears) the device status code."""
     dev = device if device is not None else torch.cuda.current_device()
-    return int(load().txl_sync_status(_stream(stream, dev)))
+    return int(_invoke(dev, "txl_sync_status", _stream(stream, dev)))
 
 
 def check_status(stream=None) -> None:

@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include "txl_device.cuh"
 
 namespace txl {
 
@@ -435,16 +436,16 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, co
     if ((e = cudaMemsetAsync(du, 0, nb, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dvb, 0, nb, stream)) != cudaSuccess) return e;
     if (dh <= kDT) {
-        static bool attr_set = false;
-        if (!attr_set) {
-            if ((e = cudaFuncSetAttribute(attn_bwd_tiled_kernel<float>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem)) != cudaSuccess)
-                return e;
-            if ((e = cudaFuncSetAttribute(attn_bwd_tiled_kernel<__nv_bfloat16>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem)) != cudaSuccess)
-                return e;
-            attr_set = true;
-        }
+        static PerDeviceOnce attrs;
+        e = attrs.run([] {
+            cudaError_t r = cudaFuncSetAttribute(attn_bwd_tiled_kernel<float>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(attn_bwd_tiled_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTiledSmem);
+            return r;
+        });
+        if (e != cudaSuccess) return e;
         const long long blocks = (long long)B * H * ((L + kQR - 1) / kQR);
         if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
         if (bf16)

@@ -553,8 +553,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     // the window: word K = (band c0+K, band c0+K+32), and
                     // position x of the shifted row is word (31 - lane) + x =
                     // the terms of keys x and x+32.  Half the shared-memory
-                    // traffic of moving f32 values; the f16 rounding of the
-                    // position term is bounded in the design notes.
+                    // traffic of moving f32 values.  The f16 rounding changes
+                    // the position term (already in log2 units: scale * log2 e
+                    // is folded into q+v) by at most 2^-11 |BD|, relative
+                    // rounding of an 11-bit significand; |BD| > 65504 would
+                    // saturate, far beyond any softmax score that matters.
                     uint32_t hp[64];
 #pragma unroll
                     for (int K = 0; K < 64; ++K)
@@ -1084,16 +1087,7 @@ static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const cuui
     return r == CUDA_SUCCESS;
 }
 
-static int num_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 1;
-    }
-    return n;
-}
+static int num_sms() { return current_sm_count(); }
 
 // Launch with programmatic stream serialisation (the kernel waits for the
 // previous kernel of the stream before its first global access).
@@ -1160,18 +1154,20 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, int lo_shift, void* out, void* workspace, int inject,
                                 int* status, cudaStream_t stream) {
     using namespace tc;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<true, false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    static PerDeviceOnce attrs;
+    {
+        const cudaError_t e = attrs.run([] {
+            cudaError_t r = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(attn_tc_bf16_kernel<true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(attn_tc_bf16_kernel<false, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            return r;
+        });
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const int K = M + L;
     CUtensorMap mQ, mK, mV, mR, mO;

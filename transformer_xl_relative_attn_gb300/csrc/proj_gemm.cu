@@ -454,16 +454,7 @@ static bool pg_encode_out(CUtensorMap* map, void* base, int B, int T, int width,
     return pg_encode(map, base, 4, dims, strides, box);
 }
 
-static int pg_num_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 1;
-    }
-    return n;
-}
+static int pg_num_sms() { return current_sm_count(); }
 
 // (declared in proj_gemm.h)
 cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d, int H, int dh,
@@ -471,12 +462,13 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     using namespace pg;
     using C = Cfg<256>;
     constexpr int BN = C::BN;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+    static PerDeviceOnce attrs;
+    {
+        const cudaError_t e = attrs.run([] {
+            return cudaFuncSetAttribute(proj_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+        });
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     if (n_gemm < 1 || n_gemm > 2) return cudaErrorInvalidValue;
     CUtensorMap maps[2][3];  // per problem: source a, source b, weights
@@ -557,12 +549,13 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
     using namespace pg;
     using C = Cfg<BN_>;
     constexpr int BN = C::BN;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<BN_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+    static PerDeviceOnce attrs;
+    {
+        const cudaError_t e = attrs.run([] {
+            return cudaFuncSetAttribute(proj_gemm_kernel<BN_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+        });
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     CUtensorMap maps[3];
     {

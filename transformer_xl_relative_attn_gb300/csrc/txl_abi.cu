@@ -47,12 +47,18 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Address of the static scratch on the current device, looked up once.
-void* noalloc_scratch() {
+// Address of the static scratch on the current device.  Outside a stream
+// capture it is looked up on every call (cheap), so a context torn down and
+// rebuilt (cudaDeviceReset) never leaves a stale address in use; inside a
+// capture, where the lookup may not run, the address cached by the last
+// lookup on this device is used.
+void* noalloc_scratch(cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
         g_scratch_addr[dev] = p;
@@ -60,7 +66,9 @@ void* noalloc_scratch() {
     return g_scratch_addr[dev];
 }
 
-int g_inject = 0;
+// Test hook of txl_debug_inject: per host thread, consumed by the next
+// bf16 attention launch of the same thread.
+thread_local int g_inject = 0;
 
 // Device address of the status word on the current device (looked up per
 // call: cheap, and correct when the caller switches devices).
@@ -306,7 +314,7 @@ int txl_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
     if (need > TXL_NOALLOC_SCRATCH_BYTES) return TXL_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
     if (need) {
-        scratch = noalloc_scratch();
+        scratch = noalloc_scratch(static_cast<cudaStream_t>(stream));
         if (!scratch) return TXL_ERR_CUDA;
     }
     return launch_attn(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, scale, out, dtype, scratch,

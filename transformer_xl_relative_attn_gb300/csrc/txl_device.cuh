@@ -3,11 +3,56 @@
 // MMA) instructions, all as thin inline-PTX wrappers.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 namespace txl {
+
+// ---------------------------------------------------------------- host side
+// Launch set-up that the runtime keeps per device (a kernel's shared-memory
+// attribute) and properties that differ between devices (the SM count) are
+// cached per device ordinal, never once per process: a process may launch on
+// several GPUs.
+constexpr int kMaxDeviceOrdinals = 64;
+
+// SM count of the current device (1 if it cannot be queried).
+inline int current_sm_count() {
+    static std::atomic<int> cache[kMaxDeviceOrdinals];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 0 || dev >= kMaxDeviceOrdinals) {
+        int n = 0;
+        return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0 ? n : 1;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// Runs `setup` once per device (with that device current) until it
+// succeeds; returns its error, or cudaSuccess once done on this device.
+struct PerDeviceOnce {
+    std::mutex mu;
+    bool done[kMaxDeviceOrdinals] = {};
+    template <class F>
+    cudaError_t run(F setup) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDeviceOrdinals) return setup();
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[dev]) return cudaSuccess;
+        e = setup();
+        if (e == cudaSuccess) done[dev] = true;
+        return e;
+    }
+};
 
 // Internal status codes written to the device status word (first error wins).
 enum DevStatus : int {

@@ -193,10 +193,24 @@ def project_qkv(lw: LayerWeights, mem: torch.Tensor, h: torch.Tensor, H: int):
     return q, k, v
 
 
-def project_r(lw: LayerWeights, M: int, L: int, H: int, device="cpu") -> torch.Tensor:
-    """R_k [M+L, H, dh], row r <-> distance M+L-1-r (fp32)."""
-    d = lw.W_r.shape[0]
+def position_sequence(M: int, L: int, clamp_len: int | None = None) -> torch.Tensor:
+    """The positions of the relative table, klen-1 down to 0 (klen = M+L),
+    optionally clamped from above at ``clamp_len`` as MemTransformerLM._forward
+    does before the positional embedding ("Transformer-XL模型 核心源码阅读笔记",
+    section "Build the model": pos_seq.clamp_(max=clamp_len) when clamp_len > 0;
+    here any clamp_len >= 0 is applied, 0 included).  fp64."""
     pos = torch.arange(M + L - 1, -1, -1, dtype=torch.float64)
+    if clamp_len is not None:
+        pos = pos.clamp(max=float(clamp_len))
+    return pos
+
+
+def project_r(lw: LayerWeights, M: int, L: int, H: int, device="cpu",
+              clamp_len: int | None = None) -> torch.Tensor:
+    """R_k [M+L, H, dh], row r <-> distance M+L-1-r (fp32); with clamp_len,
+    every distance beyond it uses the embedding of clamp_len."""
+    d = lw.W_r.shape[0]
+    pos = position_sequence(M, L, clamp_len)
     emb = sinusoid(pos, d).to(device)
     return _mm32(emb, lw.W_r).reshape(M + L, H, d // H).contiguous()
 
