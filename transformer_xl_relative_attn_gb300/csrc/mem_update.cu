@@ -17,8 +17,31 @@
 
 namespace txl {
 
-constexpr int kChain = 8;   // sources of one chain in flight per thread
+constexpr int kChain = 16;  // sources of one chain in flight per thread
 constexpr int kCopyUnroll = 4;  // vectors in flight per thread in the plain copy
+
+// The roll kernels are launched with programmatic stream serialisation: each
+// lets the next kernel of the stream launch at once and waits for the
+// previous one to complete before its first global access, so back-to-back
+// rolls do not pay a full launch gap each.
+__device__ __forceinline__ void pdl_prologue() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, long long blocks, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // L >= M: every new row comes from h, and memory row r of batch b takes h row
 // L-M+r, so the roll is one contiguous copy of M rows per batch row: element
@@ -28,6 +51,7 @@ constexpr int kCopyUnroll = 4;  // vectors in flight per thread in the plain cop
 template <typename V, typename I>
 __global__ void __launch_bounds__(256) tail_copy_kernel(V* __restrict__ mem, const V* __restrict__ hid,
                                                         I total, I seg, I hstride, I hoff) {
+    pdl_prologue();
     const I base = (I)blockIdx.x * (256 * kCopyUnroll) + threadIdx.x;
     V buf[kCopyUnroll];
 #pragma unroll
@@ -52,6 +76,7 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(V* __restrict__ mem, con
 template <typename V, typename I>
 __global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, const V* __restrict__ hid,
                                                          int L, int M, I rowv, I total, I hstride) {
+    pdl_prologue();
     const I t = (I)blockIdx.x * 256 + threadIdx.x;
     if (t >= total) return;
     const I col = t % rowv;
@@ -106,28 +131,22 @@ cudaError_t launch_tail_m(void* mem, const void* hid, int B, int L, int L_stride
             const long long blocks = (total + 256 * kCopyUnroll - 1) / (256 * kCopyUnroll);
             if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
             if (hsz < 0x7FFFFFFFll - 256 * kCopyUnroll)
-                tail_copy_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), (int)total, (int)seg,
-                    (int)(L_stride * rowv), (int)((L - M) * rowv));
-            else
-                tail_copy_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), total, seg, L_stride * rowv,
-                    (L - M) * rowv);
+                return launch_pdl(tail_copy_kernel<V, int>, blocks, stream, static_cast<V*>(mem),
+                                  static_cast<const V*>(hid), (int)total, (int)seg, (int)(L_stride * rowv),
+                                  (int)((L - M) * rowv));
+            return launch_pdl(tail_copy_kernel<V, long long>, blocks, stream, static_cast<V*>(mem),
+                              static_cast<const V*>(hid), total, seg, L_stride * rowv, (L - M) * rowv);
         } else {
             const long long total = (long long)B * L * rowv;
             const long long msz = (long long)B * (M > L_stride ? M : L_stride) * rowv;
             const long long blocks = (total + 255) / 256;
             if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
             if (msz < 0x7FFFFFFFll - 256)
-                tail_chain_kernel<V, int><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, (int)rowv, (int)total,
-                    (int)(L_stride * rowv));
-            else
-                tail_chain_kernel<V, long long><<<(unsigned)blocks, 256, 0, stream>>>(
-                    static_cast<V*>(mem), static_cast<const V*>(hid), L, M, rowv, total,
-                    (long long)L_stride * rowv);
+                return launch_pdl(tail_chain_kernel<V, int>, blocks, stream, static_cast<V*>(mem),
+                                  static_cast<const V*>(hid), L, M, (int)rowv, (int)total, (int)(L_stride * rowv));
+            return launch_pdl(tail_chain_kernel<V, long long>, blocks, stream, static_cast<V*>(mem),
+                              static_cast<const V*>(hid), L, M, rowv, total, (long long)L_stride * rowv);
         }
-        return cudaGetLastError();
     };
     const uintptr_t a = reinterpret_cast<uintptr_t>(mem) | reinterpret_cast<uintptr_t>(hid);
     if (row_bytes % 16 == 0 && a % 16 == 0) return go(uint4{});
