@@ -51,7 +51,8 @@ enum txl_status {
     TXL_ERR_DEVICE_TIMEOUT = -6, /* a bounded device-side wait expired (reported by txl_sync_status) */
     TXL_ERR_WORKSPACE = -7,      /* workspace pointer null/misaligned or smaller than required */
     TXL_ERR_CUDA = -8,           /* a CUDA runtime/driver call failed (e.g. tensor-map encoding) */
-    TXL_ERR_SCRATCH_LIMIT = -9   /* the call needs more scratch than txl_attn_fwd_noalloc holds */
+    TXL_ERR_SCRATCH_LIMIT = -9,  /* the call needs more scratch than txl_attn_fwd_noalloc holds */
+    TXL_ERR_OUT_OF_BOUNDS = -10  /* a bounds-checked build skipped an out-of-range access */
 };
 
 /*
@@ -314,6 +315,22 @@ int txl_mem_reset(void* mems, const void* flags, int B, int rows, int d, int dty
  * call, TXL_ERR_CUDA if the stream reports a CUDA error, TXL_OK otherwise.
  */
 int txl_sync_status(void* stream);
+
+/*
+ * Bounds-checked builds (the library compiled with -DTXL_CHECKED, shipped as
+ * libtxl_checked.so beside libtxl.so): every kernel routes its computed
+ * global-memory indexes and shared-memory addresses through a check; an
+ * access outside its buffer is skipped, never performed, and the first such
+ * access per source file is recorded (no trap, no fault).  TMA copies are
+ * bounded by their tensor maps in hardware and are not re-checked.
+ * txl_bounds_status synchronises the device, then returns TXL_OK when no
+ * access was out of range since the last call, or TXL_ERR_OUT_OF_BOUNDS with
+ * the first record in *first: bit 63 set, bits 40..62 the check site (the
+ * hundreds digit names the source file), bits 0..39 the offending index
+ * (mod 2^40).  The records are cleared.  TXL_ERR_UNSUPPORTED from a library
+ * built without checks.  A debugging aid, not for production launches.
+ */
+int txl_bounds_status(unsigned long long* first);
 
 /* Human-readable name of a txl_status value (static string). */
 const char* txl_status_string(int status);

@@ -178,3 +178,22 @@ def test_attn_bwd_rejects_bad_arguments(lib):
     assert call(grads=[A] + g[1:]) == -4           # dq over the inputs
     assert call(grads=[g[0], g[0]] + g[2:]) == -4  # two gradients overlap
     assert call(same_length=1, mem_len=1) == -1
+
+
+def test_plain_build_reports_no_bounds_checks(lib):
+    """txl_bounds_status is a bounds-checked-build facility: the plain library
+    answers TXL_ERR_UNSUPPORTED without touching the GPU."""
+    st, first = txl.bounds_status()
+    assert st == -2 and first == 0
+
+
+def test_checked_build_exports_the_same_symbols():
+    """libtxl_checked.so (the -DTXL_CHECKED build of the same sources) exports
+    every function the header declares, like libtxl.so."""
+    import os
+    path = os.path.join(os.path.dirname(txl.LIB_PATH), "libtxl_checked.so")
+    assert os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    assert set(txl.header_functions()) <= exported

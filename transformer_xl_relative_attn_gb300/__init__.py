@@ -10,18 +10,19 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
     qkv_proj, r_proj                              head-split input projections (tensor cores)
     linear, layer_norm                            o_net / feed-forward GEMMs, fused residual LayerNorm
     sync_status, check_status                     device status word
+    bounds_status                                 first out-of-range access (bounds-checked build)
     SegmentDriver                                 multi-segment, multi-layer driver (caller's projections)
     AttnStack                                     the same with the library's projections
     DecoderStack                                  full decoder layers (attention, o_net, LayerNorm, feed-forward)
 """
 from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_bwd, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
-                   attn_workspace_bytes,
+                   attn_workspace_bytes, bounds_status,
                    check_status, debug_inject, header_functions, layer_norm, linear, load, mem_reset, mem_ring_push, mem_update, qkv_proj, r_proj,
                    status_string,
                    sync_status, version, LIB_PATH)
 from .driver import AttnStack, DecoderStack, SegmentDriver
 
 __all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_bwd", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
-           "attn_workspace_bytes",
+           "attn_workspace_bytes", "bounds_status",
            "check_status", "debug_inject", "header_functions", "layer_norm", "linear", "load", "mem_reset", "mem_ring_push", "mem_update", "qkv_proj", "r_proj",
            "status_string", "sync_status", "version", "SegmentDriver", "AttnStack", "DecoderStack", "LIB_PATH"]

@@ -11,7 +11,9 @@ import threading
 import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libtxl.so")
+# TXL_BOUNDS_CHECKED=1 selects the bounds-checked build of the same library
+LIB_PATH = os.path.join(PKG, "libtxl_checked.so" if os.environ.get("TXL_BOUNDS_CHECKED") == "1"
+                        else "libtxl.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "txl_attn.h")
 
 TXL_F32 = 0
@@ -28,6 +30,7 @@ STATUS = {
     -7: "TXL_ERR_WORKSPACE",
     -8: "TXL_ERR_CUDA",
     -9: "TXL_ERR_SCRATCH_LIMIT",
+    -10: "TXL_ERR_OUT_OF_BOUNDS",
 }
 
 _lib = None
@@ -93,6 +96,8 @@ def load() -> ctypes.CDLL:
         lib.txl_version.restype = i
         lib.txl_debug_inject.argtypes = [i]
         lib.txl_debug_inject.restype = i
+        lib.txl_bounds_status.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+        lib.txl_bounds_status.restype = i
         _lib = lib
         return lib
 
@@ -444,6 +449,14 @@ def check_status(stream=None) -> None:
     rc = sync_status(stream)
     if rc != 0:
         raise TxlError(rc, "device status")
+
+
+def bounds_status() -> tuple[int, int]:
+    """txl_bounds_status: (status, first record) of a bounds-checked build;
+    status TXL_ERR_UNSUPPORTED (-2) from the plain build."""
+    w = ctypes.c_ulonglong(0)
+    rc = load().txl_bounds_status(ctypes.byref(w))
+    return int(rc), int(w.value)
 
 
 def debug_inject(kind: int) -> None:

@@ -32,6 +32,16 @@ constexpr int kBwdWarps = 4;
 __device__ __forceinline__ float ld_f(const float* p) { return *p; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// Element idx of an array of n elements (bounds-checked builds skip and
+// record an index outside it; otherwise the check compiles away).
+template <typename T>
+__device__ __forceinline__ float ld_at(const T* base, long long idx, long long n, int site) {
+    return TXL_BOUNDS(idx >= 0 && idx < n, site, idx) ? ld_f(base + idx) : 0.f;
+}
+__device__ __forceinline__ void add_at(float* base, long long idx, long long n, int site, float v) {
+    if (TXL_BOUNDS(idx >= 0 && idx < n, site, idx)) atomicAdd(base + idx, v);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(32 * kBwdWarps)
 attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
@@ -50,34 +60,33 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     const long long bh = row / L;
     const int h = (int)(bh % H);
     const int K = M + L;
+    const long long n_q = (long long)B * H * L * dh, n_kv = (long long)B * H * K * dh;
+    const long long n_r = (long long)K * H * dh, n_b = (long long)H * dh;
     for (int t = lane; t < dh; t += 32) {
-        const float x = ld_f(q + row * dh + t);
-        s_qu[warp][t] = x + ld_f(ub + h * dh + t);
-        s_qv[warp][t] = x + ld_f(vb + h * dh + t);
-        s_do[warp][t] = ld_f(dout + row * dh + t);
+        const float x = ld_at(q, row * dh + t, n_q, 501);
+        s_qu[warp][t] = x + ld_at(ub, (long long)h * dh + t, n_b, 502);
+        s_qv[warp][t] = x + ld_at(vb, (long long)h * dh + t, n_b, 503);
+        s_do[warp][t] = ld_at(dout, row * dh + t, n_q, 504);
     }
     __syncwarp();
-    const T* kb = k + bh * (long long)K * dh;
-    const T* vbase = v + bh * (long long)K * dh;
     const int nvis = M + i + 1;                   // keys up to M+i
     const int jlo = max(0, i + 1 - lo_shift);     // ... from jlo on (same_length)
     const int ncol = (dh + 31) / 32;
 
     auto score = [&](int j) {
         const int dist = M + i - j;
-        const T* kj = kb + (long long)j * dh;
-        const T* rj = r + ((long long)(K - 1 - dist) * H + h) * dh;
+        const long long ki = (bh * K + j) * dh, ri = ((long long)(K - 1 - dist) * H + h) * dh;
         float ac = 0.f, bd = 0.f;
         for (int t = 0; t < dh; ++t) {
-            ac = fmaf(s_qu[warp][t], ld_f(kj + t), ac);
-            bd = fmaf(s_qv[warp][t], ld_f(rj + t), bd);
+            ac = fmaf(s_qu[warp][t], ld_at(k, ki + t, n_kv, 505), ac);
+            bd = fmaf(s_qv[warp][t], ld_at(r, ri + t, n_r, 506), bd);
         }
         return scale * (ac + bd);
     };
     auto dprob = [&](int j) {
-        const T* vj = vbase + (long long)j * dh;
+        const long long vi = (bh * K + j) * dh;
         float a = 0.f;
-        for (int t = 0; t < dh; ++t) a = fmaf(s_do[warp][t], ld_f(vj + t), a);
+        for (int t = 0; t < dh; ++t) a = fmaf(s_do[warp][t], ld_at(v, vi + t, n_kv, 507), a);
         return a;
     };
 
@@ -121,20 +130,16 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
             const float dsj = __shfl_sync(0xffffffffu, ds, jj);
             const int jk = j0 + jj;
             const long long rrow = (long long)(K - 1 - (M + i - jk));
-            const T* kj = kb + (long long)jk * dh;
-            const T* rj = r + (rrow * H + h) * dh;
-            float* dkj = dk + (bh * K + jk) * dh;
-            float* dvj = dv + (bh * K + jk) * dh;
-            float* drj = dr + (rrow * H + h) * dh;
+            const long long kvi = (bh * K + jk) * dh, ri = (rrow * H + h) * dh;
 #pragma unroll
             for (int c = 0; c < kBwdMaxD / 32; ++c) {
                 const int t = lane + 32 * c;
                 if (c < ncol && t < dh) {
-                    gq_c[c] = fmaf(dsj, ld_f(kj + t), gq_c[c]);
-                    gq_p[c] = fmaf(dsj, ld_f(rj + t), gq_p[c]);
-                    atomicAdd(dkj + t, scale * dsj * s_qu[warp][t]);
-                    atomicAdd(dvj + t, pj * s_do[warp][t]);
-                    atomicAdd(drj + t, scale * dsj * s_qv[warp][t]);
+                    gq_c[c] = fmaf(dsj, ld_at(k, kvi + t, n_kv, 508), gq_c[c]);
+                    gq_p[c] = fmaf(dsj, ld_at(r, ri + t, n_r, 509), gq_p[c]);
+                    add_at(dk, kvi + t, n_kv, 510, scale * dsj * s_qu[warp][t]);
+                    add_at(dv, kvi + t, n_kv, 511, pj * s_do[warp][t]);
+                    add_at(dr, ri + t, n_r, 512, scale * dsj * s_qv[warp][t]);
                 }
             }
         }
@@ -143,9 +148,9 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     for (int c = 0; c < kBwdMaxD / 32; ++c) {
         const int t = lane + 32 * c;
         if (c < ncol && t < dh) {
-            dq[row * dh + t] = scale * (gq_c[c] + gq_p[c]);
-            atomicAdd(du + h * dh + t, scale * gq_c[c]);
-            atomicAdd(dvb + h * dh + t, scale * gq_p[c]);
+            if (TXL_BOUNDS(row * dh + t < n_q, 513, row * dh + t)) dq[row * dh + t] = scale * (gq_c[c] + gq_p[c]);
+            add_at(du, (long long)h * dh + t, n_b, 514, scale * gq_c[c]);
+            add_at(dvb, (long long)h * dh + t, n_b, 515, scale * gq_p[c]);
         }
     }
 }
@@ -198,14 +203,16 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     const int i0 = (int)(blockIdx.x % nqt) * kQR;
     const int h = (int)(bh % H);
     const int K = M + L;
+    const long long n_q = (long long)B * H * L * dh, n_kv = (long long)B * H * K * dh;
+    const long long n_r = (long long)K * H * dh, n_b = (long long)H * dh;
     for (int idx = tid; idx < kQR * kDT; idx += 256) {
         const int rr = idx / kDT, t = idx % kDT, i = i0 + rr;
         float a = 0.f, b = 0.f, c = 0.f;
         if (i < L && t < dh) {
-            const float x = ld_f(q + (bh * L + i) * dh + t);
-            a = x + ld_f(ub + h * dh + t);
-            b = x + ld_f(vb + h * dh + t);
-            c = ld_f(dout + (bh * L + i) * dh + t);
+            const float x = ld_at(q, (bh * L + i) * dh + t, n_q, 521);
+            a = x + ld_at(ub, (long long)h * dh + t, n_b, 522);
+            b = x + ld_at(vb, (long long)h * dh + t, n_b, 523);
+            c = ld_at(dout, (bh * L + i) * dh + t, n_q, 524);
         }
         s_qu[idx] = a;
         s_qv[idx] = b;
@@ -221,8 +228,8 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
             const int jj = idx / kDT, t = idx % kDT, j = j0 + jj;
             float a = 0.f, b = 0.f;
             if (j < K && t < dh) {
-                a = ld_f(k + (bh * K + j) * dh + t);
-                b = ld_f(v + (bh * K + j) * dh + t);
+                a = ld_at(k, (bh * K + j) * dh + t, n_kv, 525);
+                b = ld_at(v, (bh * K + j) * dh + t, n_kv, 526);
             }
             t_k[jj * kPad + t] = a;
             t_v[jj * kPad + t] = b;
@@ -230,7 +237,7 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
         for (int idx = tid; idx < kSpan * kDT; idx += 256) {
             const int sl = idx / kDT, t = idx % kDT;
             const long long rrow = (long long)K - 1 - (M + (sl - 31) + i0 - j0);
-            t_r[sl * kPad + t] = (rrow >= 0 && rrow < K && t < dh) ? ld_f(r + (rrow * H + h) * dh + t) : 0.f;
+            t_r[sl * kPad + t] = (rrow >= 0 && rrow < K && t < dh) ? ld_at(r, (rrow * H + h) * dh + t, n_r, 527) : 0.f;
         }
         __syncthreads();
     };
@@ -357,15 +364,13 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
                 for (int c = 0; c < 2; ++c) {
                     const int t = 32 * c + 4 * cg;
                     if (t < dh) {
-                        float* pk = dk + (bh * K + jk) * dh + t;
-                        float* pv2 = dv + (bh * K + jk) * dh + t;
                         const float ek[4] = {ak[c].x, ak[c].y, ak[c].z, ak[c].w};
                         const float ev[4] = {av[c].x, av[c].y, av[c].z, av[c].w};
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
                             if (t + x >= dh) break;
-                            if (ek[x] != 0.f) atomicAdd(pk + x, scale * ek[x]);
-                            if (ev[x] != 0.f) atomicAdd(pv2 + x, ev[x]);
+                            if (ek[x] != 0.f) add_at(dk, (bh * K + jk) * dh + t + x, n_kv, 528, scale * ek[x]);
+                            if (ev[x] != 0.f) add_at(dv, (bh * K + jk) * dh + t + x, n_kv, 529, ev[x]);
                         }
                     }
                 }
@@ -388,11 +393,10 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
             for (int c = 0; c < 2; ++c) {
                 const int t = 32 * c + 4 * cg;
                 if (t < dh) {
-                    float* pr = dr + (rrow * H + h) * dh + t;
                     const float e[4] = {ar[c].x, ar[c].y, ar[c].z, ar[c].w};
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
-                        if (t + x < dh && e[x] != 0.f) atomicAdd(pr + x, scale * e[x]);
+                        if (t + x < dh && e[x] != 0.f) add_at(dr, (rrow * H + h) * dh + t + x, n_r, 530, scale * e[x]);
                 }
             }
         }
@@ -409,9 +413,10 @@ attn_bwd_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {
                         if (t + x >= dh) break;
-                        dq[(bh * L + i) * dh + t + x] = scale * (ec[x] + ep[x]);
-                        atomicAdd(du + h * dh + t + x, scale * ec[x]);
-                        atomicAdd(dvb + h * dh + t + x, scale * ep[x]);
+                        if (TXL_BOUNDS((bh * L + i) * dh + t + x < n_q, 531, (bh * L + i) * dh + t + x))
+                            dq[(bh * L + i) * dh + t + x] = scale * (ec[x] + ep[x]);
+                        add_at(du, (long long)h * dh + t + x, n_b, 532, scale * ec[x]);
+                        add_at(dvb, (long long)h * dh + t + x, n_b, 533, scale * ep[x]);
                     }
                 }
             }
@@ -479,5 +484,7 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* k, const void* v, co
             static_cast<const float*>(dout), B, H, L, M, dh, scale, lo_shift, dq, dk, dv, dr, du, dvb);
     return cudaGetLastError();
 }
+
+TXL_BOUNDS_READER(bounds_word_attn_bwd)
 
 }  // namespace txl

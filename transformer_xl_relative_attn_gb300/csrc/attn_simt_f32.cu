@@ -13,6 +13,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "txl_device.cuh"
+
 namespace txl {
 
 constexpr int kSimtMaxD = 256;
@@ -33,10 +35,13 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     const int h = (int)(bh % H);
     const int K = M + L;
     const float* qi = q + row * dh;
+    const long long n_q = (long long)B * H * L * dh, n_kv = (long long)B * H * K * dh;
+    const long long n_r = (long long)K * H * dh, n_b = (long long)H * dh;
     for (int t = lane; t < dh; t += 32) {
-        const float x = qi[t];
-        s_qu[warp][t] = x + ub[h * dh + t];
-        s_qv[warp][t] = x + vb[h * dh + t];
+        const float x = TXL_BOUNDS(row * dh + t < n_q, 101, row * dh + t) ? qi[t] : 0.f;
+        const bool bo = TXL_BOUNDS(h * dh + t < n_b, 102, h * dh + t);
+        s_qu[warp][t] = x + (bo ? ub[h * dh + t] : 0.f);
+        s_qv[warp][t] = x + (bo ? vb[h * dh + t] : 0.f);
     }
     __syncwarp();
     const float* kb = k + bh * (long long)K * dh;
@@ -54,11 +59,14 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
         if (j < nvis) {
             const int dist = M + i - j;
             const float* kj = kb + (long long)j * dh;
-            const float* rj = r + ((long long)(K - 1 - dist) * H + h) * dh;
+            const long long ri = ((long long)(K - 1 - dist) * H + h) * dh;
+            const float* rj = r + ri;
             float ac = 0.f, bd = 0.f;
+            const bool kin = TXL_BOUNDS((bh * K + j) * dh + dh <= n_kv, 103, (bh * K + j) * dh);
+            const bool rin = TXL_BOUNDS(ri >= 0 && ri + dh <= n_r, 104, ri);
             for (int t = 0; t < dh; ++t) {
-                ac = fmaf(s_qu[warp][t], kj[t], ac);
-                bd = fmaf(s_qv[warp][t], rj[t], bd);
+                if (kin) ac = fmaf(s_qu[warp][t], kj[t], ac);
+                if (rin) bd = fmaf(s_qv[warp][t], rj[t], bd);
             }
             s = scale * (ac + bd);
         }
@@ -79,6 +87,7 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
         for (int jj = 0; jj < nk; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
             const float* vj = vbase + (long long)(j0 + jj) * dh;
+            if (!TXL_BOUNDS((bh * K + j0 + jj) * dh + dh <= n_kv, 105, (bh * K + j0 + jj) * dh)) continue;
 #pragma unroll
             for (int c = 0; c < kSimtMaxD / 32; ++c) {
                 const int t = lane + 32 * c;
@@ -91,7 +100,7 @@ attn_simt_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 #pragma unroll
     for (int c = 0; c < kSimtMaxD / 32; ++c) {
         const int t = lane + 32 * c;
-        if (c < ncol && t < dh) o[t] = acc[c] * inv;
+        if (c < ncol && t < dh && TXL_BOUNDS(row * dh + t < n_q, 106, row * dh + t)) o[t] = acc[c] * inv;
     }
 }
 
@@ -105,5 +114,7 @@ cudaError_t launch_attn_simt_f32(const float* q, const float* k, const float* v,
         q, k, v, r, ub, vb, B, H, L, M, dh, scale, lo_shift, out);
     return cudaGetLastError();
 }
+
+TXL_BOUNDS_READER(bounds_word_attn_simt)
 
 }  // namespace txl

@@ -355,6 +355,11 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
                  : "memory");
 }
 
+// Bounds-checked builds: a shared-memory access of `bytes` at `addr` stays
+// inside this CTA's dynamic shared memory.
+#define TXL_SMEM_IN(addr, bytes, site) \
+    TXL_BOUNDS((addr) >= s_base && (addr) + (bytes) <= s_base + tc::SMEM_BYTES, (site), (long long)(addr) - s_base)
+
 // SPLIT: the units are key splits of items and write partial results (see
 // attn_combine_kernel); otherwise every unit is a whole item.  LOWER: the
 // same_length lower key bound is applied (tiles below it skipped, keys below
@@ -478,7 +483,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const uint4* brow = reinterpret_cast<const uint4*>((grp == 0 ? p.ub : p.vb) + (size_t)cur.h * DH);
                 uint4 b4[8];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) b4[ch] = __ldg(brow + ch);
+                for (int ch = 0; ch < 8; ++ch)
+                    b4[ch] = TXL_BOUNDS(cur.h < p.H, 401, cur.h) ? __ldg(brow + ch) : make_uint4(0, 0, 0, 0);
                 ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full, 0, kDevTimeoutSoftmax, abort, p.status));
                 if (!ok && tid == 0) drain_wait(&sh->q_full, 0, p.status);
                 if (ok) {
@@ -488,6 +494,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     for (int ch = 0; ch < 8; ++ch) {
                         const uint32_t a = row + ((ch ^ (ii & 7)) << 4);
                         float raw[4];
+                        if (!TXL_SMEM_IN(a, 16, 402)) continue;
                         ld_shared_v4(a, raw);
                         const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
                         const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(&b4[ch]);
@@ -569,6 +576,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         store_pending = false;
                     }
                     __syncwarp();
+                    if (!TXL_SMEM_IN(t_ld, 128 * 31 + 4, 403)) break;
                     st_shift_all<0>(31 - lane, t_st, *reinterpret_cast<uint32_t(*)[32]>(&hp[0]),
                                     *reinterpret_cast<uint32_t(*)[32]>(&hp[32]));
                     ld_shift_all<0>(t_ld, win);
@@ -622,7 +630,8 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         rs = add2(rs, make_float2(p0, p1));
                         w[e] = pack_bf16x2(p0, p1);
                     }
-                    st_shared_v4(p_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
+                    if (TXL_SMEM_IN(p_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4), 16, 404))
+                        st_shared_v4(p_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4), w[0], w[1], w[2], w[3]);
                 }
                 l_run = l_run * alpha + (rs.x + rs.y);
                 m_run = m_new;
@@ -645,16 +654,22 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // keeps every P write of the next tiles behind all (m, l) reads.
             {
                 float* ml_out = reinterpret_cast<float*>(smem + OFF_P + (grp ^ 1) * SZ_Q);
-                ml_out[2 * ii] = seen ? m_run : -INFINITY;
-                ml_out[2 * ii + 1] = seen ? l_run : -1.f;
+                if (TXL_SMEM_IN(smem_u32(ml_out + 2 * ii), 8, 405)) {
+                    ml_out[2 * ii] = seen ? m_run : -INFINITY;
+                    ml_out[2 * ii + 1] = seen ? l_run : -1.f;
+                }
             }
             // both groups reach these barriers on every path (ok is warp-uniform)
             asm volatile("bar.sync 1, 256;" ::: "memory");
             float mo, lo;
             {
                 const float* ml_in = reinterpret_cast<const float*>(smem + OFF_P + grp * SZ_Q);
-                mo = ml_in[2 * ii];
-                lo = ml_in[2 * ii + 1];
+                mo = -INFINITY;
+                lo = -1.f;
+                if (TXL_SMEM_IN(smem_u32(ml_in + 2 * ii), 8, 406)) {
+                    mo = ml_in[2 * ii];
+                    lo = ml_in[2 * ii + 1];
+                }
             }
             // One snapshot of the abort flag decides for all 256 threads, so
             // that either every softmax warp runs the merge (with its group
@@ -700,6 +715,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             const float x0 = has0 ? __uint_as_float(o0[8 * c + e]) * a0 : 0.f;
                             y[e] = has1 ? fmaf(__uint_as_float(o1[8 * c + e]), a1, x0) : x0;
                         }
+                        if (TXL_SMEM_IN(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), 16, 407))
                         st_shared_v4(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(y[0], y[1]),
                                      pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                     }
@@ -726,9 +742,10 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             const float x0 = has0 ? __uint_as_float(o0[4 * c + e]) * f0 : 0.f;
                             y[e] = has1 ? fmaf(__uint_as_float(o1[4 * c + e]), f1, x0) : x0;
                         }
-                        orow[c] = make_float4(y[0], y[1], y[2], y[3]);
+                        if (TXL_BOUNDS(cur.unit < p.n_units, 408, cur.unit))
+                            orow[c] = make_float4(y[0], y[1], y[2], y[3]);
                     }
-                    if (grp == 0)
+                    if (grp == 0 && TXL_BOUNDS(cur.unit < p.n_units, 409, cur.unit))
                         p.ws_ml[(size_t)cur.unit * BM + ii] =
                             make_float2(m, (has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
                 }
@@ -915,8 +932,11 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 tma_load_3d(smem + qb + SZ_Q, &tmQ, &sh->q_full, 0, it.i0, it.bh);
             }
             ++issued;
-            const uint4 bu = __ldg(reinterpret_cast<const uint4*>(p.ub + (size_t)it.h * DH) + ch);
-            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.vb + (size_t)it.h * DH) + ch);
+            const bool hin = TXL_BOUNDS(it.h < p.H, 410, it.h);
+            const uint4 bu = hin ? __ldg(reinterpret_cast<const uint4*>(p.ub + (size_t)it.h * DH) + ch)
+                                 : make_uint4(0, 0, 0, 0);
+            const uint4 bv = hin ? __ldg(reinterpret_cast<const uint4*>(p.vb + (size_t)it.h * DH) + ch)
+                                 : make_uint4(0, 0, 0, 0);
             ok = __all_sync(0xffffffffu, mbar_wait(&sh->q_full, k & 1, kDevTimeoutMma, abort, p.status));
             if (!ok) break;
             ++landed;
@@ -927,6 +947,7 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 for (int slot = 0; slot < 2; ++slot) {
                     const uint4& b4 = slot ? bv : bu;
                     float raw[4];
+                    if (!TXL_SMEM_IN(a + slot * SZ_Q, 16, 411)) continue;
                     ld_shared_v4(a + slot * SZ_Q, raw);
                     const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(raw);
                     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b4);
@@ -1029,6 +1050,8 @@ attn_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ w
     const int i = row % L, bh = row / L;
     const int qt = i / BM, ii = i % BM;
     const int witem = (n_qtiles - 1 - qt) * n_bh + bh;
+    // every unit this row reads exists: n_bh * n_qtiles items of nsplit units
+    if (!TXL_BOUNDS((long long)(witem + 1) * nsplit <= (long long)n_bh * n_qtiles * nsplit, 412, witem)) return;
     float mx = -INFINITY;
     for (int sp = 0; sp < nsplit; ++sp) {
         const float2 ml = ws_ml[(size_t)(witem * nsplit + sp) * BM + ii];
@@ -1237,5 +1260,7 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
         p.ws_o, p.ws_ml, p.out, B * H, L, p.n_qtiles, p.nsplit);
     return cudaGetLastError();
 }
+
+TXL_BOUNDS_READER(bounds_word_attn_tc)
 
 }  // namespace txl

@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "txl_device.cuh"
+
 namespace txl {
 
 template <int VPL>  // 16-byte vectors per lane: d = 256 * VPL
@@ -33,7 +35,9 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const __nv_bfloat16* x,
     const uint4* y4 = y ? reinterpret_cast<const uint4*>(y + r * d) : nullptr;
 #pragma unroll
     for (int c = 0; c < VPL; ++c) {
-        const uint4 a = x4[c * 32 + lane];
+        // vector index within the row: (c * 32 + lane) of d / 8
+        const bool in_row = TXL_BOUNDS(c * 32 + lane < d / 8, 301, r * (d / 8) + c * 32 + lane);
+        const uint4 a = in_row ? x4[c * 32 + lane] : make_uint4(0, 0, 0, 0);
         const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -41,7 +45,7 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const __nv_bfloat16* x,
             z[8 * c + 2 * e] = f.x;
             z[8 * c + 2 * e + 1] = f.y;
         }
-        if (y4) {
+        if (y4 && in_row) {
             const uint4 b = y4[c * 32 + lane];
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -72,6 +76,7 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const __nv_bfloat16* x,
     uint4* o4 = reinterpret_cast<uint4*>(out + r * d);
 #pragma unroll
     for (int c = 0; c < VPL; ++c) {
+        if (!TXL_BOUNDS(c * 32 + lane < d / 8, 302, c * 32 + lane)) continue;
         const uint4 gv = __ldg(g4 + c * 32 + lane), bv = __ldg(b4 + c * 32 + lane);
         const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
         const __nv_bfloat162* bb2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
@@ -119,5 +124,7 @@ cudaError_t launch_layer_norm(const void* x, const void* y, const void* gamma, c
         default: return cudaErrorInvalidValue;
     }
 }
+
+TXL_BOUNDS_READER(bounds_word_layer_norm)
 
 }  // namespace txl

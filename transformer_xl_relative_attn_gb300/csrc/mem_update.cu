@@ -15,6 +15,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "txl_device.cuh"
+
 namespace txl {
 
 constexpr int kChain = 16;  // sources of one chain in flight per thread
@@ -59,13 +61,15 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(V* __restrict__ mem, con
         const I e = base + (I)u * 256;
         if (e < total) {
             const I b = e / seg;
-            buf[u] = hid[b * hstride + hoff + (e - b * seg)];
+            const I hi = b * hstride + hoff + (e - b * seg);
+            // hid holds total / seg batch rows of hstride vectors
+            if (TXL_BOUNDS(hi >= 0 && hi < (total / seg) * hstride, 201, hi)) buf[u] = hid[hi];
         }
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
         const I e = base + (I)u * 256;
-        if (e < total) mem[e] = buf[u];
+        if (e < total && TXL_BOUNDS(e >= 0, 202, e)) mem[e] = buf[u];
     }
 }
 
@@ -92,13 +96,21 @@ __global__ void __launch_bounds__(256) tail_chain_kernel(V* __restrict__ mem, co
             const int r = r0 + s * L;
             if (r < M) {
                 const int src = r + L;
-                buf[s] = src < M ? mrow[(I)src * rowv] : hrow[(I)(src - M) * rowv];
+                if (src < M) {
+                    const I mi = (b * (I)M + src) * rowv + col;
+                    if (TXL_BOUNDS(mi < (total / ((I)L * rowv)) * (I)M * rowv, 203, mi)) buf[s] = mrow[(I)src * rowv];
+                } else {
+                    const I hi = b * hstride + (I)(src - M) * rowv + col;
+                    if (TXL_BOUNDS(hi < (total / ((I)L * rowv)) * hstride, 204, hi)) buf[s] = hrow[(I)(src - M) * rowv];
+                }
             }
         }
 #pragma unroll
         for (int s = 0; s < kChain; ++s) {
             const int r = r0 + s * L;
-            if (r < M) mrow[(I)r * rowv] = buf[s];
+            if (r < M && TXL_BOUNDS((b * (I)M + r) * rowv + col < (total / ((I)L * rowv)) * (I)M * rowv, 205,
+                                    (b * (I)M + r) * rowv + col))
+                mrow[(I)r * rowv] = buf[s];
         }
     }
 }
@@ -112,7 +124,7 @@ __global__ void __launch_bounds__(256) mem_reset_kernel(V* __restrict__ mem, con
                                                         I per_b, I total) {
     const I e = (I)blockIdx.x * 256 + threadIdx.x;
     if (e >= total) return;
-    if (flags[e / per_b]) mem[e] = V{};
+    if (TXL_BOUNDS(e / per_b < total / per_b, 206, e) && flags[e / per_b]) mem[e] = V{};
 }
 
 // Launches the roll with the widest vector the alignment allows and 32-bit
@@ -171,7 +183,8 @@ __global__ void __launch_bounds__(256) ring_push_kernel(V* __restrict__ ring, co
     const I b = br / (I)L;
     int pos = start + r;
     if (pos >= M) pos -= M;
-    ring[(b * (I)M + pos) * rowv + col] = hid[e];
+    const I ri = (b * (I)M + pos) * rowv + col;
+    if (TXL_BOUNDS(pos >= 0 && pos < M && ri < (total / ((I)L * rowv)) * (I)M * rowv, 207, ri)) ring[ri] = hid[e];
 }
 
 cudaError_t launch_ring_push(void* ring, const void* hid, int B, int L, int M, int start,
@@ -219,5 +232,7 @@ cudaError_t launch_mem_reset(void* mem, const unsigned char* flags, int B, long 
     if (per_b_bytes % 4 == 0 && a % 4 == 0) return go(uint32_t{});
     return go(uint16_t{});
 }
+
+TXL_BOUNDS_READER(bounds_word_mem_update)
 
 }  // namespace txl

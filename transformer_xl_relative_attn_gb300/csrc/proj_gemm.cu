@@ -322,7 +322,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                     float f[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) f[x] = __uint_as_float(v[x]);
-                    if (p.bias) {
+                    // bias: d columns; residual: laid out like the plain output [B, T_out, d]
+                    if (p.bias && TXL_BOUNDS(n + 32 <= p.d, 601, n)) {
                         const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + n);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -340,7 +341,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
 #pragma unroll
                         for (int x = 0; x < 32; ++x) f[x] = fmaxf(f[x], 0.f);
                     }
-                    if (p.resid) {
+                    if (p.resid && TXL_BOUNDS((dst - base) >= 0 && (dst - base) + 32 <= (long long)p.B * pr.T_out * p.d,
+                                              602, dst - base)) {
                         const uint4* r4 = reinterpret_cast<const uint4*>(p.resid + (dst - base));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -364,6 +366,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c16 = 4 * (cc & 1) + q;
+                    if (TXL_BOUNDS(slice + lane * 128 + ((c16 ^ (lane & 7)) << 4) + 16 <= s_base + C::SMEM_BYTES &&
+                                       slice >= s_base,
+                                   603, (long long)slice - s_base))
                     st_shared_v4(slice + lane * 128 + ((c16 ^ (lane & 7)) << 4),
                                  pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
                                  pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
@@ -618,5 +623,7 @@ cudaError_t launch_linear(const void* x, int x_heads, int B, int T, int K, const
         return launch_linear_bn<128>(x, x_heads, B, T, K, w, N, bias, resid, relu, out, status, stream);
     return launch_linear_bn<256>(x, x_heads, B, T, K, w, N, bias, resid, relu, out, status, stream);
 }
+
+TXL_BOUNDS_READER(bounds_word_proj_gemm)
 
 }  // namespace txl

@@ -35,6 +35,15 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 int* status, cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
 
+// first bounds violation recorded by each translation unit (bounds-checked
+// builds; 0 otherwise), read and cleared
+unsigned long long bounds_word_attn_simt();
+unsigned long long bounds_word_attn_tc();
+unsigned long long bounds_word_attn_bwd();
+unsigned long long bounds_word_mem_update();
+unsigned long long bounds_word_layer_norm();
+unsigned long long bounds_word_proj_gemm();
+
 }  // namespace txl
 
 namespace {
@@ -442,11 +451,31 @@ const char* txl_status_string(int status) {
         case TXL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case TXL_ERR_CUDA: return "CUDA runtime/driver call failed";
         case TXL_ERR_SCRATCH_LIMIT: return "call needs more scratch than the static no-alloc buffer";
+        case TXL_ERR_OUT_OF_BOUNDS: return "a bounds-checked kernel skipped an out-of-range access";
         default: return "unknown status";
     }
 }
 
 int txl_version(void) { return (1 << 16) | 0; }
+
+int txl_bounds_status(unsigned long long* first) {
+#ifndef TXL_CHECKED
+    if (first) *first = 0;
+    return TXL_ERR_UNSUPPORTED;  // this library was built without bounds checks
+#else
+    if (cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
+    const unsigned long long words[6] = {txl::bounds_word_attn_simt(), txl::bounds_word_attn_tc(),
+                                         txl::bounds_word_attn_bwd(), txl::bounds_word_mem_update(),
+                                         txl::bounds_word_layer_norm(), txl::bounds_word_proj_gemm()};
+    unsigned long long w = 0;
+    for (unsigned long long x : words) {
+        if (x == ~0ull) return TXL_ERR_CUDA;
+        if (!w && x) w = x;
+    }
+    if (first) *first = w;
+    return w ? TXL_ERR_OUT_OF_BOUNDS : TXL_OK;
+#endif
+}
 
 int txl_debug_inject(int kind) {
     if (kind < 0 || kind > 1) return TXL_ERR_INVALID_ARG;

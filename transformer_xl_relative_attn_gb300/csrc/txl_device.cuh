@@ -12,6 +12,40 @@
 
 namespace txl {
 
+// ---------------------------------------------------------------- bounds checks
+// Built with -DTXL_CHECKED, every computed global index and every computed
+// shared-memory address of the kernels goes through TXL_BOUNDS(cond, site,
+// index): an access whose condition fails is skipped (no trap) and the first
+// violation of the translation unit is recorded as (1 << 63) | (site << 40)
+// | (index & (2^40 - 1)) in a device word that txl_bounds_status() reads and
+// clears.  Without the flag the macro is the constant true and compiles away.
+#ifdef TXL_CHECKED
+static __device__ unsigned long long g_oob_word;
+__device__ __forceinline__ bool bounds_ok(bool ok, int site, long long index) {
+    if (!ok)
+        atomicCAS(&g_oob_word, 0ull,
+                  (1ull << 63) | ((unsigned long long)(site & 0x7FFFFF) << 40) |
+                      ((unsigned long long)index & 0xFFFFFFFFFFull));
+    return ok;
+}
+#define TXL_BOUNDS(cond, site, index) ::txl::bounds_ok((cond), (site), (long long)(index))
+// Host side of one translation unit's word: read it, clear it if set.
+#define TXL_BOUNDS_READER(fn)                                                            \
+    unsigned long long fn() {                                                            \
+        unsigned long long v = 0;                                                        \
+        if (cudaMemcpyFromSymbol(&v, g_oob_word, sizeof(v)) != cudaSuccess) return ~0ull; \
+        if (v) {                                                                         \
+            const unsigned long long z = 0;                                              \
+            cudaMemcpyToSymbol(g_oob_word, &z, sizeof(z));                               \
+        }                                                                                \
+        return v;                                                                        \
+    }
+#else
+#define TXL_BOUNDS(cond, site, index) true
+#define TXL_BOUNDS_READER(fn) \
+    unsigned long long fn() { return 0; }
+#endif
+
 // ---------------------------------------------------------------- host side
 // Launch set-up that the runtime keeps per device (a kernel's shared-memory
 // attribute) and properties that differ between devices (the SM count) are
