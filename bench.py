@@ -429,7 +429,8 @@ def measured_traffic(workload):
 
 def time_projections(wl, dev, stream, peaks):
     """The layer projections that produce the attention's inputs (txl_qkv_proj:
-    q from h, k/v from memory and h; txl_r_proj), timed alone for one layer of
+    q from h, k/v from memory and h; txl_r_proj; and both in one launch,
+    txl_qkvr_proj), timed alone for one layer of
     the workload in a captured graph (kernel time, not the host launch path).
     They are not part of the timed step: the step starts from projected
     inputs.  None when the sizes are outside the projection kernel's range."""
@@ -450,10 +451,11 @@ def time_projections(wl, dev, stream, peaks):
     v = torch.empty_like(k)
     r = torch.empty(M + L, H, dh, dtype=torch.bfloat16, device=dev)
     reps = 10
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
     with torch.cuda.stream(stream):
         txl.qkv_proj(h, mem, w, H, q, k, v)
         txl.r_proj(emb, wr, H, r)
+        txl.qkvr_proj(h, mem, w, emb, wr, H, q, k, v, r)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
@@ -464,11 +466,15 @@ def time_projections(wl, dev, stream, peaks):
         for _ in range(reps):
             txl.r_proj(emb, wr, H, r)
         ev[2].record()
+        for _ in range(reps):
+            txl.qkvr_proj(h, mem, w, emb, wr, H, q, k, v, r)
+        ev[3].record()
     graph.replay()
     torch.cuda.synchronize()
     txl.check_status()
     qkv_ms = ev[0].elapsed_time(ev[1]) / reps
     r_ms = ev[1].elapsed_time(ev[2]) / reps
+    qkvr_ms = ev[2].elapsed_time(ev[3]) / reps
     f_qkv = 2.0 * B * L * d * d + 2.0 * B * (M + L) * 2 * d * d
     f_r = 2.0 * (M + L) * d * d
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -476,7 +482,11 @@ def time_projections(wl, dev, stream, peaks):
         "qkv_proj": {"ms": round(qkv_ms, 5), "tflops": round(f_qkv / (qkv_ms * 1e-3) / 1e12, 2),
                      "frac": round(f_qkv / (qkv_ms * 1e-3) / 1e12 / peak, 4), "flops": f_qkv},
         "r_proj": {"ms": round(r_ms, 5), "tflops": round(f_r / (r_ms * 1e-3) / 1e12, 2),
-                   "frac": round(f_r / (r_ms * 1e-3) / 1e12 / peak, 4), "flops": f_r},
+                   "frac": round(f_r / (r_ms * 1e-3) / 1e12 / peak, 4), "flops": f_r,
+                   "note": "alone: a few tiles on 152 SMs (launch-bound)"},
+        "qkvr_proj": {"ms": round(qkvr_ms, 5), "tflops": round((f_qkv + f_r) / (qkvr_ms * 1e-3) / 1e12, 2),
+                      "frac": round((f_qkv + f_r) / (qkvr_ms * 1e-3) / 1e12 / peak, 4), "flops": f_qkv + f_r,
+                      "note": "q, k|v and r of one layer in one launch (txl_qkvr_proj)"},
         "peak": peak, "peak_source": "bf16_tflops (burst: kernels timed alone)",
         "measured": "one layer's projections, 10 back-to-back repeats in a CUDA graph",
     }

@@ -189,6 +189,20 @@ int txl_qkv_proj(const void* h, const void* mem, const void* w_qkv, int B, int L
                  int d_h, void* q, void* k, void* v, void* stream);
 
 /*
+ * txl_qkvr_proj: one layer's projections in one launch -- txl_qkv_proj_ring's
+ * q, k, v (same arguments and contract) and txl_r_proj's r_k = emb W_r^T over
+ * K = M + L rows of the position embedding emb [M+L, d] (same contract) --
+ * dealt from one tile list, so the small position projection rides in the
+ * q/k/v launch instead of occupying a few SMs of a launch of its own
+ * ("Transformer-XL模型 核心源码阅读笔记", RelPartialLearnableMultiHeadAttn.forward:
+ * w_heads = qkv_net(cat), r_head_k = r_net(r)).  r_k must not overlap any
+ * other argument (TXL_ERR_ALIAS).
+ */
+int txl_qkvr_proj(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+                  const void* w_qkv, const void* emb, const void* w_r, int B, int L, int M, int H,
+                  int d_h, void* q, void* k, void* v, void* r_k, void* stream);
+
+/*
  * txl_qkv_proj_ex: txl_qkv_proj with the layout of h and mem chosen per
  * argument.  TXL_LAYOUT_ROWS: [B, T, d] as above.  TXL_LAYOUT_HEADS:
  * [B, H, T, d_h], the layout txl_attn_fwd writes its output in, so a stack of

@@ -197,3 +197,23 @@ def test_checked_build_exports_the_same_symbols():
                          check=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
     assert set(txl.header_functions()) <= exported
+
+
+def test_qkvr_proj_rejects_bad_arguments(lib):
+    """txl_qkvr_proj: the q/k/v contract, the r_proj contract over M+L rows,
+    and no overlap between r_k and the other arguments."""
+    X = A + (1 << 32)
+
+    def call(**kw):
+        a = dict(h=A, mem=A + (1 << 28), w=A + (2 << 28), emb=A + (3 << 28), wr=A + (4 << 28), B=1, L=128,
+                 M=128, H=4, dh=64, q=O, k=O + (1 << 28), v=O + (2 << 28), r=X)
+        a.update(kw)
+        return lib.txl_qkvr_proj(a["h"], 0, a["mem"], 0, 0, a["w"], a["emb"], a["wr"], a["B"], a["L"], a["M"],
+                                 a["H"], a["dh"], a["q"], a["k"], a["v"], a["r"], None)
+    assert call(emb=None) == -1
+    assert call(r=None) == -1
+    assert call(L=100) == -2             # not a multiple of 128
+    assert call(dh=32) == -2
+    assert call(emb=A + (3 << 28) + 8) == -3
+    assert call(r=O) == -4               # r_k overlaps q
+    assert call(r=A) == -4               # r_k overlaps h

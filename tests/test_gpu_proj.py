@@ -72,3 +72,30 @@ def test_projections_reject_unsupported_sizes():
     with pytest.raises(txl.TxlError) as e:
         txl.qkv_proj(h, mem, w, H)
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("B,L,M,H,h_heads,mem_start", [
+    (22, 512, 512, 8, False, 0),    # the base-size workload's layer
+    (1, 256, 0, 4, False, 0),       # no memory yet: r over L rows only
+    (2, 128, 384, 16, True, 256),   # heads-layout input, ring memory read from row 256
+])
+def test_qkvr_proj_is_qkv_proj_and_r_proj_in_one_launch(B, L, M, H, h_heads, mem_start):
+    """txl_qkvr_proj writes exactly (bit for bit) what txl_qkv_proj_ring and
+    txl_r_proj write separately (same tiles, same accumulation order), and
+    r_k matches the oracle's projection."""
+    d = H * 64
+    h, mem = rand(B, L, d, seed=11), rand(B, M, d, seed=12)
+    w = rand(3 * d, d, std=0.03, seed=13)
+    emb, wr = rand(M + L, d, seed=14), rand(d, d, std=0.03, seed=15)
+    hd = h.cuda()
+    if h_heads:
+        hd = hd.view(B, L, H, 64).permute(0, 2, 1, 3).contiguous()
+    q0, k0, v0 = txl.qkv_proj(hd, mem.cuda(), w.cuda(), H, mem_start=mem_start)
+    r0 = txl.r_proj(emb.cuda(), wr.cuda(), H)
+    q1, k1, v1, r1 = txl.qkvr_proj(hd, mem.cuda(), w.cuda(), emb.cuda(), wr.cuda(), H, mem_start=mem_start)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    for a, b in ((q0, q1), (k0, k1), (v0, v1), (r0, r1)):
+        assert torch.equal(a, b)
+    ref = oracle.r_proj(emb, wr, H)
+    assert np.abs(r1.float().cpu().double().numpy() - ref).max() <= tol(ref)

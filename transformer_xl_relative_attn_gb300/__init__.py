@@ -8,6 +8,7 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
     mem_update, mem_reset                         Tail_M memory roll (ext_len), per-row reset, in place
     mem_ring_push                                 ring-buffer memory update (qkv_proj reads the ring)
     qkv_proj, r_proj                              head-split input projections (tensor cores)
+    qkvr_proj                                     both in one launch
     linear, layer_norm                            o_net / feed-forward GEMMs, fused residual LayerNorm
     sync_status, check_status                     device status word
     bounds_status                                 first out-of-range access (bounds-checked build)
@@ -17,12 +18,12 @@ Public API (all computation runs in libtxl.so's CUDA kernels):
 """
 from ._lib import (TXL_BF16, TXL_F32, TxlError, attn_bwd, attn_fwd, attn_fwd_noalloc, attn_fwd_ws,
                    attn_workspace_bytes, bounds_status,
-                   check_status, debug_inject, header_functions, layer_norm, linear, load, mem_reset, mem_ring_push, mem_update, qkv_proj, r_proj,
+                   check_status, debug_inject, header_functions, layer_norm, linear, load, mem_reset, mem_ring_push, mem_update, qkv_proj, qkvr_proj, r_proj,
                    status_string,
                    sync_status, version, LIB_PATH)
 from .driver import AttnStack, DecoderStack, SegmentDriver
 
 __all__ = ["TXL_BF16", "TXL_F32", "TxlError", "attn_bwd", "attn_fwd", "attn_fwd_noalloc", "attn_fwd_ws",
            "attn_workspace_bytes", "bounds_status",
-           "check_status", "debug_inject", "header_functions", "layer_norm", "linear", "load", "mem_reset", "mem_ring_push", "mem_update", "qkv_proj", "r_proj",
+           "check_status", "debug_inject", "header_functions", "layer_norm", "linear", "load", "mem_reset", "mem_ring_push", "mem_update", "qkv_proj", "qkvr_proj", "r_proj",
            "status_string", "sync_status", "version", "SegmentDriver", "AttnStack", "DecoderStack", "LIB_PATH"]

@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
         lib.txl_qkv_proj_ring.restype = i
         lib.txl_mem_ring_push.argtypes = [vp, vp] + [i] * 5 + [ctypes.POINTER(ctypes.c_int), i, vp]
         lib.txl_mem_ring_push.restype = i
+        lib.txl_qkvr_proj.argtypes = [vp, i, vp, i, i, vp, vp, vp] + [i] * 5 + [vp] * 5
+        lib.txl_qkvr_proj.restype = i
         lib.txl_r_proj.argtypes = [vp, vp] + [i] * 3 + [vp, vp]
         lib.txl_r_proj.restype = i
         lib.txl_attn_workspace_bytes.argtypes = [i] * 6
@@ -263,13 +265,9 @@ def attn_fwd_noalloc(q, k, v, r_k, u, vb, scale=None, out=None, stream=None):
     return out
 
 
-def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0):
-    """txl_qkv_proj_ex: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
-    h is [B, L, d] (rows) or [B, H, L, d_h] (heads: an attention output),
-    mem likewise [B, M, d] or [B, H, M, d_h] (M may be 0); w_qkv [3d, d]; bf16
-    CUDA tensors.  mem_start: mem is a ring whose logical row 0 is stored at
-    row mem_start (txl_qkv_proj_ring).  Returns (q [B, H, L, d_h], k, v
-    [B, H, M+L, d_h])."""
+def _qkv_args(h, mem, w_qkv, H, q, k, v):
+    """Shapes, layouts and outputs of the q/k/v projections (txl_qkv_proj_ex's
+    contract); returns (q, k, v, (B, L, M))."""
     if h.dim() == 3:
         B, L, d = h.shape
         h_layout = 0
@@ -284,10 +282,10 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0)
     dh = d // H
     if mem.dim() == 3:
         M = mem.shape[1]
-        mem_layout, mem_shape = 0, (B, M, d)
+        mem_shape = (B, M, d)
     elif mem.dim() == 4:
         M = mem.shape[2]
-        mem_layout, mem_shape = 1, (B, H, M, dh)
+        mem_shape = (B, H, M, dh)
     else:
         raise ValueError("mem must be [B, M, d] or [B, H, M, d_h]")
     _need(h, "h", (B, L, d) if h_layout == 0 else (B, H, L, dh), torch.bfloat16)
@@ -303,12 +301,53 @@ def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0)
     _need(q, "q", (B, H, L, dh), torch.bfloat16, h.device)
     _need(k, "k", (B, H, M + L, dh), torch.bfloat16, h.device)
     _need(v, "v", (B, H, M + L, dh), torch.bfloat16, h.device)
-    rc = _invoke(h.device, "txl_qkv_proj_ring", h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0, mem_layout,
-                                  int(mem_start), w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(),
-                                  k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
+    return q, k, v, (B, L, M)
+
+
+def qkv_proj(h, mem, w_qkv, H, q=None, k=None, v=None, stream=None, mem_start=0):
+    """txl_qkv_proj_ex: q = h W_q^T, k/v = [mem; h] W_{k,v}^T split into heads.
+    h is [B, L, d] (rows) or [B, H, L, d_h] (heads: an attention output),
+    mem likewise [B, M, d] or [B, H, M, d_h] (M may be 0); w_qkv [3d, d]; bf16
+    CUDA tensors.  mem_start: mem is a ring whose logical row 0 is stored at
+    row mem_start (txl_qkv_proj_ring).  Returns (q [B, H, L, d_h], k, v
+    [B, H, M+L, d_h])."""
+    q, k, v, (B, L, M) = _qkv_args(h, mem, w_qkv, H, q, k, v)
+    dh = q.shape[3]
+    h_layout = 0 if h.dim() == 3 else 1
+    mem_layout = 0 if mem.dim() == 3 else 1
+    rc = _invoke(h.device, "txl_qkv_proj_ring", h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0,
+                 mem_layout, int(mem_start), w_qkv.data_ptr(), B, L, M, H, dh, q.data_ptr(),
+                 k.data_ptr(), v.data_ptr(), _stream(stream, h.device))
     if rc != 0:
         raise TxlError(rc, "txl_qkv_proj_ring")
     return q, k, v
+
+
+def qkvr_proj(h, mem, w_qkv, emb, w_r, H, q=None, k=None, v=None, r_k=None, stream=None, mem_start=0):
+    """txl_qkvr_proj: qkv_proj's q, k, v and r_proj's r_k = emb W_r^T in one
+    launch; emb [M+L, d] (M+L rows of the position embedding), w_r [d, d].
+    Returns (q, k, v, r_k)."""
+    d = w_qkv.shape[1]
+    dh = d // H
+    if emb.dim() != 2 or emb.shape[1] != d:
+        raise ValueError("emb must be [M+L, d]")
+    Kr = emb.shape[0]
+    _need(emb, "emb", (Kr, d), torch.bfloat16, h.device)
+    _need(w_r, "w_r", (d, d), torch.bfloat16, h.device)
+    if r_k is None:
+        r_k = torch.empty((Kr, H, dh), dtype=torch.bfloat16, device=h.device)
+    _need(r_k, "r_k", (Kr, H, dh), torch.bfloat16, h.device)
+    q, k, v, (B, L, M) = _qkv_args(h, mem, w_qkv, H, q, k, v)
+    if Kr != M + L:
+        raise ValueError(f"emb has {Kr} rows, expected M+L = {M + L}")
+    h_layout = 0 if h.dim() == 3 else 1
+    mem_layout = 0 if mem.dim() == 3 else 1
+    rc = _invoke(h.device, "txl_qkvr_proj", h.data_ptr(), h_layout, mem.data_ptr() if M > 0 else 0,
+                 mem_layout, int(mem_start), w_qkv.data_ptr(), emb.data_ptr(), w_r.data_ptr(), B, L, M, H,
+                 dh, q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), _stream(stream, h.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_qkvr_proj")
+    return q, k, v, r_k
 
 
 def linear(x, w, bias=None, resid=None, relu=False, out=None, stream=None):

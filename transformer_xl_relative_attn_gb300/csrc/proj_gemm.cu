@@ -11,8 +11,9 @@
 // GEMM, so no [mem; h] concatenation is formed, and the epilogue writes each
 // 64-column head slice straight into the head-split layout.
 //
-// One launch may carry two GEMMs (q from h, and k|v from [mem; h]) dealt from
-// one tile list, so the smaller one does not leave a partial round of its own.
+// One launch may carry up to three GEMMs (q from h, k|v from [mem; h], and r
+// from the position embedding) dealt from one tile list, so the smaller ones
+// do not leave partial rounds (or, for r, a launch) of their own.
 // One CTA per SM walks output tiles of 128 rows x 256 columns; K (= d) is
 // streamed in 64-element steps through a 4-stage TMA ring (A tile 16 KB, B tile
 // 32 KB, 128B swizzle).  Roles (384 threads): warp 0 lane 0 issues the TMA
@@ -87,6 +88,8 @@ struct Cfg {
 // One GEMM of the launch: per batch row, Ta rows of source a (the memory)
 // then Tb rows of source b (current), times the problem's weights.
 struct PgProblem {
+    int B;          // batch rows of the problem
+    int plain;      // 1: outputs are [rows, d] row-major (no head split)
     int Ta, Tb;     // rows per batch from source a, then source b (Ta a multiple of BM)
     int a_start;    // source a is a ring: logical row t is stored at row (a_start + t) % Ta
     int N;          // output columns (a multiple of BN)
@@ -95,13 +98,13 @@ struct PgProblem {
     __nv_bfloat16* out[3];  // output column c -> tensor c / d
 };
 
+constexpr int kMaxProblems = 3;
+
 struct PgParams {
-    int B;          // batch rows
     int K;          // reduction length (= d)
     int d, H, dh;   // output column c -> head (c % d) / dh, element c % dh
-    int plain;      // 1: outputs are [rows, d] row-major (no head split)
-    int n_tiles;    // tiles of problem 0, then of problem 1
-    PgProblem pr[2];
+    int n_tiles;    // tiles of problem 0, then of problem 1, then of problem 2
+    PgProblem pr[kMaxProblems];
     int* status;
     // plain outputs only: out = act(acc + bias[col]) + resid (resid laid
     // out like the output); null / 0 to skip
@@ -110,11 +113,16 @@ struct PgParams {
     int relu;
 };
 
+// Input tensor maps of problem g: source a, source b, weights.
+struct PgIn {
+    CUtensorMap m[kMaxProblems][3];
+};
+
 // Output tensor maps: problem g, output tensor o, viewed as (element of a
 // 64-column slice, row t, slice (head, or 64-column chunk of a row-major
 // output), batch row b); box 64 x 32 rows.
 struct PgOut {
-    CUtensorMap m[2][3];
+    CUtensorMap m[kMaxProblems][3];
 };
 
 struct PgShared {
@@ -127,13 +135,20 @@ struct PgShared {
     int abort;
 };
 
-// Tile w of the launch: problem 0's tiles, then problem 1's; within a
-// problem the column tile runs fastest, then the row tile, then the batch row.
+// Tile w of the launch: problem 0's tiles, then problem 1's, then 2's; within
+// a problem the column tile runs fastest, then the row tile, then the batch row.
 template <int BN>
 __device__ __forceinline__ int pg_tile(const PgParams& p, int w, int& b, int& t0, int& n0) {
-    const int g = w < p.pr[0].tiles ? 0 : 1;
+    int g = 0;
+    if (w >= p.pr[0].tiles) {
+        w -= p.pr[0].tiles;
+        g = 1;
+        if (w >= p.pr[1].tiles) {
+            w -= p.pr[1].tiles;
+            g = 2;
+        }
+    }
     const PgProblem& pr = p.pr[g];
-    if (g) w -= p.pr[0].tiles;
     const int nt = w % pr.n_nt, rest = w / pr.n_nt;
     n0 = nt * BN;
     t0 = (rest % pr.n_rt) * pg::BM;
@@ -143,10 +158,7 @@ __device__ __forceinline__ int pg_tile(const PgParams& p, int w, int& b, int& t0
 
 template <int BN_>
 __global__ void __launch_bounds__(pg::NTHREADS, 1)
-proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
-                 const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmA1,
-                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmW1,
-                 const __grid_constant__ PgOut outm, const PgParams p) {
+proj_gemm_kernel(const __grid_constant__ PgIn inm, const __grid_constant__ PgOut outm, const PgParams p) {
     using namespace pg;
     using C = Cfg<BN_>;
     constexpr int BN = C::BN, STAGES = C::STAGES;
@@ -179,12 +191,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
         mbar_init(&sh->drain, 1);
         sh->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmB0);
-        tma_prefetch_desc(&tmW0);
-        tma_prefetch_desc(&tmA1);
-        tma_prefetch_desc(&tmB1);
-        tma_prefetch_desc(&tmW1);
+        for (int g = 0; g < kMaxProblems; ++g)
+            if (p.pr[g].tiles > 0)
+                for (int m = 0; m < 3; ++m) tma_prefetch_desc(&inm.m[g][m]);
     }
     tc_fence_before();
     __syncthreads();
@@ -203,10 +212,10 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                 const int g = pg_tile<BN>(p, w, b, t0, n0);
                 const int Ta = p.pr[g].Ta;
                 // a row tile lies wholly in one source (Ta is a multiple of BM)
-                const CUtensorMap* mA = t0 < Ta ? (g ? &tmA1 : &tmA0) : (g ? &tmB1 : &tmB0);
+                const CUtensorMap* mA = t0 < Ta ? &inm.m[g][0] : &inm.m[g][1];
                 // a_start and t0 are multiples of BM, so a ring tile never wraps
                 const int ta = t0 < Ta ? (t0 + p.pr[g].a_start) % Ta : t0 - Ta;
-                const CUtensorMap* mW = g ? &tmW1 : &tmW0;
+                const CUtensorMap* mW = &inm.m[g][2];
                 for (int k = 0; k < ksteps; ++k, ++c) {
                     const int s = c % STAGES;
                     if (c >= STAGES && !mbar_wait(&sh->empty[s], ((c / STAGES) & 1) ^ 1,
@@ -311,7 +320,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                 const int o = n / p.d, nd = n - o * p.d;
                 __nv_bfloat16* const base = o == 0 ? pr.out[0] : (o == 1 ? pr.out[1] : pr.out[2]);
                 __nv_bfloat16* dst;
-                if (p.plain) {
+                if (pr.plain) {
                     dst = base + ((size_t)b * pr.T_out + t) * p.d + nd;
                 } else {
                     const int head = nd / p.dh, e = nd - head * p.dh;
@@ -341,7 +350,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
 #pragma unroll
                         for (int x = 0; x < 32; ++x) f[x] = fmaxf(f[x], 0.f);
                     }
-                    if (p.resid && TXL_BOUNDS((dst - base) >= 0 && (dst - base) + 32 <= (long long)p.B * pr.T_out * p.d,
+                    if (p.resid && TXL_BOUNDS((dst - base) >= 0 && (dst - base) + 32 <= (long long)pr.B * pr.T_out * p.d,
                                               602, dst - base)) {
                         const uint4* r4 = reinterpret_cast<const uint4*>(p.resid + (dst - base));
 #pragma unroll
@@ -381,7 +390,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
                     if (lane == 0) {
                         const int ns = n - 32;  // the slice's first column
                         const int os = ns / p.d, nds = ns - os * p.d;
-                        tma_store_4d(&outm.m[g][os], slice, 0, t0 + 32 * wq, p.plain ? nds / 64 : nds / p.dh, b);
+                        tma_store_4d(&outm.m[g][os], slice, 0, t0 + 32 * wq, pr.plain ? nds / 64 : nds / p.dh, b);
                         store_pending = true;
                     }
                 }
@@ -430,10 +439,8 @@ static bool pg_encode(CUtensorMap* map, const void* base, int rank, const cuuint
 // Launch with programmatic stream serialisation (the kernel waits for the
 // previous kernel of the stream before its first global access).
 template <typename Kern>
-static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_t stream, const CUtensorMap& a0,
-                                 const CUtensorMap& b0, const CUtensorMap& w0, const CUtensorMap& a1,
-                                 const CUtensorMap& b1, const CUtensorMap& w1, const PgOut& outm,
-                                 const PgParams& p) {
+static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_t stream, const PgIn& inm,
+                                 const PgOut& outm, const PgParams& p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(pg::NTHREADS);
@@ -444,7 +451,7 @@ static cudaError_t launch_pg_pdl(Kern kern, int grid, uint32_t smem, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a0, b0, w0, a1, b1, w1, outm, p);
+    return cudaLaunchKernelEx(&cfg, kern, inm, outm, p);
 }
 
 // Output map of one bf16 tensor: heads [B, H, T, dh] (dh = 64) or row-major
@@ -475,16 +482,14 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         });
         if (e != cudaSuccess) return e;
     }
-    if (n_gemm < 1 || n_gemm > 2) return cudaErrorInvalidValue;
-    CUtensorMap maps[2][3];  // per problem: source a, source b, weights
+    if (n_gemm < 1 || n_gemm > kMaxProblems) return cudaErrorInvalidValue;
+    PgIn inm;  // per problem: source a, source b, weights
     PgOut outm;
     PgParams p;
-    p.B = B;
     p.K = K;
     p.d = d;
     p.H = H;
     p.dh = dh;
-    p.plain = plain;
     p.status = status;
     p.bias = nullptr;
     p.resid = nullptr;
@@ -492,8 +497,8 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     // Both layouts as one 4-D view (element, row t, 64-column chunk k, batch
     // row b), so the kernel loads chunk k of rows t0.. with coordinates
     // (0, t0, k, b) either way.
-    auto encode_src = [&](CUtensorMap* map, const void* src, int T, int heads) {
-        const cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)(K / BK), (cuuint64_t)B};
+    auto encode_src = [&](CUtensorMap* map, const void* src, int T, int heads, int Bp) {
+        const cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)(K / BK), (cuuint64_t)Bp};
         const cuuint64_t row = heads ? (cuuint64_t)BK * 2 : (cuuint64_t)K * 2;
         const cuuint64_t chunk = heads ? (cuuint64_t)T * BK * 2 : (cuuint64_t)BK * 2;
         const cuuint64_t strides[3] = {row, chunk, (cuuint64_t)T * K * 2};
@@ -501,21 +506,25 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         return pg_encode(map, src, 4, dims, strides, box);
     };
     long long total = 0;
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < kMaxProblems; ++g) {
         const ProjGemm& q = gm[g < n_gemm ? g : 0];
-        if (!encode_src(&maps[g][1], q.b_src, q.Tb, q.b_heads)) return cudaErrorInvalidValue;
+        const int Bp = q.B > 0 ? q.B : B;
+        const int plain_g = q.plain >= 0 ? q.plain : plain;
+        if (!encode_src(&inm.m[g][1], q.b_src, q.Tb, q.b_heads, Bp)) return cudaErrorInvalidValue;
         if (q.Ta > 0) {
-            if (!encode_src(&maps[g][0], q.a_src, q.Ta, q.a_heads)) return cudaErrorInvalidValue;
+            if (!encode_src(&inm.m[g][0], q.a_src, q.Ta, q.a_heads, Bp)) return cudaErrorInvalidValue;
         } else {
-            maps[g][0] = maps[g][1];  // no memory rows: every row tile comes from b_src
+            inm.m[g][0] = inm.m[g][1];  // no memory rows: every row tile comes from b_src
         }
         {
             const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)q.N};
             const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
             const cuuint32_t box[2] = {BK, BN};
-            if (!pg_encode(&maps[g][2], q.w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+            if (!pg_encode(&inm.m[g][2], q.w, 2, dims, strides, box)) return cudaErrorInvalidValue;
         }
         PgProblem& pr = p.pr[g];
+        pr.B = Bp;
+        pr.plain = plain_g;
         pr.Ta = q.Ta;
         pr.Tb = q.Tb;
         pr.a_start = q.a_start;
@@ -523,7 +532,7 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         pr.T_out = q.T_out;
         pr.n_rt = (q.Ta + q.Tb) / BM;
         pr.n_nt = q.N / BN;
-        const long long tiles = g < n_gemm ? (long long)B * pr.n_rt * pr.n_nt : 0;
+        const long long tiles = g < n_gemm ? (long long)Bp * pr.n_rt * pr.n_nt : 0;
         pr.tiles = (int)(tiles > 0x7FFFFFFFll ? 0 : tiles);
         total += tiles;
         for (int o = 0; o < 3; ++o) pr.out[o] = static_cast<__nv_bfloat16*>(q.out[o]);
@@ -532,7 +541,7 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
         const int n_out = q.N / d;
         for (int o = 0; o < 3; ++o) {
             if (o < n_out) {
-                if (!pg_encode_out(&outm.m[g][o], q.out[o], B, q.T_out, d, !plain)) return cudaErrorInvalidValue;
+                if (!pg_encode_out(&outm.m[g][o], q.out[o], Bp, q.T_out, d, !plain_g)) return cudaErrorInvalidValue;
             } else {
                 outm.m[g][o] = outm.m[g][0];
             }
@@ -541,8 +550,7 @@ cudaError_t launch_proj_gemm(const ProjGemm* gm, int n_gemm, int B, int K, int d
     if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_tiles = (int)total;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    return launch_pg_pdl(proj_gemm_kernel<256>, grid, C::SMEM_BYTES, stream, maps[0][0], maps[0][1], maps[0][2],
-                         maps[1][0], maps[1][1], maps[1][2], outm, p);
+    return launch_pg_pdl(proj_gemm_kernel<256>, grid, C::SMEM_BYTES, stream, inm, outm, p);
 }
 
 // A plain Linear over rows of x (layout 0: [B, T, K]; 1: [B, K / 64, T, 64]):
@@ -562,7 +570,8 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
         });
         if (e != cudaSuccess) return e;
     }
-    CUtensorMap maps[3];
+    PgIn inm;
+    CUtensorMap* maps = inm.m[0];
     {
         const cuuint64_t dims[4] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)(K / BK), (cuuint64_t)B};
         const cuuint64_t row = x_heads ? (cuuint64_t)BK * 2 : (cuuint64_t)K * 2;
@@ -579,17 +588,17 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
     }
     maps[1] = maps[0];
     PgParams p;
-    p.B = B;
     p.K = K;
     p.d = N;   // one output, row-major [B, T, N]
     p.H = 1;
     p.dh = N;
-    p.plain = 1;
     p.status = status;
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.resid = static_cast<const __nv_bfloat16*>(resid);
     p.relu = relu;
     PgProblem& pr = p.pr[0];
+    pr.B = B;
+    pr.plain = 1;
     pr.Ta = 0;
     pr.Tb = T;
     pr.a_start = 0;
@@ -604,13 +613,15 @@ static cudaError_t launch_linear_bn(const void* x, int x_heads, int B, int T, in
     pr.out[1] = pr.out[2] = nullptr;
     PgOut outm;
     if (!pg_encode_out(&outm.m[0][0], out, B, T, N, 0)) return cudaErrorInvalidValue;
-    for (int i = 0; i < 6; ++i) (&outm.m[0][0])[i] = outm.m[0][0];
-    p.pr[1] = pr;
-    p.pr[1].tiles = 0;
+    for (int i = 0; i < kMaxProblems * 3; ++i) (&outm.m[0][0])[i] = outm.m[0][0];
+    for (int g = 1; g < kMaxProblems; ++g) {
+        for (int m = 0; m < 3; ++m) inm.m[g][m] = inm.m[0][m];
+        p.pr[g] = pr;
+        p.pr[g].tiles = 0;
+    }
     p.n_tiles = (int)tiles;
     const int grid = p.n_tiles < pg_num_sms() ? p.n_tiles : pg_num_sms();
-    return launch_pg_pdl(proj_gemm_kernel<BN_>, grid, C::SMEM_BYTES, stream, maps[0], maps[1], maps[2], maps[0],
-                         maps[1], maps[2], outm, p);
+    return launch_pg_pdl(proj_gemm_kernel<BN_>, grid, C::SMEM_BYTES, stream, inm, outm, p);
 }
 
 // 256-column tiles unless that leaves fewer than two tiles per SM (then

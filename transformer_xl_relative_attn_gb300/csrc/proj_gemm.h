@@ -17,11 +17,14 @@ struct ProjGemm {
     int T_out;             // rows per (batch row, head) of the outputs
     void* out[3];          // output column c -> out[c / d]
     int a_start;           // a_src is a ring of Ta rows starting at this row (a multiple of 128)
+    int B = 0;             // batch rows of this problem (0: the launch's B)
+    int plain = -1;        // -1: the launch's layout; 1: outputs row-major [rows, d]; 0: [B, H, T_out, dh]
 };
 
-// One launch of up to two projection GEMMs: out[c / d] <- rows of [a_src;
+// One launch of up to three projection GEMMs: out[c / d] <- rows of [a_src;
 // b_src] (per batch row: Ta rows of a_src, then Tb rows of b_src) times w^T.
-// plain = 1 writes row-major [rows, d] outputs, otherwise [B, H, T_out, dh].
+// plain = 1 writes row-major [rows, d] outputs, otherwise [B, H, T_out, dh]
+// (a problem may override B and the layout).
 // Requires Ta, Tb multiples of 128 (Ta may be 0), K a multiple of 64, N a
 // multiple of 256, N / d <= 3.  cudaErrorInvalidValue: a tensor map could not
 // be encoded.

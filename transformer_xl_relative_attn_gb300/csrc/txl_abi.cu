@@ -342,9 +342,13 @@ int txl_qkv_proj_ex(const void* h, int h_layout, const void* mem, int mem_layout
     return txl_qkv_proj_ring(h, h_layout, mem, mem_layout, 0, w_qkv, B, L, M, H, d_h, q, k, v, stream);
 }
 
-int txl_qkv_proj_ring(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
-                      const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
-                      void* v, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host validation of the q/k/v projections (txl_qkv_proj_ring's contract).
+int check_qkv(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+              const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k, void* v) {
     if (!h || !w_qkv || !q || !k || !v || (M > 0 && !mem)) return TXL_ERR_INVALID_ARG;
     const auto layout_ok = [](int l) { return l == TXL_LAYOUT_ROWS || l == TXL_LAYOUT_HEADS; };
     if (!layout_ok(h_layout) || !layout_ok(mem_layout)) return TXL_ERR_INVALID_ARG;
@@ -370,22 +374,11 @@ int txl_qkv_proj_ring(const void* h, int h_layout, const void* mem, int mem_layo
         for (int o2 = o + 1; o2 < 3; ++o2)
             if (overlap(outs[o], nout[o], outs[o2], nout[o2])) return TXL_ERR_ALIAS;
     }
-    int* status = dev_status_ptr();
-    if (!status) return TXL_ERR_CUDA;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned char* w = static_cast<const unsigned char*>(w_qkv);
-    // one launch: q from h and W_q; k, v from [mem; h] and the W_k, W_v rows
-    const int hh = h_layout == TXL_LAYOUT_HEADS, mh = mem_layout == TXL_LAYOUT_HEADS;
-    const txl::ProjGemm gm[2] = {
-        {nullptr, h, 0, L, 0, hh, w, (int)d, L, {q, nullptr, nullptr}},
-        {M > 0 ? mem : nullptr, h, M, L, mh, hh, w + (size_t)d * d * 2, (int)(2 * d), M + L,
-         {k, v, nullptr}, mem_start}};
-    cudaError_t e = txl::launch_proj_gemm(gm, 2, B, (int)d, (int)d, H, d_h, 0, status, st);
-    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
-    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+    return TXL_OK;
 }
 
-int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream) {
+// Host validation of the position projection (txl_r_proj's contract).
+int check_r(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k) {
     if (!emb || !w_r || !r_k || K <= 0 || H <= 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
     if (d_h != 64 || H % 4 != 0 || K % 128 != 0) return TXL_ERR_UNSUPPORTED;
     const long long d = (long long)H * d_h;
@@ -393,13 +386,81 @@ int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_
     if (!aligned16(emb) || !aligned16(w_r) || !aligned16(r_k)) return TXL_ERR_MISALIGNED;
     const size_t nr = (size_t)K * d * 2;
     if (overlap(r_k, nr, emb, nr) || overlap(r_k, nr, w_r, (size_t)d * d * 2)) return TXL_ERR_ALIAS;
+    return TXL_OK;
+}
+
+// The q and k|v problems of one layer's projection launch.
+void qkv_problems(txl::ProjGemm* gm, const void* h, int h_layout, const void* mem, int mem_layout,
+                  int mem_start, const void* w_qkv, int L, int M, long long d, void* q, void* k, void* v) {
+    const unsigned char* w = static_cast<const unsigned char*>(w_qkv);
+    const int hh = h_layout == TXL_LAYOUT_HEADS, mh = mem_layout == TXL_LAYOUT_HEADS;
+    gm[0] = {nullptr, h, 0, L, 0, hh, w, (int)d, L, {q, nullptr, nullptr}};
+    gm[1] = {M > 0 ? mem : nullptr, h, M, L, mh, hh, w + (size_t)d * d * 2, (int)(2 * d), M + L,
+             {k, v, nullptr}, mem_start};
+}
+
+int launch_status(cudaError_t e) {
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // a tensor map could not be encoded
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int txl_qkv_proj_ring(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+                      const void* w_qkv, int B, int L, int M, int H, int d_h, void* q, void* k,
+                      void* v, void* stream) {
+    const int rc = check_qkv(h, h_layout, mem, mem_layout, mem_start, w_qkv, B, L, M, H, d_h, q, k, v);
+    if (rc != TXL_OK) return rc;
     int* status = dev_status_ptr();
     if (!status) return TXL_ERR_CUDA;
+    // one launch: q from h and W_q; k, v from [mem; h] and the W_k, W_v rows
+    txl::ProjGemm gm[2];
+    qkv_problems(gm, h, h_layout, mem, mem_layout, mem_start, w_qkv, L, M, (long long)H * d_h, q, k, v);
+    return launch_status(txl::launch_proj_gemm(gm, 2, B, H * d_h, H * d_h, H, d_h, 0, status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int txl_qkvr_proj(const void* h, int h_layout, const void* mem, int mem_layout, int mem_start,
+                  const void* w_qkv, const void* emb, const void* w_r, int B, int L, int M, int H,
+                  int d_h, void* q, void* k, void* v, void* r_k, void* stream) {
+    int rc = check_qkv(h, h_layout, mem, mem_layout, mem_start, w_qkv, B, L, M, H, d_h, q, k, v);
+    if (rc != TXL_OK) return rc;
+    rc = check_r(emb, w_r, M + L, H, d_h, r_k);
+    if (rc != TXL_OK) return rc;
+    const long long d = (long long)H * d_h;
+    const size_t nr = (size_t)(M + L) * d * 2, nq = (size_t)B * L * d * 2, nkv = (size_t)B * (M + L) * d * 2;
+    const size_t nh = nq, nm = (size_t)B * M * d * 2, nw = (size_t)3 * d * d * 2;
+    // r_k overlaps no other output and no input of the q/k/v problems
+    if (overlap(r_k, nr, q, nq) || overlap(r_k, nr, k, nkv) || overlap(r_k, nr, v, nkv) ||
+        overlap(r_k, nr, h, nh) || overlap(r_k, nr, w_qkv, nw) || (M > 0 && overlap(r_k, nr, mem, nm)))
+        return TXL_ERR_ALIAS;
+    const void* outs[3] = {q, k, v};
+    const size_t nout[3] = {nq, nkv, nkv};
+    for (int o = 0; o < 3; ++o)
+        if (overlap(outs[o], nout[o], emb, nr) || overlap(outs[o], nout[o], w_r, (size_t)d * d * 2))
+            return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    // one launch: q, k|v as in txl_qkv_proj_ring, and r from the position
+    // embedding (one batch row, row-major output)
+    txl::ProjGemm gm[3];
+    qkv_problems(gm, h, h_layout, mem, mem_layout, mem_start, w_qkv, L, M, d, q, k, v);
+    gm[2] = {nullptr, emb, 0, M + L, 0, 0, w_r, (int)d, M + L, {r_k, nullptr, nullptr}, 0, 1, 1};
+    return launch_status(txl::launch_proj_gemm(gm, 3, B, (int)d, (int)d, H, d_h, 0, status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int txl_r_proj(const void* emb, const void* w_r, int K, int H, int d_h, void* r_k, void* stream) {
+    const int rc = check_r(emb, w_r, K, H, d_h, r_k);
+    if (rc != TXL_OK) return rc;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    const long long d = (long long)H * d_h;
     const txl::ProjGemm gm = {nullptr, emb, 0, K, 0, 0, w_r, (int)d, K, {r_k, nullptr, nullptr}};
-    cudaError_t e = txl::launch_proj_gemm(&gm, 1, 1, (int)d, (int)d, H, d_h, 1, status,
-                                          static_cast<cudaStream_t>(stream));
-    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
-    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+    return launch_status(txl::launch_proj_gemm(&gm, 1, 1, (int)d, (int)d, H, d_h, 1, status,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 int txl_linear(const void* x, int x_layout, int B, int T, int K, const void* w, int N,
