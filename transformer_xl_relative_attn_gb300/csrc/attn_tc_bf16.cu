@@ -969,29 +969,20 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (landed < issued) drain_wait(&sh->q_full, (issued - 1) & 1, p.status);
         __syncwarp();
     } else if (warp == 9) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------------ TMA producers
+        // Lane 0 streams the K/V stages (and warms L2 ahead of them), lane 1
+        // the R boxes, each gated only by its own ring: a K/V stage still
+        // held by P V does not hold back the next R box, nor the reverse.
+        // The prologue ran on lane 0: every lane learns what it issued.
+        pre_kv = __shfl_sync(0xffffffffu, pre_kv, 0);
+        pre_r = __shfl_sync(0xffffffffu, pre_r, 0);
         if (lane == 0) {
-            int kvc = pre_kv, rc = pre_r;  // loads issued into each ring (item 0's first in the prologue)
+            int kvc = pre_kv;  // K/V stages issued (item 0's first in the prologue)
             bool ok = true;
             Item it;
             for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
                 const int nkv = (it.ntiles + 1) >> 1;  // K/V stages of this item
-                const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
-                int rb = k == 0 ? pre_r : 0;
-                for (int u = 0; ok && u < nkv; ++u) {
-                    // R boxes that S(2u) and S(2u+1) read, then the K/V stage
-                    for (; rb <= u + 1 && rb < nrb; ++rb, ++rc) {
-                        const int s = rc % R_STAGES;
-                        if (rc >= R_STAGES && !mbar_wait(&sh->r_empty[s], ((rc / R_STAGES) & 1) ^ 1,
-                                                         kDevTimeoutProducer, abort, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_expect_tx(&sh->r_full[s], SZ_BOX);
-                        tma_load_2d(smem + OFF_R + s * SZ_BOX, &tmR, &sh->r_full[s], it.h * DH,
-                                    it.rbase + SLOT * 2 * rb);
-                    }
-                    if (!ok) break;
+                for (int u = 0; u < nkv; ++u) {
                     if (k == 0 && u < pre_kv) {
                         // issued in the prologue; warm L2 for the next stages
                         for (int w = 1; w <= PREFETCH && w < nkv; ++w) {
@@ -1023,6 +1014,24 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // drain: the last load into each ring slot has landed
             for (int c = kvc - KV_STAGES; c < kvc; ++c)
                 if (c >= 0) drain_wait(&sh->kv_full[c % KV_STAGES], (c / KV_STAGES) & 1, p.status);
+        } else if (lane == 1) {
+            int rc = pre_r;  // R boxes issued (item 0's first in the prologue)
+            bool ok = true;
+            Item it;
+            for (int k = 0; ok && item_of<SPLIT, LOWER>(p, k, it); ++k) {
+                const int nrb = (it.ntiles + 3) >> 1;  // R boxes: slots 0 .. ntiles+1
+                for (int rb = (k == 0 ? pre_r : 0); rb < nrb; ++rb, ++rc) {
+                    const int s = rc % R_STAGES;
+                    if (rc >= R_STAGES && !mbar_wait(&sh->r_empty[s], ((rc / R_STAGES) & 1) ^ 1,
+                                                     kDevTimeoutProducer, abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&sh->r_full[s], SZ_BOX);
+                    tma_load_2d(smem + OFF_R + s * SZ_BOX, &tmR, &sh->r_full[s], it.h * DH,
+                                it.rbase + SLOT * 2 * rb);
+                }
+            }
             for (int c = rc - R_STAGES; c < rc; ++c)
                 if (c >= 0) drain_wait(&sh->r_full[c % R_STAGES], (c / R_STAGES) & 1, p.status);
         }
