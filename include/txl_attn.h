@@ -260,6 +260,37 @@ int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, c
                  float* dvb, int dtype, void* stream);
 
 /*
+ * txl_attn_bwd_ws: the gradients of txl_attn_bwd (same arguments, layouts,
+ * outputs and errors) on the tensor cores, for bf16 inputs with d_h = 64 and
+ * the plain causal mask with memory (same_length = 0).  Any other call needs
+ * no workspace and runs txl_attn_bwd.
+ *
+ * The pass follows the derivative of the attention of "Transformer-XL模型 核心
+ * 源码阅读笔记", section "Build the model" (RelPartialLearnableMultiHeadAttn.
+ * forward: AC + shifted BD, masked softmax, P V) with the memory a constant
+ * input ("Transformer-XL" notes, section "Segment-Level Recurrence"), in four
+ * launches on `stream`: the forward kernel computes each query row's softmax
+ * statistics into the workspace; a small kernel turns them into lse and
+ * D = dout . out per row and writes (q+u) and (q+v) scaled by scale * log2 e
+ * in bf16; a query-major pass recomputes P, dP and dS per 128-row query tile
+ * and writes dq and accumulates dr, du, dvb; a key-major pass recomputes
+ * them per 128-key tile and writes dk, dv.  dr, du and dvb are zeroed and
+ * accumulated with fp32 atomics (summation order not fixed); dq, dk and dv
+ * are written once per element.  Contractions in bf16 with fp32
+ * accumulation: P and dS are rounded to bf16 before their products.
+ *
+ * workspace: device memory owned by the caller, 256-byte aligned, at least
+ * txl_attn_bwd_workspace_bytes(...) bytes (0 when the call runs
+ * txl_attn_bwd); it must not overlap an input or a gradient (TXL_ERR_ALIAS).
+ * TXL_ERR_WORKSPACE when it is null, misaligned or too small.
+ */
+size_t txl_attn_bwd_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype, int same_length);
+int txl_attn_bwd_ws(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                    const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
+                    int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,
+                    float* dvb, int dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * The rest of a decoder layer ("Transformer-XL模型 核心源码阅读笔记":
  * RelPartialLearnableMultiHeadAttn.forward after the attention, PositionwiseFF,
  * RelPartialLearnableDecoderLayer), bf16 with fp32 accumulation:

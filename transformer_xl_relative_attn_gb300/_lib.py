@@ -62,6 +62,10 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_fwd_ex.restype = i
         lib.txl_attn_bwd.argtypes = [vp] * 7 + [i] * 5 + [f, i, i] + [vp] * 6 + [i, vp]
         lib.txl_attn_bwd.restype = i
+        lib.txl_attn_bwd_workspace_bytes.argtypes = [i] * 7
+        lib.txl_attn_bwd_workspace_bytes.restype = sz
+        lib.txl_attn_bwd_ws.argtypes = [vp] * 7 + [i] * 5 + [f, i, i] + [vp] * 6 + [i, vp, sz, vp]
+        lib.txl_attn_bwd_ws.restype = i
         lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
         lib.txl_attn_fwd_ws.restype = i
         lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
@@ -208,23 +212,55 @@ def attn_fwd(q, k, v, r_k, u, vb, scale=None, out=None, stream=None, same_length
     return out
 
 
-def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=None, stream=None):
-    """txl_attn_bwd: fp32 gradients of sum(out * dout) with respect to q, k,
-    v, r_k, u and vb (stop-gradient memory: the memory rows' dk, dv are
-    included and left to the caller).  Returns a dict dq, dk, dv, dr, du, dvb."""
+def attn_bwd_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16, same_length=False, device=None) -> int:
+    """txl_attn_bwd_workspace_bytes: scratch of the tensor-core backward (0
+    when the call takes the CUDA-core path)."""
+    code = TXL_BF16 if dtype == torch.bfloat16 else TXL_F32
+    dev = device if device is not None else torch.cuda.current_device()
+    return int(_invoke(dev, "txl_attn_bwd_workspace_bytes", B, H, L, M, dh, code, int(bool(same_length))))
+
+
+def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=None, stream=None,
+             tensor_cores=True, workspace=None, grads=None):
+    """fp32 gradients of sum(out * dout) with respect to q, k, v, r_k, u and
+    vb (stop-gradient memory: the memory rows' dk, dv are included and left
+    to the caller).  Returns a dict dq, dk, dv, dr, du, dvb.
+
+    tensor_cores: txl_attn_bwd_ws (the tcgen05 passes where they apply: bf16,
+    d_h = 64, no same_length; otherwise the same as txl_attn_bwd); False:
+    txl_attn_bwd, the CUDA-core kernels.  workspace: a uint8 tensor on the
+    device of at least attn_bwd_workspace_bytes(...) bytes (allocated here
+    when None); grads: a dict of preallocated gradient tensors to fill."""
     B, H, L, M, dh, scale, _ = _attn_args(q, k, v, r_k, u, vb, scale, dout)
     _need(dout, "dout", (B, H, L, dh), q.dtype, q.device)
     f32 = dict(dtype=torch.float32, device=q.device)
-    g = {"dq": torch.empty((B, H, L, dh), **f32), "dk": torch.empty((B, H, M + L, dh), **f32),
-         "dv": torch.empty((B, H, M + L, dh), **f32), "dr": torch.empty((M + L, H, dh), **f32),
-         "du": torch.empty((H, dh), **f32), "dvb": torch.empty((H, dh), **f32)}
-    rc = _invoke(q.device, "txl_attn_bwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(),
-                             vb.data_ptr(), dout.data_ptr(), B, H, L, M, dh, scale, int(bool(same_length)),
-                             M if mem_len is None else int(mem_len),
-                             *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")],
-                             _dtype_code(q), _stream(stream, q.device))
+    shapes = {"dq": (B, H, L, dh), "dk": (B, H, M + L, dh), "dv": (B, H, M + L, dh), "dr": (M + L, H, dh),
+              "du": (H, dh), "dvb": (H, dh)}
+    if grads is None:
+        g = {n: torch.empty(sh, **f32) for n, sh in shapes.items()}
+    else:
+        g = grads
+        for n, sh in shapes.items():
+            _need(g[n], n, sh, torch.float32, q.device)
+    ml = M if mem_len is None else int(mem_len)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(), vb.data_ptr(), dout.data_ptr(),
+            B, H, L, M, dh, scale, int(bool(same_length)), ml,
+            *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")], _dtype_code(q))
+    if tensor_cores:
+        need = attn_bwd_workspace_bytes(B, H, L, M, dh, q.dtype, same_length, q.device)
+        if workspace is None and need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None and (not isinstance(workspace, torch.Tensor) or workspace.device != q.device):
+            raise ValueError(f"workspace must be a tensor on {q.device}")
+        wp = workspace.data_ptr() if workspace is not None else 0
+        wn = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = _invoke(q.device, "txl_attn_bwd_ws", *args, wp, wn, _stream(stream, q.device))
+        name = "txl_attn_bwd_ws"
+    else:
+        rc = _invoke(q.device, "txl_attn_bwd", *args, _stream(stream, q.device))
+        name = "txl_attn_bwd"
     if rc != 0:
-        raise TxlError(rc, "txl_attn_bwd")
+        raise TxlError(rc, name)
     return g
 
 

@@ -86,6 +86,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "attn_tc_common.cuh"
 #include "txl_device.cuh"
 
 namespace txl {
@@ -226,134 +227,6 @@ __device__ __forceinline__ bool item_of(const TcParams& p, int k, Item& it) {
 // rounded up to an even count so that every item starts on an even global
 // slot and each score MMA writes two adjacent slots (one R box of 128 rows).
 __device__ __forceinline__ int slots_of(int ntiles) { return 2 * (((ntiles + 1) >> 1) + 1); }
-
-// Bounded wait that ignores the abort flag: used to drain in-flight copies and
-// MMAs before the CTA releases its shared and tensor memory.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_status(status, kDevTimeoutDrain);
-            return;
-        }
-    }
-}
-
-// One arrival per warp: every lane has issued its fences before the
-// __syncwarp, which orders their writes before lane 0's release-arrive.
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-// Two f32 values rounded to f16 (finite: out-of-range values saturate to
-// +-65504) in one 32-bit word, lo in the low half.
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// (lo(h) + a, hi(h) + b): each f16 half of h added in f32 to an f32 value
-__device__ __forceinline__ float2 add_h2_f32(uint32_t h, float a, float b) {
-    float d, e;
-    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
-        : "=f"(d), "=f"(e)
-        : "r"(h), "f"(a), "f"(b));
-    return make_float2(d, e);
-}
-
-// TMA store of a shared-memory box to a 3-D tensor (out-of-range rows are
-// clipped), committed as one bulk group of the issuing thread
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n\t"
-        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
-        "r"(src), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-// the issuing thread's bulk stores have read their shared-memory source
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// the issuing thread's bulk stores are complete
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// one arrival on an mbarrier that counts as n
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n)
-                 : "memory");
-}
-
-// (a.x + b.x, a.y + b.y) in one packed instruction
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;"
-        : "=l"(r)
-        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
-    return *reinterpret_cast<float2*>(&r);
-}
-
-// Per-row shift through shared memory.  A thread holds 64 consecutive band
-// columns w0[0..31] | w1[0..31] of its row and needs window columns o .. o+31
-// (o = 31 - lane).  It writes window column k to position k - o when k >= o
-// and window column 32 + k to position k + 32 - o otherwise (for each k
-// exactly one of the two lands in 0..31), then reads positions 0..31 back in
-// order.  Position x of lane l is word 32 x + l of the warp's 4 KB scratch:
-// each store and load of the warp touches 32 distinct banks, and a lane only
-// ever touches its own words.  `base` is the lane's word of position 0 minus
-// 128 o bytes.
-template <int K>
-__device__ __forceinline__ void st_shift_pair(int o, uint32_t base, uint32_t w0k, uint32_t w1k) {
-    asm volatile(
-        "{\n\t.reg .pred q;\n\t"
-        "setp.le.s32 q, %0, %1;\n\t"
-        "@q st.shared.b32 [%2+%3], %4;\n\t"
-        "@!q st.shared.b32 [%2+%5], %6;\n\t}"
-        ::"r"(o), "n"(K), "r"(base), "n"(128 * K), "r"(w0k), "n"(4096 + 128 * K), "r"(w1k)
-        : "memory");
-}
-template <int K>
-__device__ __forceinline__ float ld_shift(uint32_t base) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(base), "n"(128 * K) : "memory");
-    return v;
-}
-template <int K>
-__device__ __forceinline__ void st_shift_all(int o, uint32_t base, const uint32_t (&w0)[32],
-                                             const uint32_t (&w1)[32]) {
-    if constexpr (K < 32) {
-        st_shift_pair<K>(o, base, w0[K], w1[K]);
-        st_shift_all<K + 1>(o, base, w0, w1);
-    }
-}
-template <int K>
-__device__ __forceinline__ void ld_shift_all(uint32_t base, float (&win)[32]) {
-    if constexpr (K < 32) {
-        win[K] = ld_shift<K>(base);
-        ld_shift_all<K + 1>(base, win);
-    }
-}
-
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
-                 : "r"(addr)
-                 : "memory");
-}
 
 // Bounds-checked builds: a shared-memory access of `bytes` at `addr` stays
 // inside this CTA's dynamic shared memory.
@@ -1088,37 +961,6 @@ attn_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ w
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                        const cuuint64_t* strides_bytes, const cuuint32_t* box,
-                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-    EncodeTiledFn fn = get_encode_fn();
-    if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                    strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 static int num_sms() { return current_sm_count(); }
 
 // Launch with programmatic stream serialisation (the kernel waits for the
@@ -1181,10 +1023,14 @@ size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M) {
     return units * BM * (DH * sizeof(float) + sizeof(float2));
 }
 
-cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
-                                const void* ub, const void* vb, int B, int H, int L, int M,
-                                float scale, int lo_shift, void* out, void* workspace, int inject,
-                                int* status, cudaStream_t stream) {
+// The launch behind both entry points below.  stats_o / stats_ml non-null:
+// every item runs as a single split unit of attn_tc_bf16_kernel<true, false>
+// and leaves its unnormalised O and per-row (max, sum) there, indexed by the
+// item number (no combine pass, `out` is not written).
+static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
+                             const void* vb, int B, int H, int L, int M, float scale, int lo_shift, void* out,
+                             void* workspace, float* stats_o, float2* stats_ml, int inject, int* status,
+                             cudaStream_t stream) {
     using namespace tc;
     static PerDeviceOnce attrs;
     {
@@ -1245,29 +1091,56 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
     // the same_length bound runs unsplit (txl_attn_fwd_ex takes no workspace)
     const bool lower = lo_shift < (1 << 30);
     p.nsplit = (workspace && !lower) ? attn_tc_bf16_splits(B, H, L, M) : 1;
+    const bool stats = stats_o != nullptr;
+    if (stats && lower) return cudaErrorInvalidValue;
     if ((long long)p.n_items * p.nsplit + 2ll * num_sms() >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_units = p.n_items * p.nsplit;
     const size_t units = (size_t)p.n_units;
     p.ws_o = p.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = p.nsplit > 1 ? reinterpret_cast<float2*>(static_cast<float*>(workspace) + units * BM * DH)
                            : nullptr;
+    if (stats) {
+        p.ws_o = stats_o;
+        p.ws_ml = stats_ml;
+    }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.inject = inject;
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
-    if (p.nsplit > 1)
+    if (p.nsplit > 1 || stats)
         launch_pdl(attn_tc_bf16_kernel<true, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     else if (lower)
         launch_pdl(attn_tc_bf16_kernel<false, true>, grid, stream, mQ, mK, mV, mR, mO, p);
     else
         launch_pdl(attn_tc_bf16_kernel<false, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.nsplit == 1) return e;
+    if (e != cudaSuccess || p.nsplit == 1 || stats) return e;
     const long long threads = (long long)B * H * L * 8;
     if (threads >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     attn_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
         p.ws_o, p.ws_ml, p.out, B * H, L, p.n_qtiles, p.nsplit);
     return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, const void* r,
+                                const void* ub, const void* vb, int B, int H, int L, int M,
+                                float scale, int lo_shift, void* out, void* workspace, int inject,
+                                int* status, cudaStream_t stream) {
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, workspace, nullptr, nullptr, inject,
+                     status, stream);
+}
+
+// Forward statistics for the backward pass: item w = (query tile qq counted
+// from the last, then b*H+h), i.e. w = (n_qtiles-1-qt)*B*H + b*H + h, leaves
+// O_unnorm [w][128][64] (fp32, relative to the row max) in stats_o and
+// (max, sum) [w][128] in log2 units in stats_ml.  No output is written; the
+// output tensor map is encoded over q and never used.
+cudaError_t launch_attn_tc_bf16_stats(const void* q, const void* k, const void* v, const void* r,
+                                      const void* ub, const void* vb, int B, int H, int L, int M, float scale,
+                                      float* stats_o, float2* stats_ml, int* status, cudaStream_t stream) {
+    if (!stats_o || !stats_ml) return cudaErrorInvalidValue;
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, 1 << 30, const_cast<void*>(q), nullptr, stats_o,
+                     stats_ml, 0, status, stream);
 }
 
 TXL_BOUNDS_READER(bounds_word_attn_tc)

@@ -34,12 +34,18 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, int lo_shift, void* out, void* workspace, int inject,
                                 int* status, cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
+cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
+                               const void* vb, const void* dout, int B, int H, int L, int M, float scale, float* dq,
+                               float* dk, float* dv, float* dr, float* du, float* dvb, void* workspace, int* status,
+                               cudaStream_t stream);
+size_t attn_bwd_tc_workspace_bytes(int B, int H, int L, int M);
 
 // first bounds violation recorded by each translation unit (bounds-checked
 // builds; 0 otherwise), read and cleared
 unsigned long long bounds_word_attn_simt();
 unsigned long long bounds_word_attn_tc();
 unsigned long long bounds_word_attn_bwd();
+unsigned long long bounds_word_attn_bwd_tc();
 unsigned long long bounds_word_mem_update();
 unsigned long long bounds_word_layer_norm();
 unsigned long long bounds_word_proj_gemm();
@@ -121,6 +127,39 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* r_k
     return TXL_OK;
 }
 
+// Arguments of both backward entry points (gradients fp32, inputs in dtype).
+int check_bwd_args(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                   const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, int same_length,
+                   int mem_len, const float* dq, const float* dk, const float* dv, const float* dr,
+                   const float* du, const float* dvb, int dtype) {
+    const int es = elem_size(dtype);
+    if (!es) return TXL_ERR_INVALID_ARG;
+    if (!q || !k || !v || !r_k || !u_bias || !v_bias || !dout || !dq || !dk || !dv || !dr || !du || !dvb)
+        return TXL_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || L <= 0 || M < 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
+    if (same_length && (mem_len < M || mem_len >= (1 << 30))) return TXL_ERR_INVALID_ARG;
+    if (d_h > 256) return TXL_ERR_UNSUPPORTED;
+    const long long K = (long long)M + L;
+    if (K >= (1ll << 30) || (long long)B * H * K * d_h >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
+    const void* ins[7] = {q, k, v, r_k, u_bias, v_bias, dout};
+    const void* outs[6] = {dq, dk, dv, dr, du, dvb};
+    for (const void* p : ins)
+        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
+    for (const void* p : outs)
+        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
+    const size_t nq = (size_t)B * H * L * d_h, nkv = (size_t)B * H * K * d_h, nr = (size_t)K * H * d_h,
+                 nb = (size_t)H * d_h;
+    const size_t in_n[7] = {nq * es, nkv * es, nkv * es, nr * es, nb * es, nb * es, nq * es};
+    const size_t out_n[6] = {nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
+    for (int o = 0; o < 6; ++o) {
+        for (int i2 = 0; i2 < 7; ++i2)
+            if (overlap(outs[o], out_n[o], ins[i2], in_n[i2])) return TXL_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 6; ++o2)
+            if (overlap(outs[o], out_n[o], outs[o2], out_n[o2])) return TXL_ERR_ALIAS;
+    }
+    return TXL_OK;
+}
+
 // No lower key bound: the plain causal mask with memory.
 constexpr int kNoLowerBound = 1 << 30;
 
@@ -183,34 +222,47 @@ int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, c
                  const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
                  int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,
                  float* dvb, int dtype, void* stream) {
-    const int es = elem_size(dtype);
-    if (!es) return TXL_ERR_INVALID_ARG;
-    if (!q || !k || !v || !r_k || !u_bias || !v_bias || !dout || !dq || !dk || !dv || !dr || !du || !dvb)
-        return TXL_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || L <= 0 || M < 0 || d_h <= 0) return TXL_ERR_INVALID_ARG;
-    if (same_length && (mem_len < M || mem_len >= (1 << 30))) return TXL_ERR_INVALID_ARG;
-    if (d_h > 256) return TXL_ERR_UNSUPPORTED;
-    const long long K = (long long)M + L;
-    if (K >= (1ll << 30) || (long long)B * H * K * d_h >= (1ll << 40)) return TXL_ERR_UNSUPPORTED;
-    const void* ins[7] = {q, k, v, r_k, u_bias, v_bias, dout};
-    const void* outs[6] = {dq, dk, dv, dr, du, dvb};
-    for (const void* p : ins)
-        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
-    for (const void* p : outs)
-        if (!aligned16(p)) return TXL_ERR_MISALIGNED;
-    const size_t nq = (size_t)B * H * L * d_h, nkv = (size_t)B * H * K * d_h, nr = (size_t)K * H * d_h,
-                 nb = (size_t)H * d_h;
-    const size_t in_n[7] = {nq * es, nkv * es, nkv * es, nr * es, nb * es, nb * es, nq * es};
-    const size_t out_n[6] = {nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
-    for (int o = 0; o < 6; ++o) {
-        for (int i2 = 0; i2 < 7; ++i2)
-            if (overlap(outs[o], out_n[o], ins[i2], in_n[i2])) return TXL_ERR_ALIAS;
-        for (int o2 = o + 1; o2 < 6; ++o2)
-            if (overlap(outs[o], out_n[o], outs[o2], out_n[o2])) return TXL_ERR_ALIAS;
-    }
+    const int rc = check_bwd_args(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, d_h, same_length, mem_len, dq,
+                                  dk, dv, dr, du, dvb, dtype);
+    if (rc != TXL_OK) return rc;
     const cudaError_t e = txl::launch_attn_bwd_simt(q, k, v, r_k, u_bias, v_bias, dout, dtype == TXL_BF16, B, H,
                                                     L, M, d_h, scale, lower_shift(same_length, L, M, mem_len),
                                                     dq, dk, dv, dr, du, dvb, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+size_t txl_attn_bwd_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype, int same_length) {
+    // the tensor-core backward: bf16, d_h = 64, plain causal mask with memory
+    if (dtype != TXL_BF16 || d_h != 64 || same_length || B <= 0 || H <= 0 || L <= 0 || M < 0) return 0;
+    if ((long long)M + L >= (1ll << 30) || (long long)B * H >= (1ll << 30)) return 0;
+    return txl::attn_bwd_tc_workspace_bytes(B, H, L, M);
+}
+
+int txl_attn_bwd_ws(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                    const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
+                    int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,
+                    float* dvb, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+    const int rc = check_bwd_args(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, d_h, same_length, mem_len, dq,
+                                  dk, dv, dr, du, dvb, dtype);
+    if (rc != TXL_OK) return rc;
+    const size_t need = txl_attn_bwd_workspace_bytes(B, H, L, M, d_h, dtype, same_length);
+    if (!need)
+        return txl_attn_bwd(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, d_h, scale, same_length, mem_len, dq,
+                            dk, dv, dr, du, dvb, dtype, stream);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < need) return TXL_ERR_WORKSPACE;
+    const long long K = (long long)M + L;
+    const size_t nq = (size_t)B * H * L * d_h, nkv = (size_t)B * H * K * d_h, nr = (size_t)K * H * d_h,
+                 nb = (size_t)H * d_h;
+    const void* others[13] = {q, k, v, r_k, u_bias, v_bias, dout, dq, dk, dv, dr, du, dvb};
+    const size_t sizes[13] = {nq * 2, nkv * 2, nkv * 2, nr * 2, nb * 2, nb * 2, nq * 2,
+                              nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
+    for (int o = 0; o < 13; ++o)
+        if (overlap(workspace, need, others[o], sizes[o])) return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    const cudaError_t e = txl::launch_attn_bwd_tc(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, scale, dq, dk, dv,
+                                                  dr, du, dvb, workspace, status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // tensor-map encoding failed
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 
@@ -525,9 +577,10 @@ int txl_bounds_status(unsigned long long* first) {
     return TXL_ERR_UNSUPPORTED;  // this library was built without bounds checks
 #else
     if (cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
-    const unsigned long long words[6] = {txl::bounds_word_attn_simt(), txl::bounds_word_attn_tc(),
-                                         txl::bounds_word_attn_bwd(), txl::bounds_word_mem_update(),
-                                         txl::bounds_word_layer_norm(), txl::bounds_word_proj_gemm()};
+    const unsigned long long words[7] = {txl::bounds_word_attn_simt(),   txl::bounds_word_attn_tc(),
+                                         txl::bounds_word_attn_bwd(),    txl::bounds_word_attn_bwd_tc(),
+                                         txl::bounds_word_mem_update(),  txl::bounds_word_layer_norm(),
+                                         txl::bounds_word_proj_gemm()};
     unsigned long long w = 0;
     for (unsigned long long x : words) {
         if (x == ~0ull) return TXL_ERR_CUDA;

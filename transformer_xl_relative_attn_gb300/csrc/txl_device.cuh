@@ -249,13 +249,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 x bf16 -> f32, M x N, K-major A,
-// B K-major (b_mn = 0) or MN-major (b_mn = 1).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn) {
+// Instruction descriptor of kind::f16: bf16 x bf16 -> f32, M x N, A K-major
+// (a_mn = 0) or MN-major (a_mn = 1, A read transposed), B K-major (b_mn = 0)
+// or MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn, int a_mn = 0) {
     return (1u << 4)            // D format f32
            | (1u << 7)          // A format bf16
            | (1u << 10)         // B format bf16
-           | (0u << 15)         // A K-major
+           | ((uint32_t)a_mn << 15)
            | ((uint32_t)b_mn << 16)
            | ((uint32_t)(N >> 3) << 17)
            | ((uint32_t)(M >> 4) << 24);
