@@ -838,9 +838,30 @@ def time_backward(wl, calls, rks, u, vb, dev, peak_tf=None, peak_src=""):
     else:
         kern = "attn_bwd_tiled_kernel" if wl.dh <= 64 else "attn_bwd_simt_kernel"
         bound, peak, psrc = "alu", 152 * 128 * 2 * 2.07e9 / 1e12, "derived: fp32 FMA units x max SM clock"
-    return {"kernel": kern, "ms": round(ms, 4), "tflops": round(tf, 3), "bound": bound, "peak": round(peak, 1),
-            "frac": round(tf / peak, 4), "peak_source": psrc, "flops": flops,
-            "measured": f"the workload's first call alone, CUDA events, {n} calls, whole backward (all launches)"}
+    res = {"kernel": kern, "ms": round(ms, 4), "tflops": round(tf, 3), "bound": bound, "peak": round(peak, 1),
+           "frac": round(tf / peak, 4), "peak_source": psrc, "flops": flops,
+           "measured": f"the workload's first call alone, CUDA events, {n} calls, whole backward (all launches, "
+                       "the forward statistics recomputed inside)"}
+    if need and wl.dh == 64:
+        # the same gradients from the forward's saved state (out and the rows'
+        # log2-sum-exp, as a training forward keeps them): no recomputed forward
+        out, lse = txl.attn_fwd_lse(c["q"], c["k"], c["v"], rks[0], u, vb, scale=wl.scale)
+        for _ in range(2):
+            txl.attn_bwd(*args, workspace=ws, grads=grads, out=out, lse=lse)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            txl.attn_bwd(*args, workspace=ws, grads=grads, out=out, lse=lse)
+        e1.record()
+        torch.cuda.synchronize()
+        txl.check_status()
+        ms2 = e0.elapsed_time(e1) / n
+        tf2 = flops / (ms2 * 1e-3) / 1e12
+        res["from_saved_state"] = {
+            "entry": "txl_attn_bwd_saved (out and lse from txl_attn_fwd_lse)",
+            "kernel": "attn_bwd_prep_kernel + attn_bwd_q_kernel + attn_bwd_kv_kernel",
+            "ms": round(ms2, 4), "tflops": round(tf2, 3), "frac": round(tf2 / peak, 4)}
+    return res
 
 
 def cpu_baseline_and_parity(wl, calls, rks, u, vb):

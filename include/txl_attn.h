@@ -285,6 +285,29 @@ int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, c
  * TXL_ERR_WORKSPACE when it is null, misaligned or too small.
  */
 size_t txl_attn_bwd_workspace_bytes(int B, int H, int L, int M, int d_h, int dtype, int same_length);
+
+/*
+ * txl_attn_fwd_lse: txl_attn_fwd (bf16, d_h = 64) that also writes each query
+ * row's log2-sum-exp of its scores, lse [B, H, L] fp32 (log2 units: with s_ij
+ * the score of "Transformer-XL模型 核心源码阅读笔记", RelPartialLearnableMultiHead
+ * Attn.forward, P_ij = 2^(s_ij log2 e - lse_i)), the state a backward pass
+ * needs besides `out`.  lse: device memory, 16-byte aligned, not overlapping
+ * any other argument (TXL_ERR_ALIAS); TXL_ERR_UNSUPPORTED for TXL_F32.
+ *
+ * txl_attn_bwd_saved: the gradients of txl_attn_bwd_ws from the forward's
+ * saved state instead of a recomputed forward: out [B, H, L, d_h] (bf16) and
+ * lse as written by txl_attn_fwd_lse for the same inputs, D = dout . out per
+ * row.  bf16, d_h = 64, no same_length (TXL_ERR_UNSUPPORTED otherwise); the
+ * workspace of txl_attn_bwd_workspace_bytes(..., same_length = 0); the
+ * gradients must overlap neither the inputs, out, lse nor the workspace.
+ */
+int txl_attn_fwd_lse(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                     const void* v_bias, int B, int H, int L, int M, int d_h, float scale, void* out, float* lse,
+                     int dtype, void* stream);
+int txl_attn_bwd_saved(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                       const void* v_bias, const void* out, const float* lse, const void* dout, int B, int H, int L,
+                       int M, int d_h, float scale, float* dq, float* dk, float* dv, float* dr, float* du,
+                       float* dvb, int dtype, void* workspace, size_t ws_bytes, void* stream);
 int txl_attn_bwd_ws(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
                     const void* v_bias, const void* dout, int B, int H, int L, int M, int d_h, float scale,
                     int same_length, int mem_len, float* dq, float* dk, float* dv, float* dr, float* du,

@@ -114,3 +114,66 @@ def test_batch_summed_gradients_of_a_reduced_batch():
     ci, _, _ = W.first_call_inputs(wl, B=2)
     g = torch.randn(2, wl.H, wl.L, 64, generator=torch.Generator().manual_seed(9)).bfloat16()
     check(ci, g, names=("dr", "du", "dvb", "dq"))
+
+
+def _lse_bound(ci):
+    """Per-row bound on |lse_gpu - lse_ref| in log2 units: the scores carry
+    the bf16 rounding of (q+u)c, (q+v)c (relative 2^-9 per element) and the
+    f16 rounding of the position term (2^-11); a log-sum-exp moves by at most
+    the largest score error, bounded here with a factor 2 of margin."""
+    q, k, r, u, vb = (t.double() for t in (ci.q, ci.k, ci.r_k, ci.u, ci.vb))
+    qu = (q + u[None, :, None, :]).norm(dim=-1)                  # [B,H,L]
+    qv = (q + vb[None, :, None, :]).norm(dim=-1)
+    kn = k.norm(dim=-1).amax(dim=-1)                              # [B,H]
+    rn = r.norm(dim=-1).amax(dim=0)                               # [H]
+    s_max = qu * kn[:, :, None] + qv * rn[None, :, None]
+    return (2.0 ** -8) * ci.scale * 1.4426950408889634 * s_max + 1e-4
+
+
+@pytest.mark.parametrize("B,H,L,M", [(1, 2, 128, 128), (2, 2, 100, 37), (1, 1, 200, 0)])
+def test_forward_lse_matches_oracle(B, H, L, M):
+    ci = W.random_call_inputs(B, H, L, M, 64, std=0.5, seed=21 + L + M)
+    d = _dev(ci)
+    out0 = txl.attn_fwd(*d, scale=ci.scale)
+    out, lse = txl.attn_fwd_lse(*d, scale=ci.scale)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    assert torch.equal(out, out0)  # the same kernel, plus one store per row
+    _, sc = oracle.attn(ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb, ci.scale, want_scores=True)
+    m = sc.max(axis=-1, keepdims=True)
+    ref = (m[..., 0] + np.log(np.exp(sc - m).sum(axis=-1))) * 1.4426950408889634
+    err = np.abs(lse.cpu().double().numpy() - ref)
+    assert (err <= _lse_bound(ci).numpy()).all(), float(err.max())
+
+
+@pytest.mark.parametrize("B,H,L,M", [(1, 2, 128, 128), (2, 2, 100, 37), (1, 1, 200, 0), (2, 3, 257, 64)])
+def test_backward_from_saved_forward_state_matches_oracle(B, H, L, M):
+    """txl_attn_bwd_saved: the gradients from the forward's saved out and lse
+    (no recomputed forward) against the oracle."""
+    ci = W.random_call_inputs(B, H, L, M, 64, std=0.5, seed=31 + L + M)
+    d = _dev(ci)
+    out, lse = txl.attn_fwd_lse(*d, scale=ci.scale)
+    g = torch.randn(B, H, L, 64, generator=torch.Generator().manual_seed(5)).bfloat16()
+    got = txl.attn_bwd(*d, g.cuda(), ci.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    ref = oracle.attn_bwd(ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb, ci.scale, g)
+    for n in NAMES:
+        _close(n, got[n].cpu().double().numpy(), ref[n])
+
+
+def test_saved_state_entries_reject_bad_arguments():
+    ci = W.random_call_inputs(1, 1, 64, 64, 64, std=0.5, seed=4)
+    d = _dev(ci)
+    out, lse = txl.attn_fwd_lse(*d, scale=ci.scale)
+    g = torch.randn(1, 1, 64, 64).bfloat16().cuda()
+    with pytest.raises(ValueError):
+        txl.attn_bwd(*d, g, ci.scale, out=out)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(txl.TxlError) as e:
+        txl.attn_bwd(*d, g, ci.scale, out=out, lse=lse, workspace=small)
+    assert e.value.code == -7
+    f32 = W.random_call_inputs(1, 1, 16, 16, 64, dtype=torch.float32, std=0.5, seed=4)
+    with pytest.raises(txl.TxlError) as e:
+        txl.attn_fwd_lse(*_dev(f32), scale=f32.scale)
+    assert e.value.code == -2

@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
         lib.txl_attn_bwd_workspace_bytes.restype = sz
         lib.txl_attn_bwd_ws.argtypes = [vp] * 7 + [i] * 5 + [f, i, i] + [vp] * 6 + [i, vp, sz, vp]
         lib.txl_attn_bwd_ws.restype = i
+        lib.txl_attn_fwd_lse.argtypes = [vp] * 6 + [i] * 5 + [f, vp, vp, i, vp]
+        lib.txl_attn_fwd_lse.restype = i
+        lib.txl_attn_bwd_saved.argtypes = [vp] * 9 + [i] * 5 + [f] + [vp] * 6 + [i, vp, sz, vp]
+        lib.txl_attn_bwd_saved.restype = i
         lib.txl_attn_fwd_ws.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp, sz, vp]
         lib.txl_attn_fwd_ws.restype = i
         lib.txl_attn_fwd_noalloc.argtypes = [vp] * 6 + [i] * 5 + [f, vp, i, vp]
@@ -220,8 +224,23 @@ def attn_bwd_workspace_bytes(B, H, L, M, dh, dtype=torch.bfloat16, same_length=F
     return int(_invoke(dev, "txl_attn_bwd_workspace_bytes", B, H, L, M, dh, code, int(bool(same_length))))
 
 
+def attn_fwd_lse(q, k, v, r_k, u, vb, scale=None, out=None, lse=None, stream=None):
+    """txl_attn_fwd_lse: attn_fwd (bf16, d_h = 64) that also returns each query
+    row's log2-sum-exp of its scores, lse [B, H, L] fp32: (out, lse)."""
+    B, H, L, M, dh, scale, out = _attn_args(q, k, v, r_k, u, vb, scale, out)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need(lse, "lse", (B, H, L), torch.float32, q.device)
+    rc = _invoke(q.device, "txl_attn_fwd_lse", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                 u.data_ptr(), vb.data_ptr(), B, H, L, M, dh, scale, out.data_ptr(), lse.data_ptr(), _dtype_code(q),
+                 _stream(stream, q.device))
+    if rc != 0:
+        raise TxlError(rc, "txl_attn_fwd_lse")
+    return out, lse
+
+
 def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=None, stream=None,
-             tensor_cores=True, workspace=None, grads=None):
+             tensor_cores=True, workspace=None, grads=None, out=None, lse=None):
     """fp32 gradients of sum(out * dout) with respect to q, k, v, r_k, u and
     vb (stop-gradient memory: the memory rows' dk, dv are included and left
     to the caller).  Returns a dict dq, dk, dv, dr, du, dvb.
@@ -230,7 +249,9 @@ def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=N
     d_h = 64, no same_length; otherwise the same as txl_attn_bwd); False:
     txl_attn_bwd, the CUDA-core kernels.  workspace: a uint8 tensor on the
     device of at least attn_bwd_workspace_bytes(...) bytes (allocated here
-    when None); grads: a dict of preallocated gradient tensors to fill."""
+    when None); grads: a dict of preallocated gradient tensors to fill.
+    out, lse: the forward's saved output and row log2-sum-exp (attn_fwd_lse):
+    txl_attn_bwd_saved, which takes them instead of recomputing the forward."""
     B, H, L, M, dh, scale, _ = _attn_args(q, k, v, r_k, u, vb, scale, dout)
     _need(dout, "dout", (B, H, L, dh), q.dtype, q.device)
     f32 = dict(dtype=torch.float32, device=q.device)
@@ -246,6 +267,21 @@ def attn_bwd(q, k, v, r_k, u, vb, dout, scale=None, same_length=False, mem_len=N
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(), u.data_ptr(), vb.data_ptr(), dout.data_ptr(),
             B, H, L, M, dh, scale, int(bool(same_length)), ml,
             *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")], _dtype_code(q))
+    if (out is None) != (lse is None):
+        raise ValueError("out and lse are given together")
+    if out is not None:
+        _need(out, "out", (B, H, L, dh), q.dtype, q.device)
+        _need(lse, "lse", (B, H, L), torch.float32, q.device)
+        need = attn_bwd_workspace_bytes(B, H, L, M, dh, q.dtype, False, q.device)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        rc = _invoke(q.device, "txl_attn_bwd_saved", q.data_ptr(), k.data_ptr(), v.data_ptr(), r_k.data_ptr(),
+                     u.data_ptr(), vb.data_ptr(), out.data_ptr(), lse.data_ptr(), dout.data_ptr(), B, H, L, M, dh,
+                     scale, *[g[n].data_ptr() for n in ("dq", "dk", "dv", "dr", "du", "dvb")], _dtype_code(q),
+                     workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+        if rc != 0:
+            raise TxlError(rc, "txl_attn_bwd_saved")
+        return g
     if tensor_cores:
         need = attn_bwd_workspace_bytes(B, H, L, M, dh, q.dtype, same_length, q.device)
         if workspace is None and need:

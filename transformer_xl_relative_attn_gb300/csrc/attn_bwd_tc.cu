@@ -62,24 +62,28 @@ constexpr uint32_t SZ_Q = BM * DH * 2;  // 16 KB: 128 rows of d_h (or 128 x 64 b
 constexpr float kLn2 = 0.69314718055994531f;
 
 // ---- attn_bwd_q_kernel (query-major)
-// warps 0-3 softmax (one query row per thread), 4 MMA issuer, 5 TMA
-// producer (lane 0: q-side tiles and K/V, lane 1: R boxes), 6-9 dR flush
-constexpr int QA_THREADS = 320;
-constexpr int QA_KV = 3;     // K/V ring, one 64-key tile per stage
+// warps 0-3 softmax (one query row per thread), 4 score issuer (AC, the
+// position slots, dP), 5 TMA producer (lane 0: q-side tiles and K/V, lane 1:
+// R boxes), 6-9 band scatter / dR / dq (row quarter w%4), 10 gradient issuer
+// (dq_c, dq_p, dR)
+constexpr int QA_THREADS = 352;
+constexpr int QA_KV = 2;     // K/V ring, one 64-key tile per stage
 constexpr int QA_RB = 3;     // R ring, one 128-row box (two band slots) per stage
 constexpr int QA_G = 4;      // G ring (band slots of dS) in shared memory
+constexpr int QA_RING = 3;   // position slots in TMEM: tile t reads slots t, t+1, t+2
 constexpr uint32_t QA_OFF_QU = 0;
-constexpr uint32_t QA_OFF_QV = QA_OFF_QU + SZ_Q;
-constexpr uint32_t QA_OFF_DO = QA_OFF_QV + SZ_Q;
-constexpr uint32_t QA_OFF_KV = QA_OFF_DO + SZ_Q;          // stage s: K at +16K*s, V at +16K*s+8K
+constexpr uint32_t QA_OFF_DO = QA_OFF_QU + SZ_Q;
+constexpr uint32_t QA_OFF_QV = QA_OFF_DO + SZ_Q;          // buffer b (item parity) at +16K*b
+constexpr uint32_t QA_OFF_KV = QA_OFF_QV + 2 * SZ_Q;      // stage s: K at +16K*s, V at +16K*s+8K
 constexpr uint32_t QA_OFF_R = QA_OFF_KV + QA_KV * 2 * SZ_T;
 constexpr uint32_t QA_OFF_DS = QA_OFF_R + QA_RB * SZ_Q;   // dS tile; also the per-row shift scratch
 constexpr uint32_t QA_OFF_G = QA_OFF_DS + SZ_Q;           // G slot g at +16K*g
 constexpr uint32_t QA_OFF_BAR = QA_OFF_G + QA_G * SZ_Q;
 constexpr uint32_t QA_SMEM = QA_OFF_BAR + 1024 + 1024;
 static_assert(QA_SMEM <= 232448, "shared memory budget of one sm_103a CTA");
-// TMEM columns: AC 0-63, dP (and dR) 64-127, position ring 128-383, dq_c, dq_p
-constexpr uint32_t QA_COL_S = 0, QA_COL_DP = 64, QA_COL_RING = 128, QA_COL_DQC = 384, QA_COL_DQP = 448;
+// TMEM columns: AC 0-63, dP 64-127, position ring 128-319, dR 320-383, dq_c, dq_p
+constexpr uint32_t QA_COL_S = 0, QA_COL_DP = 64, QA_COL_RING = 128, QA_COL_DR = 320, QA_COL_DQC = 384,
+                   QA_COL_DQP = 448;
 
 // ---- attn_bwd_kv_kernel (key-major)
 // warps 0-7 softmax (two threads per query row: warp w takes keys 64 (w/4)
@@ -123,14 +127,19 @@ struct BwdParams {
 struct QaShared {
     uint64_t kv_full[bw::QA_KV], kv_empty[bw::QA_KV];
     uint64_t r_full[bw::QA_RB], r_empty[bw::QA_RB];
-    uint64_t q_full, q_empty;    // q-side tiles of the item landed / no longer read
+    uint64_t qa_full, qa_empty;    // (q+u)c and dout of the item landed / no longer read
+    uint64_t qv_full[2], qv_empty[2];  // (q+v)c of the item (buffer = item parity)
     uint64_t s_full, s_free;     // AC and the tile's band slots are in TMEM / have been read
     uint64_t dp_full, dp_free;   // dP of the tile is in TMEM / has been read
-    uint64_t ds_full;            // dS tile and its band scatter are in shared memory
-    uint64_t post;               // the MMAs that read them (and all before) completed
+    uint64_t ds_full;            // the dS tile is in shared memory
+    uint64_t ds_read;            // the flush warps have read it
+    uint64_t dqc_done;           // the dq_c MMA that reads it completed
+    uint64_t g_full;             // the tile's band scatter is in G
+    uint64_t post;               // the MMAs after the scatter (and all before) completed
     uint64_t dr_full, dr_free;   // a dR pair is in TMEM / the flush warps read it
     uint64_t dq_done;            // every MMA of the item completed
-    uint64_t drain;
+    uint64_t dq_free;            // the flush warps read the item's dq accumulators
+    uint64_t drain[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -195,15 +204,15 @@ __device__ __forceinline__ bool kb_item(const BwdParams& p, int k, KbItem& it) {
     return true;
 }
 
-// Warp-wide sum of 64 values per lane into two values per lane: lane l ends
-// with the sums of columns 2l and 2l+1 (a butterfly reduce-scatter).
-__device__ __forceinline__ float2 warp_sum64(float (&v)[64]) {
+// Warp-wide sum of 32 values per lane: lane l ends with the sum over the
+// warp of column l (a butterfly reduce-scatter, 31 shuffles).
+__device__ __forceinline__ float warp_sum32(float (&v)[32]) {
     const int lane = threadIdx.x & 31;
-    // level l: each lane holds 64 >> l partial columns; the lanes with bit
+    // level l: each lane holds 32 >> l partial columns; the lanes with bit
     // (16 >> l) set keep the upper half of them, their partners the lower
 #pragma unroll
     for (int l = 0; l < 5; ++l) {
-        const int bit = 16 >> l, hl = 32 >> l;
+        const int bit = 16 >> l, hl = 16 >> l;
         const bool up = (lane & bit) != 0;
 #pragma unroll
         for (int x = 0; x < hl; ++x) {
@@ -212,7 +221,7 @@ __device__ __forceinline__ float2 warp_sum64(float (&v)[64]) {
             v[x] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
         }
     }
-    return make_float2(v[0], v[1]);
+    return v[0];
 }
 
 // bf16 halves: (hi of a, lo of b) when odd, else a
@@ -220,6 +229,10 @@ __device__ __forceinline__ uint32_t prmt_sel(uint32_t a, uint32_t b, uint32_t se
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
+}
+
+__device__ __forceinline__ void ld_shared_v4u(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
@@ -276,21 +289,27 @@ __device__ __forceinline__ void g_align(const uint32_t (&cw)[4], const uint32_t 
 // attn_bwd_q_kernel: dq, dR, du, dv_bias.
 //
 // Per key tile t of an item (global tile counter gt across items):
-//   issuer:  [scores]  AC(t) = (q+u)c K_t^T -> S; for even t the position
-//                      MMA of band slots t+2, t+3 (slots 0-3 for t = 0) into
-//                      the TMEM ring (the forward's rolling band)
-//            [dP]      dP(t) = dout V_t^T -> DP
-//            [post]    after the tile's dS: dq_c += dS K_t, dq_p += G_slot(t)
-//                      R_slot(t) (and slots nt, nt+1 after the last tile),
-//                      dR of each completed slot pair -> DP (then flushed)
-//   softmax: reads AC and its band (releases them), shifts the band, P =
-//            2^(s - lse), reads dP (releases it), dS = P (dP - D), writes
-//            the dS tile (K-major, for dq_c) and scatters dS into G.
-// The issuer runs [dP](t), [scores](t+1) (within the item), [post](t), so the
-// next tile's scores are computed while the softmax works on dS.  G slot g
-// is complete once tile g has been scattered (tile t writes slots t, t+1,
-// t+2); a slot's ring position is rewritten two tiles later, after the
-// softmax has waited for `post` of the tile before.
+//   score issuer (warp 4):  AC(t) = (q+u)c K_t^T -> S and the position MMA of
+//            band slot t+2 (slots 0-2 for t = 0) into a 3-slot TMEM ring
+//            (the forward's rolling band, one slot per tile), then
+//            dP(t) = dout V_t^T -> DP
+//   softmax (warps 0-3, one query row per thread): reads AC and the tile's
+//            band (releases them), shifts the band, P = 2^(s - lse), reads
+//            dP (releases it), dS = P (dP - D) -> the dS tile (K-major)
+//   flush (warps 6-9, row 32 (w%4) + lane): reads its row of the dS tile,
+//            scatters it into G (band coordinates), reads and reduces each
+//            dR pair into dr, and after the item's last tile writes dq and
+//            adds the row sums of dq_c, dq_p to du, dv_bias
+//   gradient issuer (warp 10): dq_c += dS K_t once the dS tile is in shared
+//            memory; once the tile's scatter is in G, dq_p += G_slot R_slot
+//            for the band slots complete after tile t (slot t; after the
+//            last tile also nt, nt+1) and dR = G^T (q+v)c of each complete
+//            slot pair -> DR
+// The two issuers run independent chains: the scores and dP of the next
+// tile go out as soon as the softmax has read the current ones.  G slot g is
+// complete once tile g has been scattered (tile t writes slots t, t+1, t+2);
+// a slot's position in the 4-slot G ring is rewritten two tiles later,
+// after the flush warps have waited for `post` of the tile before.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(bw::QA_THREADS, 1)
 attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constant__ CUtensorMap tmQv,
@@ -318,26 +337,36 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmR);
+        // buffers read by both issuers are released by a commit of each
         for (int s = 0; s < QA_KV; ++s) {
             mbar_init(&sh->kv_full[s], 1);
-            mbar_init(&sh->kv_empty[s], 1);
+            mbar_init(&sh->kv_empty[s], 2);
         }
         for (int s = 0; s < QA_RB; ++s) {
             mbar_init(&sh->r_full[s], 1);
-            mbar_init(&sh->r_empty[s], 1);
+            mbar_init(&sh->r_empty[s], 2);
         }
-        mbar_init(&sh->q_full, 1);
-        mbar_init(&sh->q_empty, 1);
+        mbar_init(&sh->qa_full, 1);
+        mbar_init(&sh->qa_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh->qv_full[b], 1);
+            mbar_init(&sh->qv_empty[b], 2);
+        }
         mbar_init(&sh->s_full, 1);
         mbar_init(&sh->s_free, 4);
         mbar_init(&sh->dp_full, 1);
         mbar_init(&sh->dp_free, 4);
         mbar_init(&sh->ds_full, 4);
+        mbar_init(&sh->ds_read, 4);
+        mbar_init(&sh->dqc_done, 1);
+        mbar_init(&sh->g_full, 4);
         mbar_init(&sh->post, 1);
         mbar_init(&sh->dr_full, 1);
         mbar_init(&sh->dr_free, 4);
         mbar_init(&sh->dq_done, 1);
-        mbar_init(&sh->drain, 1);
+        mbar_init(&sh->dq_free, 4);
+        mbar_init(&sh->drain[0], 1);
+        mbar_init(&sh->drain[1], 1);
         sh->abort = 0;
         fence_mbar_init();
     }
@@ -346,22 +375,18 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
+    const uint32_t ds_tile = s_base + QA_OFF_DS;
 
     if (warp < 4) {
         // ---------------------------------------------------------- softmax
         const int wq = warp;
         const int ii = tid;                      // query row within the item
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t ds_tile = s_base + QA_OFF_DS;
         // the warp's quarter of the dS tile doubles as its shift scratch
         const uint32_t t_ld = ds_tile + wq * 4096 + 4 * lane;
         const uint32_t t_st = t_ld - 128u * (uint32_t)(31 - lane);
-        const uint32_t g_base = s_base + QA_OFF_G;
-        const int o = 127 - ii;      // band column of key 0 of tile 0
-        const int e = o & 7;         // columns of the first chunk before it
-        const int a0 = o >> 3;       // chunk of the row's first value in tile 0
         bool ok = true;
-        int gt = 0, gslot = 0;
+        int gt = 0, gring = 0;  // global tile, global position slot of the item's slot 0
         QaItem it;
         for (int k = 0; ok && qa_item(p, k, it); ++k) {
             const int i = it.i0 + ii;
@@ -371,40 +396,48 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 lse = st.x;
                 Dv = st.y;
             }
-            uint32_t cw[4] = {0u, 0u, 0u, 0u};  // previous tile's last 8 dS values of the row
             for (int t = 0; t < it.nt; ++t, ++gt) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&sh->s_full, gt & 1, kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
                 tc_fence_after();
                 float sc[64];
                 {
-                    uint32_t ac[64], bwv[96];
-                    tmem_ld32(tmem + lane_off + QA_COL_S, *reinterpret_cast<uint32_t(*)[32]>(&ac[0]));
-                    tmem_ld32(tmem + lane_off + QA_COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&ac[32]));
-#pragma unroll
-                    for (int kc = 0; kc < 3; ++kc) {
-                        const int c = 96 - 32 * wq + 32 * kc;
-                        const uint32_t rc = QA_COL_RING + 64 * ((gslot + t + (c >> 6)) & 3) + (c & 63);
-                        tmem_ld32(tmem + lane_off + rc, *reinterpret_cast<uint32_t(*)[32]>(&bwv[32 * kc]));
-                    }
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    warp_arrive(&sh->s_free);
+                    // the band first (packed and stored to the shift scratch),
+                    // then AC: the two are never held in registers together
                     uint32_t hp[64];
+                    {
+                        uint32_t bwv[96];
 #pragma unroll
-                    for (int K = 0; K < 64; ++K)
-                        hp[K] = pack_f16x2_sat(__uint_as_float(bwv[K]), __uint_as_float(bwv[K + 32]));
-                    // the scratch (dS tile) and the G slots this tile writes
-                    // are free once the MMAs after the previous tile completed
-                    if (gt > 0)
-                        ok = __all_sync(0xffffffffu,
-                                        mbar_wait(&sh->post, (gt - 1) & 1, kDevTimeoutSoftmax, abort, p.status));
+                        for (int kc = 0; kc < 3; ++kc) {
+                            const int c = 96 - 32 * wq + 32 * kc;
+                            const uint32_t rc = QA_COL_RING + 64 * ((gring + t + (c >> 6)) % QA_RING) + (c & 63);
+                            tmem_ld32(tmem + lane_off + rc, *reinterpret_cast<uint32_t(*)[32]>(&bwv[32 * kc]));
+                        }
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int K = 0; K < 64; ++K)
+                            hp[K] = pack_f16x2_sat(__uint_as_float(bwv[K]), __uint_as_float(bwv[K + 32]));
+                    }
+                    // the scratch (the dS tile) is free once the previous
+                    // tile's dq_c MMA and the flush warps have read it
+                    if (gt > 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&sh->dqc_done, (gt - 1) & 1, kDevTimeoutSoftmax,
+                                                               abort, p.status) &&
+                                                         mbar_wait(&sh->ds_read, (gt - 1) & 1, kDevTimeoutSoftmax,
+                                                                   abort, p.status));
+                    }
                     if (!ok) break;
-                    float win[32];
                     __syncwarp();
                     if (!QA_SMEM_IN(t_ld, 128 * 31 + 4, 701)) break;
                     st_shift_all<0>(31 - lane, t_st, *reinterpret_cast<uint32_t(*)[32]>(&hp[0]),
                                     *reinterpret_cast<uint32_t(*)[32]>(&hp[32]));
+                    uint32_t ac[64];
+                    tmem_ld32(tmem + lane_off + QA_COL_S, *reinterpret_cast<uint32_t(*)[32]>(&ac[0]));
+                    tmem_ld32(tmem + lane_off + QA_COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&ac[32]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    warp_arrive(&sh->s_free);
+                    float win[32];
                     ld_shift_all<0>(t_ld, win);
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
@@ -445,219 +478,85 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                     if (QA_SMEM_IN(a, 16, 702))
                         st_shared_v4(a, w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 }
-                // band scatter: leading zero chunks before tile 0's first
-                // chunk, the tile's 8 chunks, and after the last tile its
-                // remaining values and the trailing zero chunks up to the
-                // end of slot nt+1
-                if (t == 0) {
-                    for (int ch = 0; ch < a0; ++ch) {
-                        const uint32_t a = g_chunk_addr(g_base, gslot, ch, ii);
-                        if (QA_SMEM_IN(a, 16, 703)) st_shared_v4(a, 0u, 0u, 0u, 0u);
-                    }
-                }
-                {
-                    uint32_t ow[32];
-                    g_align(cw, w, e, ow);
-#pragma unroll
-                    for (int kc = 0; kc < 8; ++kc) {
-                        const uint32_t a = g_chunk_addr(g_base, gslot, 8 * t + a0 + kc, ii);
-                        if (QA_SMEM_IN(a, 16, 704))
-                            st_shared_v4(a, ow[4 * kc], ow[4 * kc + 1], ow[4 * kc + 2], ow[4 * kc + 3]);
-                    }
-                }
-#pragma unroll
-                for (int x = 0; x < 4; ++x) cw[x] = w[28 + x];
-                if (t == it.nt - 1) {
-                    // chunk 8 of the last tile: its last e values, then zeros
-                    uint32_t ow[32];
-                    const uint32_t zw[32] = {};
-                    g_align(cw, zw, e, ow);
-                    const int ch0 = 8 * (t + 1) + a0;
-                    const int ch_end = 8 * (it.nt + 2);
-                    for (int ch = ch0; ch < ch_end; ++ch) {
-                        const uint32_t a = g_chunk_addr(g_base, gslot, ch, ii);
-                        const bool first = ch == ch0;
-                        if (QA_SMEM_IN(a, 16, 705))
-                            st_shared_v4(a, first ? ow[0] : 0u, first ? ow[1] : 0u, first ? ow[2] : 0u,
-                                         first ? ow[3] : 0u);
-                    }
-                }
                 fence_proxy_async_smem();
-                tc_fence_before();
                 warp_arrive(&sh->ds_full);
             }
-            if (!ok) break;
-            // ------------------------------------------ dq, du, dv_bias
-            ok = __all_sync(0xffffffffu, mbar_wait(&sh->dq_done, k & 1, kDevTimeoutSoftmax, abort, p.status));
-            if (!ok) break;
-            tc_fence_after();
-            float vc[64], vp[64];
-            {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tmem + lane_off + QA_COL_DQC + 32 * c, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) vc[32 * c + x] = p.scale * __uint_as_float(r[x]);
-                    tmem_ld32(tmem + lane_off + QA_COL_DQP + 32 * c, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) vp[32 * c + x] = p.scale * __uint_as_float(r[x]);
-                }
-            }
-            tc_fence_before();
-            if (i < p.L && TXL_BOUNDS(it.bh < p.B * p.H, 706, it.bh)) {
-                float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)it.bh * p.L + i) * DH);
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    dst[c] = make_float4(vc[4 * c] + vp[4 * c], vc[4 * c + 1] + vp[4 * c + 1],
-                                         vc[4 * c + 2] + vp[4 * c + 2], vc[4 * c + 3] + vp[4 * c + 3]);
-            }
-            // rows past L hold dS = 0: their dq_c, dq_p are zero
-            const float2 su = warp_sum64(vc);
-            const float2 sv = warp_sum64(vp);
-            atomicAdd(p.du + it.h * DH + 2 * lane, su.x);
-            atomicAdd(p.du + it.h * DH + 2 * lane + 1, su.y);
-            atomicAdd(p.dvb + it.h * DH + 2 * lane, sv.x);
-            atomicAdd(p.dvb + it.h * DH + 2 * lane + 1, sv.y);
-            gslot += qa_slots(it.nt);
+            gring += it.nt + 2;
         }
         tc_fence_before();
     } else if (warp == 4) {
-        // ------------------------------------------------------- MMA issuer
+        // ------------------------------------------ score issuer: AC, band, dP
         const uint32_t leader = elect_one();
         bool ok = true;
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, kDevTimeoutMma, abort, p.status));
             return ok;
         };
-        // descriptors: K-major views (score and dP MMAs), MN-major views
-        // (d_h contiguous: K and R as the B of dq; G read transposed and
-        // (q+v)c as the A and B of dR)
         const uint64_t dQu = smem_desc_sw128(s_base + QA_OFF_QU, 16, 1024);
         const uint64_t dQv = smem_desc_sw128(s_base + QA_OFF_QV, 16, 1024);
         const uint64_t dDO = smem_desc_sw128(s_base + QA_OFF_DO, 16, 1024);
         const uint64_t dKV = smem_desc_sw128(s_base + QA_OFF_KV, 16, 1024);
-        const uint64_t dKmn = smem_desc_sw128(s_base + QA_OFF_KV, 8192, 1024);
         const uint64_t dR = smem_desc_sw128(s_base + QA_OFF_R, 16, 1024);
-        const uint64_t dRmn = smem_desc_sw128(s_base + QA_OFF_R, 8192, 1024);
-        const uint64_t dDS = smem_desc_sw128(s_base + QA_OFF_DS, 16, 1024);
-        const uint64_t dG = smem_desc_sw128(s_base + QA_OFF_G, 16, 1024);
-        const uint64_t dGmn = smem_desc_sw128(s_base + QA_OFF_G, SZ_Q, 1024);
-        const uint64_t dQvmn = smem_desc_sw128(s_base + QA_OFF_QV, 8192, 1024);
         constexpr uint32_t U_T = SZ_T >> 4, U_Q = SZ_Q >> 4;
-        int gt = 0;        // global tile counter (K/V stage uses)
-        int rbox = 0;      // global R box counter at the item start
-        int gslot = 0;     // global band slot at the item start
-        int ndr = 0;       // dR MMAs issued
+        int gt = 0, rbox = 0, gring = 0;
         QaItem it;
-        // scores of tile t (global gt_t): AC into S; for even t the position
-        // slots t+2, t+3 (and 0, 1 for t = 0) into the ring
-        auto scores = [&](const QaItem& c, int t, int gt_t) {
-            if (gt_t > 0) wait(&sh->s_free, (gt_t - 1) & 1);
-            const int st = gt_t % QA_KV;
-            wait(&sh->kv_full[st], (gt_t / QA_KV) & 1);
-            if ((t & 1) == 0) {
-                for (int b = (t == 0 ? 0 : t / 2 + 1); b <= t / 2 + 1; ++b) {
-                    const int rb = rbox + b;
-                    wait(&sh->r_full[rb % QA_RB], (rb / QA_RB) & 1);
-                    if (!ok) return;
-                    tc_fence_after();
-                    const uint32_t d = tmem + QA_COL_RING + 128 * (((gslot >> 1) + b) & 1);
-                    const uint64_t bR = dR + (rb % QA_RB) * U_Q;
-#pragma unroll
-                    for (int kk = 0; kk < DH / 16; ++kk)
-                        mma_ss_elect(d, dQv + 2 * kk, bR + 2 * kk, IDESC_N128, kk > 0, leader);
-                }
-            }
-            if (!ok) return;
-            tc_fence_after();
-            const uint64_t bK = dKV + st * 2 * U_T;
-#pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk)
-                mma_ss_elect(tmem + QA_COL_S, dQu + 2 * kk, bK + 2 * kk, IDESC_N64, kk > 0, leader);
-            if (leader) mma_commit(&sh->s_full);
-        };
-        auto dr_pair = [&](int b) {
-            // G slots 2b, 2b+1 (adjacent ring positions) read transposed:
-            // M = 128 band rows, K = 128 query rows
-            if (ndr > 0) wait(&sh->dr_free, (ndr - 1) & 1);
-            if (!ok) return;
-            tc_fence_after();
-            const uint64_t aG = dGmn + ((gslot + 2 * b) & (QA_G - 1)) * U_Q;
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-                mma_ss_elect(tmem + QA_COL_DP, aG + kk * 128, dQvmn + kk * 128, IDESC_N64_ABMN, kk > 0, leader);
-            if (leader) mma_commit(&sh->dr_full);
-            ++ndr;
-        };
         for (int k = 0; ok && qa_item(p, k, it); ++k) {
-            const int nb = (it.nt + 3) >> 1;  // R boxes = band slot pairs of the item
-            wait(&sh->q_full, k & 1);
-            scores(it, 0, gt);
-            int next_dr = 0;   // first slot pair without its dR
-            int next_rel = 0;  // first R box not yet released
+            const int qb = k & 1;  // (q+v)c buffer of the item
+            wait(&sh->qa_full, k & 1);
+            wait(&sh->qv_full[qb], (k >> 1) & 1);
+            const uint64_t aQv = dQv + qb * U_Q;
             for (int t = 0; ok && t < it.nt; ++t) {
                 const int gt_t = gt + t;
                 const int st = gt_t % QA_KV;
-                // dP(t): DP must be read (previous dP) and flushed (previous dR)
-                if (gt_t > 0) wait(&sh->dp_free, (gt_t - 1) & 1);
-                if (ndr > 0) wait(&sh->dr_free, (ndr - 1) & 1);
+                const bool last = t == it.nt - 1;
+                // AC(t) and the band slots tile t is the first to read: S and
+                // the ring position of slot t+2 (slot t-1's) are free once
+                // the softmax has read tile t-1
+                if (gt_t > 0) wait(&sh->s_free, (gt_t - 1) & 1);
+                wait(&sh->kv_full[st], (gt_t / QA_KV) & 1);
+                for (int s = (t == 0 ? 0 : t + 2); ok && s <= t + 2; ++s) {
+                    const int rb = rbox + (s >> 1);
+                    if ((s & 1) == 0 || s == 1) wait(&sh->r_full[rb % QA_RB], (rb / QA_RB) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + QA_COL_RING + 64 * ((gring + s) % QA_RING);
+                    const uint64_t bR = dR + (rb % QA_RB) * U_Q + (s & 1) * U_T;
+#pragma unroll
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        mma_ss_elect(d, aQv + 2 * kk, bR + 2 * kk, IDESC_N64, kk > 0, leader);
+                    // the box's last position slot (or the item's)
+                    if (leader && ((s & 1) || s == it.nt + 1)) mma_commit(&sh->r_empty[rb % QA_RB]);
+                }
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t bV = dKV + st * 2 * U_T + U_T;
+                const uint64_t bK = dKV + st * 2 * U_T;
+#pragma unroll
+                for (int kk = 0; kk < DH / 16; ++kk)
+                    mma_ss_elect(tmem + QA_COL_S, dQu + 2 * kk, bK + 2 * kk, IDESC_N64, kk > 0, leader);
+                if (leader) {
+                    mma_commit(&sh->s_full);
+                    if (last) mma_commit(&sh->qv_empty[qb]);
+                }
+                // dP(t) once the softmax has read dP(t-1)
+                if (gt_t > 0) wait(&sh->dp_free, (gt_t - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t bV = bK + U_T;
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
                     mma_ss_elect(tmem + QA_COL_DP, dDO + 2 * kk, bV + 2 * kk, IDESC_N64, kk > 0, leader);
-                if (leader) mma_commit(&sh->dp_full);
-                // the next tile's scores while the softmax works on dS(t)
-                if (t + 1 < it.nt) scores(it, t + 1, gt_t + 1);
-                // dq and dR MMAs of tile t
-                wait(&sh->ds_full, gt_t & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t acc0 = t > 0 ? 1u : 0u;
-                const uint64_t bKmn = dKmn + st * 2 * U_T;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ss_elect(tmem + QA_COL_DQC, dDS + 2 * kk, bKmn + kk * 128, IDESC_N64_BMN,
-                                 kk > 0 ? 1u : acc0, leader);
-                const int s_hi = (t == it.nt - 1) ? it.nt + 1 : t;  // band slots complete now
-                for (int s = t; s <= s_hi; ++s) {
-                    const int rb = rbox + (s >> 1);
-                    const uint64_t aG = dG + ((gslot + s) & (QA_G - 1)) * U_Q;
-                    const uint64_t bR = dRmn + (rb % QA_RB) * U_Q + (s & 1) * U_T;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ss_elect(tmem + QA_COL_DQP, aG + 2 * kk, bR + kk * 128, IDESC_N64_BMN,
-                                     (kk > 0 || s > 0) ? 1u : 0u, leader);
-                }
                 if (leader) {
+                    mma_commit(&sh->dp_full);
                     mma_commit(&sh->kv_empty[st]);
-                    // R boxes whose two slots have had their dq_p MMA
-                    const int rel_end = (t == it.nt - 1) ? nb : (t + 1) >> 1;
-                    for (int b = next_rel; b < rel_end; ++b) mma_commit(&sh->r_empty[(rbox + b) % QA_RB]);
-                }
-                next_rel = (t == it.nt - 1) ? nb : max(next_rel, (t + 1) >> 1);
-                // dR of the slot pairs complete after tile t
-                const int dr_end = (t == it.nt - 1) ? nb : (t + 1) >> 1;
-                for (; ok && next_dr < dr_end; ++next_dr) dr_pair(next_dr);
-                if (!ok) break;
-                if (leader) {
-                    mma_commit(&sh->post);
-                    if (t == it.nt - 1) {
-                        mma_commit(&sh->q_empty);
-                        mma_commit(&sh->dq_done);
-                    }
+                    if (last) mma_commit(&sh->qa_empty);
                 }
             }
             gt += it.nt;
-            rbox += nb;
-            gslot += qa_slots(it.nt);
+            rbox += (it.nt + 3) >> 1;
+            gring += it.nt + 2;
         }
-        if (leader) mma_commit(&sh->drain);
-        drain_wait(&sh->drain, 0, p.status);
+        if (leader) mma_commit(&sh->drain[0]);
+        drain_wait(&sh->drain[0], 0, p.status);
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------ TMA producer
@@ -666,14 +565,21 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
             int kvc = 0;
             QaItem it;
             for (int k = 0; ok && qa_item(p, k, it); ++k) {
-                if (k > 0 && !mbar_wait(&sh->q_empty, (k - 1) & 1, kDevTimeoutProducer, abort, p.status)) {
+                const int qb = k & 1;
+                if (k > 0 && !mbar_wait(&sh->qa_empty, (k - 1) & 1, kDevTimeoutProducer, abort, p.status)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&sh->q_full, 3 * SZ_Q);
-                tma_load_3d(smem + QA_OFF_QU, &tmQu, &sh->q_full, 0, it.i0, it.bh);
-                tma_load_3d(smem + QA_OFF_QV, &tmQv, &sh->q_full, 0, it.i0, it.bh);
-                tma_load_3d(smem + QA_OFF_DO, &tmDO, &sh->q_full, 0, it.i0, it.bh);
+                mbar_expect_tx(&sh->qa_full, 2 * SZ_Q);
+                tma_load_3d(smem + QA_OFF_QU, &tmQu, &sh->qa_full, 0, it.i0, it.bh);
+                tma_load_3d(smem + QA_OFF_DO, &tmDO, &sh->qa_full, 0, it.i0, it.bh);
+                if (k >= 2 && !mbar_wait(&sh->qv_empty[qb], ((k >> 1) & 1) ^ 1, kDevTimeoutProducer, abort,
+                                         p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&sh->qv_full[qb], SZ_Q);
+                tma_load_3d(smem + QA_OFF_QV + qb * SZ_Q, &tmQv, &sh->qv_full[qb], 0, it.i0, it.bh);
                 for (int t = 0; t < it.nt; ++t, ++kvc) {
                     const int s = kvc % QA_KV;
                     if (kvc >= QA_KV && !mbar_wait(&sh->kv_empty[s], ((kvc / QA_KV) & 1) ^ 1,
@@ -710,46 +616,241 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 if (c >= 0) drain_wait(&sh->r_full[c % QA_RB], (c / QA_RB) & 1, p.status);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------- dR flush
-        // warp w reads TMEM lane quarter w % 4: band rows 32 (w%4) + lane of
-        // each slot pair
+    } else if (warp < 10) {
+        // --------------------------------------------- band scatter, dR, dq
+        // warp w serves TMEM lane quarter w % 4: query row ii = 32 (w%4) +
+        // lane of the scatter and of dq, band row ii of each dR pair
         const int wq = warp & 3;
-        const int m = 32 * wq + lane;
+        const int ii = 32 * wq + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t g_base = s_base + QA_OFF_G;
+        const int o = 127 - ii;      // band column of key 0 of tile 0
+        const int e = o & 7;         // columns of the first chunk before it
+        const int a0 = o >> 3;       // chunk of the row's first value in tile 0
         bool ok = true;
-        int ndr = 0;
+        int gt = 0, ndr = 0, gslot = 0;
         QaItem it;
         for (int k = 0; ok && qa_item(p, k, it); ++k) {
             const int nb = (it.nt + 3) >> 1;
-            for (int b = 0; b < nb; ++b, ++ndr) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&sh->dr_full, ndr & 1, kDevTimeoutSoftmax, abort, p.status));
+            uint32_t cw[4] = {0u, 0u, 0u, 0u};  // previous tile's last 8 dS values of the row
+            int next_dr = 0;
+            for (int t = 0; t < it.nt; ++t, ++gt) {
+                const bool last = t == it.nt - 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh->ds_full, gt & 1, kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
-                tc_fence_after();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_off + QA_COL_DP, r0);
-                tmem_ld32(tmem + lane_off + QA_COL_DP + 32, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                warp_arrive(&sh->dr_free);
-                const int slot = 2 * b + (m >> 6);
-                const int row = it.rbase + 128 * b + m;
-                if (slot <= it.nt + 1 && row >= 0 && row < p.K &&
-                    TXL_BOUNDS((size_t)row * p.H + it.h < (size_t)p.K * p.H, 707, row)) {
-                    float* dst = p.dr + ((size_t)row * p.H + it.h) * DH;
+                uint32_t w[32];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        red_add_v4(dst + 4 * c, kLn2 * __uint_as_float(r0[4 * c]), kLn2 * __uint_as_float(r0[4 * c + 1]),
-                                   kLn2 * __uint_as_float(r0[4 * c + 2]), kLn2 * __uint_as_float(r0[4 * c + 3]));
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        red_add_v4(dst + 32 + 4 * c, kLn2 * __uint_as_float(r1[4 * c]),
-                                   kLn2 * __uint_as_float(r1[4 * c + 1]), kLn2 * __uint_as_float(r1[4 * c + 2]),
-                                   kLn2 * __uint_as_float(r1[4 * c + 3]));
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint32_t a = ds_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4);
+                    if (QA_SMEM_IN(a, 16, 708)) ld_shared_v4u(a, w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 }
+                warp_arrive(&sh->ds_read);
+                // the G positions of slots t .. t+2 are free once the MMAs
+                // after the previous tile's scatter completed
+                if (gt > 0)
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&sh->post, (gt - 1) & 1, kDevTimeoutSoftmax, abort, p.status));
+                if (!ok) break;
+                // leading zero chunks before tile 0's first chunk, the tile's
+                // 8 chunks, and after the last tile its remaining values and
+                // the trailing zero chunks up to the end of slot nt+1
+                if (t == 0) {
+                    for (int ch = 0; ch < a0; ++ch) {
+                        const uint32_t a = g_chunk_addr(g_base, gslot, ch, ii);
+                        if (QA_SMEM_IN(a, 16, 703)) st_shared_v4(a, 0u, 0u, 0u, 0u);
+                    }
+                }
+                {
+                    uint32_t ow[32];
+                    g_align(cw, w, e, ow);
+#pragma unroll
+                    for (int kc = 0; kc < 8; ++kc) {
+                        const uint32_t a = g_chunk_addr(g_base, gslot, 8 * t + a0 + kc, ii);
+                        if (QA_SMEM_IN(a, 16, 704))
+                            st_shared_v4(a, ow[4 * kc], ow[4 * kc + 1], ow[4 * kc + 2], ow[4 * kc + 3]);
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x) cw[x] = w[28 + x];
+                if (last) {
+                    // chunk 8 of the last tile: its last e values, then zeros
+                    uint32_t ow[32];
+                    const uint32_t zw[32] = {};
+                    g_align(cw, zw, e, ow);
+                    const int ch0 = 8 * (t + 1) + a0;
+                    const int ch_end = 8 * (it.nt + 2);
+                    for (int ch = ch0; ch < ch_end; ++ch) {
+                        const uint32_t a = g_chunk_addr(g_base, gslot, ch, ii);
+                        const bool first = ch == ch0;
+                        if (QA_SMEM_IN(a, 16, 705))
+                            st_shared_v4(a, first ? ow[0] : 0u, first ? ow[1] : 0u, first ? ow[2] : 0u,
+                                         first ? ow[3] : 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                warp_arrive(&sh->g_full);
+                // the dR pairs this tile completes
+                const int dr_end = last ? nb : (t + 1) >> 1;
+                for (; next_dr < dr_end; ++next_dr, ++ndr) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&sh->dr_full, ndr & 1, kDevTimeoutSoftmax, abort, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem + lane_off + QA_COL_DR, r0);
+                    tmem_ld32(tmem + lane_off + QA_COL_DR + 32, r1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    warp_arrive(&sh->dr_free);
+                    const int slot = 2 * next_dr + (ii >> 6);
+                    const int row = it.rbase + 128 * next_dr + ii;
+                    if (slot <= it.nt + 1 && row >= 0 && row < p.K &&
+                        TXL_BOUNDS((size_t)row * p.H + it.h < (size_t)p.K * p.H, 707, row)) {
+                        float* dst = p.dr + ((size_t)row * p.H + it.h) * DH;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            red_add_v4(dst + 4 * c, kLn2 * __uint_as_float(r0[4 * c]),
+                                       kLn2 * __uint_as_float(r0[4 * c + 1]), kLn2 * __uint_as_float(r0[4 * c + 2]),
+                                       kLn2 * __uint_as_float(r0[4 * c + 3]));
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            red_add_v4(dst + 32 + 4 * c, kLn2 * __uint_as_float(r1[4 * c]),
+                                       kLn2 * __uint_as_float(r1[4 * c + 1]), kLn2 * __uint_as_float(r1[4 * c + 2]),
+                                       kLn2 * __uint_as_float(r1[4 * c + 3]));
+                    }
+                }
+                if (!ok) break;
             }
+            if (!ok) break;
+            // ------------------------------------------ dq, du, dv_bias
+            ok = __all_sync(0xffffffffu, mbar_wait(&sh->dq_done, k & 1, kDevTimeoutSoftmax, abort, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            // two halves of 32 columns: dq = scale (dq_c + dq_p) per row, and
+            // the warp's column sums of scale dq_c, scale dq_p into du, dv_bias
+            // (rows past L hold dS = 0: their dq_c, dq_p are zero)
+            const int i = it.i0 + ii;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rc[32], rp[32];
+                tmem_ld32(tmem + lane_off + QA_COL_DQC + 32 * c, rc);
+                tmem_ld32(tmem + lane_off + QA_COL_DQP + 32 * c, rp);
+                tmem_wait_ld();
+                if (c == 1) {
+                    tc_fence_before();
+                    warp_arrive(&sh->dq_free);
+                }
+                float vc[32], vp[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    vc[x] = p.scale * __uint_as_float(rc[x]);
+                    vp[x] = p.scale * __uint_as_float(rp[x]);
+                }
+                if (i < p.L && TXL_BOUNDS(it.bh < p.B * p.H, 706, it.bh)) {
+                    float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)it.bh * p.L + i) * DH + 32 * c);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        dst[x] = make_float4(vc[4 * x] + vp[4 * x], vc[4 * x + 1] + vp[4 * x + 1],
+                                             vc[4 * x + 2] + vp[4 * x + 2], vc[4 * x + 3] + vp[4 * x + 3]);
+                }
+                atomicAdd(p.du + it.h * DH + 32 * c + lane, warp_sum32(vc));
+                atomicAdd(p.dvb + it.h * DH + 32 * c + lane, warp_sum32(vp));
+            }
+            gslot += qa_slots(it.nt);
         }
         tc_fence_before();
+    } else {
+        // --------------------------------------- gradient issuer: dq_c, dq_p, dR
+        const uint32_t leader = elect_one();
+        bool ok = true;
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, kDevTimeoutMma, abort, p.status));
+            return ok;
+        };
+        // MN-major views (d_h contiguous): K and R as the B of dq; G read
+        // transposed and (q+v)c as the A and B of dR
+        const uint64_t dKmn = smem_desc_sw128(s_base + QA_OFF_KV, 8192, 1024);
+        const uint64_t dRmn = smem_desc_sw128(s_base + QA_OFF_R, 8192, 1024);
+        const uint64_t dDS = smem_desc_sw128(s_base + QA_OFF_DS, 16, 1024);
+        const uint64_t dG = smem_desc_sw128(s_base + QA_OFF_G, 16, 1024);
+        const uint64_t dGmn = smem_desc_sw128(s_base + QA_OFF_G, SZ_Q, 1024);
+        const uint64_t dQvmn = smem_desc_sw128(s_base + QA_OFF_QV, 8192, 1024);
+        constexpr uint32_t U_T = SZ_T >> 4, U_Q = SZ_Q >> 4;
+        int gt = 0, rbox = 0, gslot = 0, ndr = 0;
+        QaItem it;
+        for (int k = 0; ok && qa_item(p, k, it); ++k) {
+            const int nb = (it.nt + 3) >> 1;
+            const int qb = k & 1;
+            const uint64_t bQv = dQvmn + qb * U_Q;
+            int next_dr = 0;
+            for (int t = 0; ok && t < it.nt; ++t) {
+                const int gt_t = gt + t;
+                const int st = gt_t % QA_KV;
+                const bool last = t == it.nt - 1;
+                // dq_c(t) once the dS tile is in shared memory (the item's
+                // first one overwrites dq_c: the flush warps have read the
+                // previous item's)
+                wait(&sh->ds_full, gt_t & 1);
+                if (t == 0 && k > 0) wait(&sh->dq_free, (k - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t bKmn = dKmn + st * 2 * U_T;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ss_elect(tmem + QA_COL_DQC, dDS + 2 * kk, bKmn + kk * 128, IDESC_N64_BMN,
+                                 (kk > 0 || t > 0) ? 1u : 0u, leader);
+                if (leader) {
+                    mma_commit(&sh->dqc_done);
+                    mma_commit(&sh->kv_empty[st]);
+                }
+                // dq_p of the band slots complete after tile t and dR of the
+                // complete slot pairs, once the tile's scatter is in G
+                wait(&sh->g_full, gt_t & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const int s_hi = last ? it.nt + 1 : t;
+                for (int s = t; s <= s_hi; ++s) {
+                    const int rb = rbox + (s >> 1);
+                    const uint64_t aG = dG + ((gslot + s) & (QA_G - 1)) * U_Q;
+                    const uint64_t bR = dRmn + (rb % QA_RB) * U_Q + (s & 1) * U_T;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ss_elect(tmem + QA_COL_DQP, aG + 2 * kk, bR + kk * 128, IDESC_N64_BMN,
+                                     (kk > 0 || s > 0) ? 1u : 0u, leader);
+                    // the box's last slot (or the item's)
+                    if (leader && ((s & 1) || s == it.nt + 1)) mma_commit(&sh->r_empty[rb % QA_RB]);
+                }
+                const int dr_end = last ? nb : (t + 1) >> 1;
+                for (; ok && next_dr < dr_end; ++next_dr) {
+                    // G slots 2b, 2b+1 (adjacent ring positions) read
+                    // transposed: M = 128 band rows, K = 128 query rows
+                    if (ndr > 0) wait(&sh->dr_free, (ndr - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t aG = dGmn + ((gslot + 2 * next_dr) & (QA_G - 1)) * U_Q;
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ss_elect(tmem + QA_COL_DR, aG + kk * 128, bQv + kk * 128, IDESC_N64_ABMN, kk > 0,
+                                     leader);
+                    if (leader) mma_commit(&sh->dr_full);
+                    ++ndr;
+                }
+                if (!ok) break;
+                if (leader) {
+                    mma_commit(&sh->post);
+                    if (last) {
+                        mma_commit(&sh->qv_empty[qb]);
+                        mma_commit(&sh->dq_done);
+                    }
+                }
+            }
+            gt += it.nt;
+            rbox += nb;
+            gslot += qa_slots(it.nt);
+        }
+        if (leader) mma_commit(&sh->drain[1]);
+        drain_wait(&sh->drain[1], 0, p.status);
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -861,31 +962,37 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
                 tc_fence_after();
                 float sc[64];
                 {
-                    uint32_t ac[64], bwv[96];
-                    tmem_ld32(tmem + lane_off + KB_COL_S + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&ac[0]));
-                    tmem_ld32(tmem + lane_off + KB_COL_S + 64 * hh + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&ac[32]));
-#pragma unroll
-                    for (int kc = 0; kc < 3; ++kc)
-                        tmem_ld32(tmem + lane_off + KB_COL_BAND + c0 + 32 * kc,
-                                  *reinterpret_cast<uint32_t(*)[32]>(&bwv[32 * kc]));
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    warp_arrive(&sh->s_free);
+                    // the band first (packed and stored to the shift scratch),
+                    // then AC: the two are never held in registers together
                     uint32_t hp[64];
+                    {
+                        uint32_t bwv[96];
 #pragma unroll
-                    for (int K = 0; K < 64; ++K)
-                        hp[K] = pack_f16x2_sat(__uint_as_float(bwv[K]), __uint_as_float(bwv[K + 32]));
+                        for (int kc = 0; kc < 3; ++kc)
+                            tmem_ld32(tmem + lane_off + KB_COL_BAND + c0 + 32 * kc,
+                                      *reinterpret_cast<uint32_t(*)[32]>(&bwv[32 * kc]));
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int K = 0; K < 64; ++K)
+                            hp[K] = pack_f16x2_sat(__uint_as_float(bwv[K]), __uint_as_float(bwv[K + 32]));
+                    }
                     // the P / dS buffer is free once the previous dK MMA completed
                     if (gs > 0)
                         ok = __all_sync(0xffffffffu,
                                         mbar_wait(&sh->post, (gs - 1) & 1, kDevTimeoutSoftmax, abort, p.status));
                     if (!ok) break;
-                    float win[32];
                     __syncwarp();
                     if (!KB_SMEM_IN(t_ld, 128 * 31 + 4, 711)) break;
                     st_shift_all<0>(31 - lane, t_st, *reinterpret_cast<uint32_t(*)[32]>(&hp[0]),
                                     *reinterpret_cast<uint32_t(*)[32]>(&hp[32]));
+                    uint32_t ac[64];
+                    tmem_ld32(tmem + lane_off + KB_COL_S + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&ac[0]));
+                    tmem_ld32(tmem + lane_off + KB_COL_S + 64 * hh + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&ac[32]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    warp_arrive(&sh->s_free);
+                    float win[32];
                     ld_shift_all<0>(t_ld, win);
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
@@ -1139,14 +1246,17 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
     }
 }
 
-// Per query row (8 threads, 8 columns each): lse = max + log2(sum) and
-// D = dout . O_unnorm / sum from the forward statistics of the row's item,
-// and the score operands (q+u)c, (q+v)c rounded to bf16 as the forward
-// rounds them: (float(q) + float(bias)) * c.
+// Per query row (8 threads, 8 columns each): the row's lse (log2 units) and
+// D = dout . out, and the score operands (q+u)c, (q+v)c rounded to bf16 as the
+// forward rounds them: (float(q) + float(bias)) * c.  SAVED: lse and the
+// bf16 output saved by the forward; otherwise from the forward statistics of
+// the row's item: lse = max + log2(sum), D = dout . O_unnorm / sum.
+template <bool SAVED>
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ ub,
                      const __nv_bfloat16* __restrict__ vb, const __nv_bfloat16* __restrict__ dout,
                      const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
+                     const __nv_bfloat16* __restrict__ out, const float* __restrict__ lse_in,
                      __nv_bfloat16* __restrict__ qu, __nv_bfloat16* __restrict__ qv, float2* __restrict__ stats,
                      int n_bh, int H, int L, int n_qtiles, float scale_log2, long long rows) {
     const long long t = (long long)blockIdx.x * 256 + threadIdx.x;
@@ -1157,20 +1267,35 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     const int bh = (int)(rr / L);
     const int i = (int)(rr - (long long)bh * L);
     const int h = bh % H;
-    const long long unit = (long long)(n_qtiles - 1 - i / bw::BM) * n_bh + bh;
-    const int r = i % bw::BM;
     float2 ml = make_float2(0.f, 1.f);
     float d = 0.f;
     if (live) {
-        ml = ws_ml[unit * bw::BM + r];
-        const float4* o4 = reinterpret_cast<const float4*>(ws_o + (unit * bw::BM + r) * bw::DH + 8 * c);
-        const float4 oa = o4[0], ob = o4[1];
+        float o[8];
+        if constexpr (SAVED) {
+            const uint4 ov = *reinterpret_cast<const uint4*>(out + rr * bw::DH + 8 * c);
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(o2[e]);
+                o[2 * e] = f.x;
+                o[2 * e + 1] = f.y;
+            }
+        } else {
+            const long long unit = (long long)(n_qtiles - 1 - i / bw::BM) * n_bh + bh;
+            const int r = i % bw::BM;
+            ml = ws_ml[unit * bw::BM + r];
+            const float4* o4 = reinterpret_cast<const float4*>(ws_o + (unit * bw::BM + r) * bw::DH + 8 * c);
+            const float4 oa = o4[0], ob = o4[1];
+            o[0] = oa.x, o[1] = oa.y, o[2] = oa.z, o[3] = oa.w;
+            o[4] = ob.x, o[5] = ob.y, o[6] = ob.z, o[7] = ob.w;
+        }
         const uint4 g = *reinterpret_cast<const uint4*>(dout + rr * bw::DH + 8 * c);
         const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
-        const float2 g0 = __bfloat1622float2(g2[0]), g1 = __bfloat1622float2(g2[1]);
-        const float2 g2f = __bfloat1622float2(g2[2]), g3 = __bfloat1622float2(g2[3]);
-        d = g0.x * oa.x + g0.y * oa.y + g1.x * oa.z + g1.y * oa.w + g2f.x * ob.x + g2f.y * ob.y + g3.x * ob.z +
-            g3.y * ob.w;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(g2[e]);
+            d += f.x * o[2 * e] + f.y * o[2 * e + 1];
+        }
     }
     d += __shfl_xor_sync(0xffffffffu, d, 1);
     d += __shfl_xor_sync(0xffffffffu, d, 2);
@@ -1191,7 +1316,12 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     }
     *reinterpret_cast<uint4*>(qu + rr * bw::DH + 8 * c) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
     *reinterpret_cast<uint4*>(qv + rr * bw::DH + 8 * c) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-    if (c == 0) stats[rr] = make_float2(ml.x + log2f(ml.y), d / ml.y);
+    if (c == 0) {
+        if constexpr (SAVED)
+            stats[rr] = make_float2(lse_in[rr], d);
+        else
+            stats[rr] = make_float2(ml.x + log2f(ml.y), d / ml.y);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1249,10 +1379,13 @@ size_t attn_bwd_tc_workspace_bytes(int B, int H, int L, int M) {
     return bwd_ws_layout(nullptr, B, H, L).bytes;
 }
 
+// out / lse non-null: the forward's saved output and per-row log2-sum-exp
+// (launch_attn_tc_bf16_lse); otherwise the forward statistics are recomputed
+// into the workspace first.
 cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
-                               const void* vb, const void* dout, int B, int H, int L, int M, float scale, float* dq,
-                               float* dk, float* dv, float* dr, float* du, float* dvb, void* workspace, int* status,
-                               cudaStream_t stream) {
+                               const void* vb, const void* out, const float* lse, const void* dout, int B, int H,
+                               int L, int M, float scale, float* dq, float* dk, float* dv, float* dr, float* du,
+                               float* dvb, void* workspace, int* status, cudaStream_t stream) {
     using namespace bw;
     static PerDeviceOnce attrs;
     {
@@ -1273,14 +1406,26 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     if (e == cudaSuccess) e = cudaMemsetAsync(du, 0, (size_t)H * DH * sizeof(float), stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(dvb, 0, (size_t)H * DH * sizeof(float), stream);
     if (e != cudaSuccess) return e;
-    e = launch_attn_tc_bf16_stats(q, k, v, r, ub, vb, B, H, L, M, scale, w.o, w.ml, status, stream);
-    if (e != cudaSuccess) return e;
+    const bool saved = out && lse;
+    if (!saved) {
+        e = launch_attn_tc_bf16_stats(q, k, v, r, ub, vb, B, H, L, M, scale, w.o, w.ml, status, stream);
+        if (e != cudaSuccess) return e;
+    }
     const long long rows = (long long)n_bh * L;
     const long long threads = rows * 8;
-    attn_bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(ub),
-        static_cast<const __nv_bfloat16*>(vb), static_cast<const __nv_bfloat16*>(dout), w.o, w.ml, w.qu, w.qv,
-        w.stats, n_bh, H, L, n_qtiles, scale * 1.4426950408889634f, rows);
+    const dim3 pgrid((unsigned)((threads + 255) / 256));
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* ubb = static_cast<const __nv_bfloat16*>(ub);
+    const auto* vbb = static_cast<const __nv_bfloat16*>(vb);
+    const auto* gb = static_cast<const __nv_bfloat16*>(dout);
+    const auto* ob = static_cast<const __nv_bfloat16*>(out);
+    const float sl = scale * 1.4426950408889634f;
+    if (saved)
+        attn_bwd_prep_kernel<true><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, nullptr, nullptr, ob, lse, w.qu, w.qv,
+                                                                 w.stats, n_bh, H, L, n_qtiles, sl, rows);
+    else
+        attn_bwd_prep_kernel<false><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, w.o, w.ml, nullptr, nullptr, w.qu,
+                                                                  w.qv, w.stats, n_bh, H, L, n_qtiles, sl, rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

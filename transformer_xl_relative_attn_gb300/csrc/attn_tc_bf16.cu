@@ -151,6 +151,7 @@ struct TcParams {
     int inject;        // 1: withhold the first score-ready signal (timeout test)
     int* status;       // device status word
     int lo_shift;      // keys j < i + 1 - lo_shift are masked too (same_length; 1 << 30: none)
+    float* lse;        // non-null: per-row log2-sum-exp of the scores, [B*H][L]
 };
 
 struct TcShared {
@@ -568,8 +569,14 @@ attn_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 warp_arrive(&sh->o_free);
                 if constexpr (!SPLIT) {
                     const float f0 = has0 ? ex2(m0 - m) : 0.f, f1 = has1 ? ex2(m1 - m) : 0.f;
-                    const float inv = 1.f / ((has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f));
+                    const float lsum = (has0 ? l0 * f0 : 0.f) + (has1 ? l1 * f1 : 0.f);
+                    const float inv = 1.f / lsum;
                     const float a0 = f0 * inv, a1 = f1 * inv;
+                    // the row's log2-sum-exp of the scores (log2 units), kept
+                    // for a backward pass
+                    if (p.lse && grp == 0 && cur.i0 + ii < p.L &&
+                        TXL_BOUNDS(cur.bh < p.B * p.H, 410, cur.bh))
+                        p.lse[(size_t)cur.bh * p.L + cur.i0 + ii] = m + log2f(lsum);
                     // Each warp writes its 32 rows of the group's 32 output columns
                     // with one TMA store of a 32 x 32 box, staged in the upper
                     // 2 KB of the warp's own quarter of the P buffer (free: the
@@ -1029,7 +1036,7 @@ size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M) {
 // item number (no combine pass, `out` is not written).
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
                              const void* vb, int B, int H, int L, int M, float scale, int lo_shift, void* out,
-                             void* workspace, float* stats_o, float2* stats_ml, int inject, int* status,
+                             void* workspace, float* stats_o, float2* stats_ml, float* lse, int inject, int* status,
                              cudaStream_t stream) {
     using namespace tc;
     static PerDeviceOnce attrs;
@@ -1104,6 +1111,8 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
         p.ws_ml = stats_ml;
     }
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse = lse;
+    if (lse && p.nsplit > 1) return cudaErrorInvalidValue;  // the unsplit kernel writes it
     p.inject = inject;
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
@@ -1126,7 +1135,17 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 const void* ub, const void* vb, int B, int H, int L, int M,
                                 float scale, int lo_shift, void* out, void* workspace, int inject,
                                 int* status, cudaStream_t stream) {
-    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, workspace, nullptr, nullptr, inject,
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, workspace, nullptr, nullptr, nullptr,
+                     inject, status, stream);
+}
+
+// The unsplit forward that also leaves each row's log2-sum-exp of the scores
+// in lse [B*H][L] (fp32, log2 units: P = 2^(scale log2 e (AC+BD) - lse)).
+cudaError_t launch_attn_tc_bf16_lse(const void* q, const void* k, const void* v, const void* r, const void* ub,
+                                    const void* vb, int B, int H, int L, int M, float scale, int lo_shift,
+                                    void* out, float* lse, int* status, cudaStream_t stream) {
+    if (!lse) return cudaErrorInvalidValue;
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, nullptr, nullptr, nullptr, lse, 0,
                      status, stream);
 }
 
@@ -1140,7 +1159,7 @@ cudaError_t launch_attn_tc_bf16_stats(const void* q, const void* k, const void* 
                                       float* stats_o, float2* stats_ml, int* status, cudaStream_t stream) {
     if (!stats_o || !stats_ml) return cudaErrorInvalidValue;
     return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, 1 << 30, const_cast<void*>(q), nullptr, stats_o,
-                     stats_ml, 0, status, stream);
+                     stats_ml, nullptr, 0, status, stream);
 }
 
 TXL_BOUNDS_READER(bounds_word_attn_tc)

@@ -34,10 +34,13 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 float scale, int lo_shift, void* out, void* workspace, int inject,
                                 int* status, cudaStream_t stream);
 size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M);
+cudaError_t launch_attn_tc_bf16_lse(const void* q, const void* k, const void* v, const void* r, const void* ub,
+                                    const void* vb, int B, int H, int L, int M, float scale, int lo_shift,
+                                    void* out, float* lse, int* status, cudaStream_t stream);
 cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
-                               const void* vb, const void* dout, int B, int H, int L, int M, float scale, float* dq,
-                               float* dk, float* dv, float* dr, float* du, float* dvb, void* workspace, int* status,
-                               cudaStream_t stream);
+                               const void* vb, const void* out, const float* lse, const void* dout, int B, int H,
+                               int L, int M, float scale, float* dq, float* dk, float* dv, float* dr, float* du,
+                               float* dvb, void* workspace, int* status, cudaStream_t stream);
 size_t attn_bwd_tc_workspace_bytes(int B, int H, int L, int M);
 
 // first bounds violation recorded by each translation unit (bounds-checked
@@ -260,9 +263,69 @@ int txl_attn_bwd_ws(const void* q, const void* k, const void* v, const void* r_k
         if (overlap(workspace, need, others[o], sizes[o])) return TXL_ERR_ALIAS;
     int* status = dev_status_ptr();
     if (!status) return TXL_ERR_CUDA;
-    const cudaError_t e = txl::launch_attn_bwd_tc(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, scale, dq, dk, dv,
-                                                  dr, du, dvb, workspace, status, static_cast<cudaStream_t>(stream));
+    const cudaError_t e =
+        txl::launch_attn_bwd_tc(q, k, v, r_k, u_bias, v_bias, nullptr, nullptr, dout, B, H, L, M, scale, dq, dk, dv,
+                                dr, du, dvb, workspace, status, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;  // tensor-map encoding failed
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_attn_fwd_lse(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                     const void* v_bias, int B, int H, int L, int M, int d_h, float scale, void* out, float* lse,
+                     int dtype, void* stream) {
+    const int rc = check_attn_args(q, k, v, r_k, u_bias, v_bias, B, H, L, M, d_h, out, dtype);
+    if (rc != TXL_OK) return rc;
+    if (dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (!lse) return TXL_ERR_INVALID_ARG;
+    if (!aligned16(lse)) return TXL_ERR_MISALIGNED;
+    const size_t nl = (size_t)B * H * L * sizeof(float), nq = (size_t)B * H * L * d_h * 2,
+                 nkv = (size_t)B * H * ((size_t)M + L) * d_h * 2, nr = ((size_t)M + L) * H * d_h * 2,
+                 nb = (size_t)H * d_h * 2;
+    if (overlap(lse, nl, out, nq) || overlap(lse, nl, q, nq) || overlap(lse, nl, k, nkv) ||
+        overlap(lse, nl, v, nkv) || overlap(lse, nl, r_k, nr) || overlap(lse, nl, u_bias, nb) ||
+        overlap(lse, nl, v_bias, nb))
+        return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    g_inject = 0;
+    const cudaError_t e = txl::launch_attn_tc_bf16_lse(q, k, v, r_k, u_bias, v_bias, B, H, L, M, scale,
+                                                       kNoLowerBound, out, lse, status,
+                                                       static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
+    return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
+}
+
+int txl_attn_bwd_saved(const void* q, const void* k, const void* v, const void* r_k, const void* u_bias,
+                       const void* v_bias, const void* out, const float* lse, const void* dout, int B, int H, int L,
+                       int M, int d_h, float scale, float* dq, float* dk, float* dv, float* dr, float* du,
+                       float* dvb, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+    const int rc = check_bwd_args(q, k, v, r_k, u_bias, v_bias, dout, B, H, L, M, d_h, 0, M, dq, dk, dv, dr, du,
+                                  dvb, dtype);
+    if (rc != TXL_OK) return rc;
+    if (dtype != TXL_BF16 || d_h != 64) return TXL_ERR_UNSUPPORTED;
+    if (!out || !lse) return TXL_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(lse)) return TXL_ERR_MISALIGNED;
+    const size_t need = txl_attn_bwd_workspace_bytes(B, H, L, M, d_h, dtype, 0);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < need) return TXL_ERR_WORKSPACE;
+    const long long K = (long long)M + L;
+    const size_t nq = (size_t)B * H * L * d_h, nkv = (size_t)B * H * K * d_h, nr = (size_t)K * H * d_h,
+                 nb = (size_t)H * d_h, nl = (size_t)B * H * L;
+    const void* others[15] = {q, k, v, r_k, u_bias, v_bias, dout, out, lse, dq, dk, dv, dr, du, dvb};
+    const size_t sizes[15] = {nq * 2, nkv * 2, nkv * 2, nr * 2, nb * 2, nb * 2, nq * 2, nq * 2, nl * 4,
+                              nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
+    for (int o = 0; o < 15; ++o)
+        if (overlap(workspace, need, others[o], sizes[o])) return TXL_ERR_ALIAS;
+    // the gradients must not overlap the saved forward state either
+    const void* gr[6] = {dq, dk, dv, dr, du, dvb};
+    const size_t gn[6] = {nq * 4, nkv * 4, nkv * 4, nr * 4, nb * 4, nb * 4};
+    for (int o = 0; o < 6; ++o)
+        if (overlap(gr[o], gn[o], out, nq * 2) || overlap(gr[o], gn[o], lse, nl * 4)) return TXL_ERR_ALIAS;
+    int* status = dev_status_ptr();
+    if (!status) return TXL_ERR_CUDA;
+    const cudaError_t e =
+        txl::launch_attn_bwd_tc(q, k, v, r_k, u_bias, v_bias, out, lse, dout, B, H, L, M, scale, dq, dk, dv, dr, du,
+                                dvb, workspace, status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return TXL_ERR_CUDA;
     return e == cudaSuccess ? TXL_OK : TXL_ERR_LAUNCH;
 }
 
