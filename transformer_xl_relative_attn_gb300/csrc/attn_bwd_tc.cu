@@ -1089,12 +1089,28 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
         const uint64_t dQv = smem_desc_sw128(s_base + KB_OFF_QV, 16, 1024);
         const uint64_t dRb = smem_desc_sw128(s_base + KB_OFF_R, 16, 1024);
         const uint64_t dPmn = smem_desc_sw128(s_base + KB_OFF_P, SZ_Q, 1024);
-        auto scores = [&](int kitem, int gs_q) {
+        // the position band of step gs_q: once the band of the step before
+        // has been read (its (q+v)c and R loaded)
+        auto band = [&](int gs_q) {
+            wait(&sh->qv_full, gs_q & 1);
+            wait(&sh->r_full, gs_q & 1);
+            if (gs_q > 0) wait(&sh->s_free, (gs_q - 1) & 1);
+            if (!ok) return;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk)
+                mma_ss_elect(tmem + KB_COL_BAND, dQv + 2 * kk, dRb + 2 * kk, IDESC_N256, kk > 0, leader);
+            if (leader) {
+                mma_commit(&sh->qv_empty);
+                mma_commit(&sh->r_empty);
+            }
+        };
+        // AC of step gs_q into S once dP of the step before has been read;
+        // the step's scores are then complete
+        auto ac = [&](int kitem, int gs_q) {
             const int stg = gs_q & 1;
             wait(&sh->kv_full[kitem & 1], (kitem >> 1) & 1);
             wait(&sh->q_full[stg], (gs_q >> 1) & 1);
-            wait(&sh->qv_full, gs_q & 1);
-            wait(&sh->r_full, gs_q & 1);
             if (gs_q > 0) wait(&sh->dp_free, (gs_q - 1) & 1);
             if (!ok) return;
             tc_fence_after();
@@ -1103,24 +1119,21 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
 #pragma unroll
             for (int kk = 0; kk < DH / 16; ++kk)
                 mma_ss_elect(tmem + KB_COL_S, aQ + 2 * kk, bK + 2 * kk, IDESC_N128, kk > 0, leader);
-#pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk)
-                mma_ss_elect(tmem + KB_COL_BAND, dQv + 2 * kk, dRb + 2 * kk, IDESC_N256, kk > 0, leader);
-            if (leader) {
-                mma_commit(&sh->s_full);
-                mma_commit(&sh->qv_empty);
-                mma_commit(&sh->r_empty);
-            }
+            if (leader) mma_commit(&sh->s_full);
         };
         int gs = 0;
         KbItem it, nx;
         bool have = kb_item(p, 0, it);
-        if (have) scores(0, 0);
+        if (have) {
+            band(0);
+            ac(0, 0);
+        }
         for (int k = 0; ok && have; ++k) {
             const bool have_next = kb_item(p, k + 1, nx);
             for (int q = 0; ok && q < it.nsteps; ++q) {
                 const int gs_q = gs + q;
                 const int stg = gs_q & 1;
+                const bool more = q + 1 < it.nsteps || have_next;  // a next step exists
                 // dP into S once the scores have been read
                 wait(&sh->s_free, gs_q & 1);
                 if (!ok) break;
@@ -1131,6 +1144,8 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
                 for (int kk = 0; kk < DH / 16; ++kk)
                     mma_ss_elect(tmem + KB_COL_S, aDO + 2 * kk, bV + 2 * kk, IDESC_N128, kk > 0, leader);
                 if (leader) mma_commit(&sh->dp_full);
+                // the next step's band as soon as this one's has been read
+                if (more) band(gs_q + 1);
                 // dV += P^T dout: A = P read transposed (M = 128 keys in two
                 // 64-key halves 16 KB apart, K = 128 query rows)
                 wait(&sh->pt_full, gs_q & 1);
@@ -1142,12 +1157,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
                     mma_ss_elect(tmem + KB_COL_DV, dPmn + kk * 128, bDOmn + kk * 128, IDESC_N64_ABMN,
                                  (q > 0 || kk > 0) ? 1u : 0u, leader);
                 if (leader) mma_commit(&sh->pv_done);
-                // the next step's scores (the next item's first step after
-                // this item's last)
+                // the next step's AC (of the next item after this item's last step)
                 if (q + 1 < it.nsteps)
-                    scores(k, gs_q + 1);
+                    ac(k, gs_q + 1);
                 else if (have_next)
-                    scores(k + 1, gs_q + 1);
+                    ac(k + 1, gs_q + 1);
                 if (!ok) break;
                 // dK += dS^T (q+u)c
                 wait(&sh->ds_full, gs_q & 1);
