@@ -93,15 +93,24 @@ ln = txl.layer_norm(hx.cuda(), gam.cuda(), bet.cuda(), y=hx.cuda())
 rl = oracle.layer_norm(hx.double().numpy() * 2, gam, bet)
 assert np.abs(ln.float().cpu().double().numpy() - rl).max() <= tol(rl)
 
-# backward: fp32 (one row per warp above d_h 64, tiled below) and bf16
-for dt, dh, rt, at in [(torch.float32, 32, 1e-4, 1e-5), (torch.float32, 128, 1e-4, 1e-5), (bf, 64, 1e-2, 1e-3)]:
-    ci = W.random_call_inputs(1, 2, 40, 24, dh, dtype=dt, std=0.5, seed=dh)
-    gout = torch.randn(1, 2, 40, dh, generator=g).to(dt)
-    got = txl.attn_bwd(*dev(ci), gout.cuda(), ci.scale)
+# backward: fp32 (one row per warp above d_h 64, tiled below), bf16 on the
+# CUDA cores and on the tensor cores (several query and key tiles, ragged),
+# and the tensor-core backward from the forward's saved out and lse
+cases = [(torch.float32, 32, 40, 24, 1e-4, 1e-5, "cc"), (torch.float32, 128, 40, 24, 1e-4, 1e-5, "cc"),
+         (bf, 64, 40, 24, 1e-2, 1e-3, "cc"), (bf, 64, 200, 100, 1e-2, 1e-3, "tc"),
+         (bf, 64, 200, 100, 1e-2, 1e-3, "saved")]
+for dt, dh, Lq, Mq, rt, at, path in cases:
+    ci = W.random_call_inputs(1, 2, Lq, Mq, dh, dtype=dt, std=0.5, seed=dh + Lq)
+    gout = torch.randn(1, 2, Lq, dh, generator=g).to(dt)
+    if path == "saved":
+        o_s, lse_s = txl.attn_fwd_lse(*dev(ci), scale=ci.scale)
+        got = txl.attn_bwd(*dev(ci), gout.cuda(), ci.scale, out=o_s, lse=lse_s)
+    else:
+        got = txl.attn_bwd(*dev(ci), gout.cuda(), ci.scale, tensor_cores=(path == "tc"))
     ref = oracle.attn_bwd(ci.q, ci.k, ci.v, ci.r_k, ci.u, ci.vb, ci.scale, gout)
     for n in ("dq", "dk", "dv", "dr", "du", "dvb"):
         r = ref[n]
-        assert np.abs(got[n].cpu().double().numpy() - r).max() <= rt * np.abs(r).max() + at, n
+        assert np.abs(got[n].cpu().double().numpy() - r).max() <= rt * np.abs(r).max() + at, (path, n)
 
 torch.cuda.synchronize()
 assert txl.sync_status() == 0

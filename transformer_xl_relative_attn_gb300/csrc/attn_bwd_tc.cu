@@ -73,11 +73,11 @@ constexpr int QA_G = 4;      // G ring (band slots of dS) in shared memory
 constexpr int QA_RING = 3;   // position slots in TMEM: tile t reads slots t, t+1, t+2
 constexpr uint32_t QA_OFF_QU = 0;
 constexpr uint32_t QA_OFF_DO = QA_OFF_QU + SZ_Q;
-constexpr uint32_t QA_OFF_QV = QA_OFF_DO + SZ_Q;          // buffer b (item parity) at +16K*b
-constexpr uint32_t QA_OFF_KV = QA_OFF_QV + 2 * SZ_Q;      // stage s: K at +16K*s, V at +16K*s+8K
+constexpr uint32_t QA_OFF_QV = QA_OFF_DO + SZ_Q;
+constexpr uint32_t QA_OFF_KV = QA_OFF_QV + SZ_Q;          // stage s: K at +16K*s, V at +16K*s+8K
 constexpr uint32_t QA_OFF_R = QA_OFF_KV + QA_KV * 2 * SZ_T;
-constexpr uint32_t QA_OFF_DS = QA_OFF_R + QA_RB * SZ_Q;   // dS tile; also the per-row shift scratch
-constexpr uint32_t QA_OFF_G = QA_OFF_DS + SZ_Q;           // G slot g at +16K*g
+constexpr uint32_t QA_OFF_DS = QA_OFF_R + QA_RB * SZ_Q;   // dS tiles (tile parity); each also the shift scratch
+constexpr uint32_t QA_OFF_G = QA_OFF_DS + 2 * SZ_Q;       // G slot g at +16K*g
 constexpr uint32_t QA_OFF_BAR = QA_OFF_G + QA_G * SZ_Q;
 constexpr uint32_t QA_SMEM = QA_OFF_BAR + 1024 + 1024;
 static_assert(QA_SMEM <= 232448, "shared memory budget of one sm_103a CTA");
@@ -128,12 +128,12 @@ struct QaShared {
     uint64_t kv_full[bw::QA_KV], kv_empty[bw::QA_KV];
     uint64_t r_full[bw::QA_RB], r_empty[bw::QA_RB];
     uint64_t qa_full, qa_empty;    // (q+u)c and dout of the item landed / no longer read
-    uint64_t qv_full[2], qv_empty[2];  // (q+v)c of the item (buffer = item parity)
+    uint64_t qv_full, qv_empty;    // (q+v)c of the item
     uint64_t s_full, s_free;     // AC and the tile's band slots are in TMEM / have been read
     uint64_t dp_full, dp_free;   // dP of the tile is in TMEM / has been read
-    uint64_t ds_full;            // the dS tile is in shared memory
-    uint64_t ds_read;            // the flush warps have read it
-    uint64_t dqc_done;           // the dq_c MMA that reads it completed
+    uint64_t ds_full[2];         // dS tile b (tile parity) is in shared memory
+    uint64_t ds_read[2];         // the flush warps have read dS tile b
+    uint64_t dqc_done[2];        // the dq_c MMA that reads dS tile b completed
     uint64_t g_full;             // the tile's band scatter is in G
     uint64_t post;               // the MMAs after the scatter (and all before) completed
     uint64_t dr_full, dr_free;   // a dR pair is in TMEM / the flush warps read it
@@ -348,17 +348,17 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
         }
         mbar_init(&sh->qa_full, 1);
         mbar_init(&sh->qa_empty, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sh->qv_full[b], 1);
-            mbar_init(&sh->qv_empty[b], 2);
-        }
+        mbar_init(&sh->qv_full, 1);
+        mbar_init(&sh->qv_empty, 2);
         mbar_init(&sh->s_full, 1);
         mbar_init(&sh->s_free, 4);
         mbar_init(&sh->dp_full, 1);
         mbar_init(&sh->dp_free, 4);
-        mbar_init(&sh->ds_full, 4);
-        mbar_init(&sh->ds_read, 4);
-        mbar_init(&sh->dqc_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh->ds_full[b], 4);
+            mbar_init(&sh->ds_read[b], 4);
+            mbar_init(&sh->dqc_done[b], 1);
+        }
         mbar_init(&sh->g_full, 4);
         mbar_init(&sh->post, 1);
         mbar_init(&sh->dr_full, 1);
@@ -382,9 +382,9 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
         const int wq = warp;
         const int ii = tid;                      // query row within the item
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        // the warp's quarter of the dS tile doubles as its shift scratch
-        const uint32_t t_ld = ds_tile + wq * 4096 + 4 * lane;
-        const uint32_t t_st = t_ld - 128u * (uint32_t)(31 - lane);
+        // the warp's quarter of the tile's dS buffer doubles as its shift
+        // scratch (written by this tile, read by tile t-2's MMA and flush)
+        const uint32_t t_ld0 = ds_tile + wq * 4096 + 4 * lane;
         bool ok = true;
         int gt = 0, gring = 0;  // global tile, global position slot of the item's slot 0
         QaItem it;
@@ -397,6 +397,9 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 Dv = st.y;
             }
             for (int t = 0; t < it.nt; ++t, ++gt) {
+                const int db = gt & 1;  // dS buffer of the tile
+                const uint32_t t_ld = t_ld0 + db * SZ_Q;
+                const uint32_t t_st = t_ld - 128u * (uint32_t)(31 - lane);
                 ok = __all_sync(0xffffffffu, mbar_wait(&sh->s_full, gt & 1, kDevTimeoutSoftmax, abort, p.status));
                 if (!ok) break;
                 tc_fence_after();
@@ -418,13 +421,13 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                         for (int K = 0; K < 64; ++K)
                             hp[K] = pack_f16x2_sat(__uint_as_float(bwv[K]), __uint_as_float(bwv[K + 32]));
                     }
-                    // the scratch (the dS tile) is free once the previous
-                    // tile's dq_c MMA and the flush warps have read it
-                    if (gt > 0) {
-                        ok = __all_sync(0xffffffffu, mbar_wait(&sh->dqc_done, (gt - 1) & 1, kDevTimeoutSoftmax,
-                                                               abort, p.status) &&
-                                                         mbar_wait(&sh->ds_read, (gt - 1) & 1, kDevTimeoutSoftmax,
-                                                                   abort, p.status));
+                    // the scratch (this tile's dS buffer) is free once tile
+                    // gt-2's dq_c MMA and the flush warps have read it
+                    if (gt >= 2) {
+                        const uint32_t ph = ((gt - 2) >> 1) & 1;
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&sh->dqc_done[db], ph, kDevTimeoutSoftmax, abort, p.status) &&
+                                            mbar_wait(&sh->ds_read[db], ph, kDevTimeoutSoftmax, abort, p.status));
                     }
                     if (!ok) break;
                     __syncwarp();
@@ -474,12 +477,12 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 __syncwarp();  // every lane's scratch reads precede the dS rows
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint32_t a = ds_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4);
+                    const uint32_t a = ds_tile + db * SZ_Q + ii * 128 + ((c8 ^ (ii & 7)) << 4);
                     if (QA_SMEM_IN(a, 16, 702))
                         st_shared_v4(a, w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 }
                 fence_proxy_async_smem();
-                warp_arrive(&sh->ds_full);
+                warp_arrive(&sh->ds_full[db]);
             }
             gring += it.nt + 2;
         }
@@ -501,10 +504,9 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
         int gt = 0, rbox = 0, gring = 0;
         QaItem it;
         for (int k = 0; ok && qa_item(p, k, it); ++k) {
-            const int qb = k & 1;  // (q+v)c buffer of the item
             wait(&sh->qa_full, k & 1);
-            wait(&sh->qv_full[qb], (k >> 1) & 1);
-            const uint64_t aQv = dQv + qb * U_Q;
+            wait(&sh->qv_full, k & 1);
+            const uint64_t aQv = dQv;
             for (int t = 0; ok && t < it.nt; ++t) {
                 const int gt_t = gt + t;
                 const int st = gt_t % QA_KV;
@@ -535,7 +537,7 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                     mma_ss_elect(tmem + QA_COL_S, dQu + 2 * kk, bK + 2 * kk, IDESC_N64, kk > 0, leader);
                 if (leader) {
                     mma_commit(&sh->s_full);
-                    if (last) mma_commit(&sh->qv_empty[qb]);
+                    if (last) mma_commit(&sh->qv_empty);
                 }
                 // dP(t) once the softmax has read dP(t-1)
                 if (gt_t > 0) wait(&sh->dp_free, (gt_t - 1) & 1);
@@ -565,7 +567,6 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
             int kvc = 0;
             QaItem it;
             for (int k = 0; ok && qa_item(p, k, it); ++k) {
-                const int qb = k & 1;
                 if (k > 0 && !mbar_wait(&sh->qa_empty, (k - 1) & 1, kDevTimeoutProducer, abort, p.status)) {
                     ok = false;
                     break;
@@ -573,13 +574,12 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 mbar_expect_tx(&sh->qa_full, 2 * SZ_Q);
                 tma_load_3d(smem + QA_OFF_QU, &tmQu, &sh->qa_full, 0, it.i0, it.bh);
                 tma_load_3d(smem + QA_OFF_DO, &tmDO, &sh->qa_full, 0, it.i0, it.bh);
-                if (k >= 2 && !mbar_wait(&sh->qv_empty[qb], ((k >> 1) & 1) ^ 1, kDevTimeoutProducer, abort,
-                                         p.status)) {
+                if (k > 0 && !mbar_wait(&sh->qv_empty, (k - 1) & 1, kDevTimeoutProducer, abort, p.status)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&sh->qv_full[qb], SZ_Q);
-                tma_load_3d(smem + QA_OFF_QV + qb * SZ_Q, &tmQv, &sh->qv_full[qb], 0, it.i0, it.bh);
+                mbar_expect_tx(&sh->qv_full, SZ_Q);
+                tma_load_3d(smem + QA_OFF_QV, &tmQv, &sh->qv_full, 0, it.i0, it.bh);
                 for (int t = 0; t < it.nt; ++t, ++kvc) {
                     const int s = kvc % QA_KV;
                     if (kvc >= QA_KV && !mbar_wait(&sh->kv_empty[s], ((kvc / QA_KV) & 1) ^ 1,
@@ -636,15 +636,18 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
             int next_dr = 0;
             for (int t = 0; t < it.nt; ++t, ++gt) {
                 const bool last = t == it.nt - 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(&sh->ds_full, gt & 1, kDevTimeoutSoftmax, abort, p.status));
+                // one barrier per dS buffer: the softmax can finish tile gt+1
+                // before this warp has seen tile gt, never tile gt+2
+                ok = __all_sync(0xffffffffu, mbar_wait(&sh->ds_full[gt & 1], (gt >> 1) & 1, kDevTimeoutSoftmax,
+                                                       abort, p.status));
                 if (!ok) break;
                 uint32_t w[32];
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint32_t a = ds_tile + ii * 128 + ((c8 ^ (ii & 7)) << 4);
+                    const uint32_t a = ds_tile + (gt & 1) * SZ_Q + ii * 128 + ((c8 ^ (ii & 7)) << 4);
                     if (QA_SMEM_IN(a, 16, 708)) ld_shared_v4u(a, w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 }
-                warp_arrive(&sh->ds_read);
+                warp_arrive(&sh->ds_read[gt & 1]);
                 // the G positions of slots t .. t+2 are free once the MMAs
                 // after the previous tile's scatter completed
                 if (gt > 0)
@@ -780,8 +783,7 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
         QaItem it;
         for (int k = 0; ok && qa_item(p, k, it); ++k) {
             const int nb = (it.nt + 3) >> 1;
-            const int qb = k & 1;
-            const uint64_t bQv = dQvmn + qb * U_Q;
+            const uint64_t bQv = dQvmn;
             int next_dr = 0;
             for (int t = 0; ok && t < it.nt; ++t) {
                 const int gt_t = gt + t;
@@ -790,17 +792,18 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 // dq_c(t) once the dS tile is in shared memory (the item's
                 // first one overwrites dq_c: the flush warps have read the
                 // previous item's)
-                wait(&sh->ds_full, gt_t & 1);
+                wait(&sh->ds_full[gt_t & 1], (gt_t >> 1) & 1);
                 if (t == 0 && k > 0) wait(&sh->dq_free, (k - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t bKmn = dKmn + st * 2 * U_T;
+                const uint64_t aDS = dDS + (gt_t & 1) * U_Q;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ss_elect(tmem + QA_COL_DQC, dDS + 2 * kk, bKmn + kk * 128, IDESC_N64_BMN,
+                    mma_ss_elect(tmem + QA_COL_DQC, aDS + 2 * kk, bKmn + kk * 128, IDESC_N64_BMN,
                                  (kk > 0 || t > 0) ? 1u : 0u, leader);
                 if (leader) {
-                    mma_commit(&sh->dqc_done);
+                    mma_commit(&sh->dqc_done[gt_t & 1]);
                     mma_commit(&sh->kv_empty[st]);
                 }
                 // dq_p of the band slots complete after tile t and dR of the
@@ -839,7 +842,7 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
                 if (leader) {
                     mma_commit(&sh->post);
                     if (last) {
-                        mma_commit(&sh->qv_empty[qb]);
+                        mma_commit(&sh->qv_empty);
                         mma_commit(&sh->dq_done);
                     }
                 }
