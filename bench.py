@@ -407,8 +407,9 @@ def run_ours(args, wl: W.Workload):
 # the kernel sources still hash to what was captured.
 _TRAFFIC_CAPTURES = {
     "base512_bf16": {
-        "sha256_prefix": {"attn_tc_bf16.cu": "65f190f09bc5e539", "txl_device.cuh": "cba029d3671e08e1"},
-        "bytes_per_launch": 60094592,
+        "sha256_prefix": {"attn_tc_bf16.cu": "b2034ff4669e1950", "txl_device.cuh": "77bcc7df07e42fb8",
+                          "attn_tc_common.cuh": "a91b70485c74670f"},
+        "bytes_per_launch": 60269056,
         "summary": "profiles/attn_tc_bf16_base512_ncu_full.md",
     },
 }
