@@ -63,10 +63,10 @@ constexpr float kLn2 = 0.69314718055994531f;
 
 // ---- attn_bwd_q_kernel (query-major)
 // warps 0-3 softmax (one query row per thread), 4 score issuer (AC, the
-// position slots, dP), 5 TMA producer (lane 0: q-side tiles and K/V, lane 1:
-// R boxes), 6-9 band scatter / dR / dq (row quarter w%4), 10 gradient issuer
-// (dq_c, dq_p, dR)
-constexpr int QA_THREADS = 352;
+// position slots, dP), 5 TMA producer of the q-side tiles and K/V, 6-9 band
+// scatter / dR / dq (row quarter w%4), 10 gradient issuer (dq_c, dq_p, dR),
+// 11 TMA producer of the R boxes
+constexpr int QA_THREADS = 384;
 constexpr int QA_KV = 2;     // K/V ring, one 64-key tile per stage
 constexpr int QA_RB = 3;     // R ring, one 128-row box (two band slots) per stage
 constexpr int QA_G = 4;      // G ring (band slots of dS) in shared memory
@@ -87,9 +87,10 @@ constexpr uint32_t QA_COL_S = 0, QA_COL_DP = 64, QA_COL_RING = 128, QA_COL_DR = 
 
 // ---- attn_bwd_kv_kernel (key-major)
 // warps 0-7 softmax (two threads per query row: warp w takes keys 64 (w/4)
-// .. of the block, rows of lane quarter w%4), 8 MMA issuer, 9 TMA producer
-// (lane 0: K/V and the q-side stages, lane 1: (q+v)c and the R band)
-constexpr int KB_THREADS = 320;
+// .. of the block, rows of lane quarter w%4), 8 MMA issuer, 9 TMA producer of
+// K/V and the q-side stages, 10 TMA producer of (q+v)c and the R band (a warp
+// of its own: two lanes of one warp in blocking waits hold each other up)
+constexpr int KB_THREADS = 352;
 constexpr uint32_t KB_OFF_KV = 0;                       // buffer b: K at +32K*b, V at +32K*b+16K
 constexpr uint32_t KB_OFF_ST = KB_OFF_KV + 4 * SZ_Q;    // stage s: (q+u)c at +32K*s, dout at +32K*s+16K
 constexpr uint32_t KB_OFF_QV = KB_OFF_ST + 4 * SZ_Q;
@@ -595,7 +596,11 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
             }
             for (int c = kvc - QA_KV; c < kvc; ++c)
                 if (c >= 0) drain_wait(&sh->kv_full[c % QA_KV], (c / QA_KV) & 1, p.status);
-        } else if (lane == 1) {
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        // -------------------------------------------- TMA producer: R boxes
+        if (lane == 0) {
             bool ok = true;
             int rc = 0;
             QaItem it;
@@ -762,7 +767,7 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
             gslot += qa_slots(it.nt);
         }
         tc_fence_before();
-    } else {
+    } else if (warp == 10) {
         // --------------------------------------- gradient issuer: dq_c, dq_p, dR
         const uint32_t leader = elect_one();
         bool ok = true;
@@ -1225,7 +1230,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
                 if (c >= 0) drain_wait(&sh->kv_full[c & 1], (c >> 1) & 1, p.status);
             for (int c = gs - 2; c < gs; ++c)
                 if (c >= 0) drain_wait(&sh->q_full[c & 1], (c >> 1) & 1, p.status);
-        } else if (lane == 1) {
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------- TMA producer: (q+v)c and the R band per step
+        if (lane == 0) {
             // (q+v)c and the 256-row R band per step (single buffers: the
             // band MMA is their only reader, early in the step)
             bool ok = true;
@@ -1254,7 +1263,6 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
         }
         __syncwarp();
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 8) {
