@@ -374,6 +374,10 @@ attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The prep kernel's outputs (and the zeroed dR, du, dv_bias) are
+    // complete: this grid starts after it.  The key-major pass, which reads
+    // none of this kernel's outputs, may be scheduled on the SMs it leaves.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t tmem = sh->tmem_base;
     volatile int* abort = &sh->abort;
     const uint32_t ds_tile = s_base + QA_OFF_DS;
@@ -1269,6 +1273,10 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // Launched as a programmatic dependent of the query-major pass and
+    // independent of it; this grid completes only after that pass completed,
+    // so work after it in the stream sees every gradient.
+    if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Per query row (8 threads, 8 columns each): the row's lse (log2 units) and
@@ -1283,8 +1291,17 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
                      const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
                      const __nv_bfloat16* __restrict__ out, const float* __restrict__ lse_in,
                      __nv_bfloat16* __restrict__ qu, __nv_bfloat16* __restrict__ qv, float2* __restrict__ stats,
-                     int n_bh, int H, int L, int n_qtiles, float scale_log2, long long rows) {
+                     int n_bh, int H, int L, int n_qtiles, float scale_log2, long long rows,
+                     float4* __restrict__ dr, int n_dr4, float4* __restrict__ du, float4* __restrict__ dvb,
+                     int n_b4) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long t = (long long)blockIdx.x * 256 + threadIdx.x;
+    // dR, du and dv_bias are sums the query-major pass accumulates: zeroed here
+    for (long long z = t; z < n_dr4; z += (long long)gridDim.x * 256) dr[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < n_b4) {
+        du[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dvb[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const long long row = t >> 3;
     const int c = (int)(t & 7);
     const bool live = row < rows;
@@ -1387,14 +1404,22 @@ BwdWs bwd_ws_layout(void* base, int B, int H, int L) {
 }
 
 template <typename Kern>
-cudaError_t launch_bwd_kernel(Kern kern, int grid, int threads, uint32_t smem, cudaStream_t stream,
+cudaError_t launch_bwd_kernel(Kern kern, int grid, int threads, uint32_t smem, cudaStream_t stream, bool pdl,
                               const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& d,
                               const CUtensorMap& e, const CUtensorMap& f, const BwdParams& p) {
+    // pdl: programmatic stream serialisation, the kernel may be scheduled
+    // before the previous one in the stream completed (the kernel states
+    // what it waits for)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, a, b, c, d, e, f, p);
 }
 }  // namespace
@@ -1427,10 +1452,7 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     const int n_bh = B * H;
     const int n_qtiles = (L + BM - 1) / BM;
     const BwdWs w = bwd_ws_layout(workspace, B, H, L);
-    cudaError_t e = cudaMemsetAsync(dr, 0, (size_t)K * H * DH * sizeof(float), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(du, 0, (size_t)H * DH * sizeof(float), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dvb, 0, (size_t)H * DH * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const bool saved = out && lse;
     if (!saved) {
         e = launch_attn_tc_bf16_stats(q, k, v, r, ub, vb, B, H, L, M, scale, w.o, w.ml, status, stream);
@@ -1445,12 +1467,18 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     const auto* gb = static_cast<const __nv_bfloat16*>(dout);
     const auto* ob = static_cast<const __nv_bfloat16*>(out);
     const float sl = scale * 1.4426950408889634f;
+    auto* dr4 = reinterpret_cast<float4*>(dr);
+    auto* du4 = reinterpret_cast<float4*>(du);
+    auto* dvb4 = reinterpret_cast<float4*>(dvb);
+    const int n_dr4 = K * H * DH / 4, n_b4 = H * DH / 4;
     if (saved)
         attn_bwd_prep_kernel<true><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, nullptr, nullptr, ob, lse, w.qu, w.qv,
-                                                                 w.stats, n_bh, H, L, n_qtiles, sl, rows);
+                                                                 w.stats, n_bh, H, L, n_qtiles, sl, rows, dr4, n_dr4,
+                                                                 du4, dvb4, n_b4);
     else
         attn_bwd_prep_kernel<false><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, w.o, w.ml, nullptr, nullptr, w.qu,
-                                                                  w.qv, w.stats, n_bh, H, L, n_qtiles, sl, rows);
+                                                                  w.qv, w.stats, n_bh, H, L, n_qtiles, sl, rows, dr4,
+                                                                  n_dr4, du4, dvb4, n_b4);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -1497,11 +1525,14 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     p.status = status;
     const int sms = current_sm_count();
     p.n_items = n_bh * n_qtiles;
-    e = launch_bwd_kernel(attn_bwd_q_kernel, p.n_items < sms ? p.n_items : sms, QA_THREADS, QA_SMEM, stream, mQu,
+    // the query-major pass starts once the prep kernel completed (its
+    // full-SM CTAs launched early would take the SMs the prep blocks still
+    // need); the key-major pass may start on each SM it leaves
+    e = launch_bwd_kernel(attn_bwd_q_kernel, p.n_items < sms ? p.n_items : sms, QA_THREADS, QA_SMEM, stream, false, mQu,
                           mQv, mDO, mKa, mVa, mR, p);
     if (e != cudaSuccess) return e;
     p.n_items = n_bh * p.n_ktiles;
-    return launch_bwd_kernel(attn_bwd_kv_kernel, p.n_items < sms ? p.n_items : sms, KB_THREADS, KB_SMEM, stream, mQu,
+    return launch_bwd_kernel(attn_bwd_kv_kernel, p.n_items < sms ? p.n_items : sms, KB_THREADS, KB_SMEM, stream, true, mQu,
                              mQv, mDO, mKb, mVb, mR, p);
 }
 
