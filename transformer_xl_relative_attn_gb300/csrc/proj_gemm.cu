@@ -20,7 +20,8 @@
 // loads, warp 1 issues the MMAs (whole warp, one elected lane: M=128, N=256,
 // K=16 per instruction into a TMEM accumulator), warps 4-11 drain the
 // accumulator (one row per thread; warps w and w+4 split the 256 columns) to
-// bf16 global stores, with the optional bias / ReLU / residual epilogue.  Two accumulators of
+// bf16, with the optional bias / ReLU / residual epilogue, and write it by
+// TMA stores of staged 64-column slices.  Two accumulators of
 // 256 columns let the epilogue of one tile overlap the MMAs of the next.
 // Every wait is bounded (1 s) and reports through the device status word.
 #include <cstdint>
@@ -68,15 +69,17 @@ constexpr int MAX_STAGES = 6;
 template <int BN_>
 struct Cfg {
     static constexpr int BN = BN_;
-    // measured: 3 stages beat 4 for 256-column tiles (q/k/v 30.6 -> 29.4 us,
-    // first feed-forward 25.3 -> 24.1 us at base512); 128-column tiles want 6
-    static constexpr int STAGES = BN_ == 256 ? 3 : 6;
+    // measured at base512: 4 stages of 48 KB with one staged output slice per
+    // epilogue warp beat 3 stages with two (q/k/v 28.3 -> 26.6 us): the MMAs
+    // wait on the TMA loads, so bytes in flight count; 128-column tiles want 6
+    static constexpr int STAGES = BN_ == 256 ? 4 : 6;
     static constexpr uint32_t SZ_B = BN_ * BK * 2;   // 32 or 16 KB
     static constexpr uint32_t OFF_B = OFF_A + STAGES * SZ_A;
-    // output staging: each of the 8 epilogue warps, 32 rows x BN / 2 columns
-    // in 64-column slices of 4 KB (128-byte rows, 128-byte swizzle)
+    // output staging: each of the 8 epilogue warps stages one 64-column slice
+    // of its 32 rows at a time (4 KB, 128-byte rows, 128-byte swizzle) and
+    // waits until the slice's TMA store has read it before staging the next
     static constexpr uint32_t OFF_STG = OFF_B + STAGES * SZ_B;
-    static constexpr uint32_t OFF_BAR = OFF_STG + 8 * 32 * (BN_ / 2) * 2;
+    static constexpr uint32_t OFF_BAR = OFF_STG + 8 * 4096;  // one 64-column slice per warp
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 2 * BN_;  // two accumulators
     static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_, 0);
@@ -287,7 +290,7 @@ proj_gemm_kernel(const __grid_constant__ PgIn inm, const __grid_constant__ PgOut
         constexpr int CPW = BN / 64;         // 32-column chunks per epilogue warp
         const int row = wq * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t stg = s_base + C::OFF_STG + (uint32_t)(warp - 4) * 32 * (BN / 2) * 2;
+        const uint32_t stg = s_base + C::OFF_STG + (uint32_t)(warp - 4) * 4096;
         bool store_pending = false;  // lane 0: this warp's last stores may still read the staging
         bool ok = true;
         int j = 0;
@@ -301,13 +304,15 @@ proj_gemm_kernel(const __grid_constant__ PgIn inm, const __grid_constant__ PgOut
             const int g = pg_tile<BN>(p, w, b, t0, n0);
             const PgProblem& pr = p.pr[g];
             const int t = t0 + row;
-            if (store_pending) {
-                bulk_wait_read();  // the previous tile's slices have been read
-                store_pending = false;
-            }
-            __syncwarp();
 #pragma unroll 1
             for (int cc = CPW * chalf; cc < CPW * chalf + CPW; ++cc) {
+                if ((cc & 1) == 0) {
+                    if (store_pending) {
+                        bulk_wait_read();  // the previous slice has been read
+                        store_pending = false;
+                    }
+                    __syncwarp();
+                }
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_off + acc * BN + 32 * cc, v);
                 tmem_wait_ld();
@@ -371,7 +376,7 @@ proj_gemm_kernel(const __grid_constant__ PgIn inm, const __grid_constant__ PgOut
                 // stage the 32 columns in the warp's 64-column slice (row = lane,
                 // 16-byte chunk c at c ^ (lane & 7)); a full slice goes out as one
                 // TMA store of 32 rows
-                const uint32_t slice = stg + (uint32_t)((cc - CPW * chalf) >> 1) * 4096;
+                const uint32_t slice = stg;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c16 = 4 * (cc & 1) + q;
