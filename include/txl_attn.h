@@ -271,12 +271,13 @@ int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, c
  * input ("Transformer-XL" notes, section "Segment-Level Recurrence"), in four
  * launches on `stream`: the forward kernel computes each query row's softmax
  * statistics into the workspace; a small kernel turns them into lse and
- * D = dout . out per row and writes (q+u) and (q+v) scaled by scale * log2 e
- * in bf16; a query-major pass recomputes P, dP and dS per 128-row query tile
- * and writes dq and accumulates dr, du, dvb; a key-major pass recomputes
- * them per 128-key tile and writes dk, dv.  dr, du and dvb are zeroed and
- * accumulated with fp32 atomics (summation order not fixed); dq, dk and dv
- * are written once per element.  Contractions in bf16 with fp32
+ * D = dout . out per row, writes (q+u) and (q+v) scaled by scale * log2 e
+ * in bf16 and zeroes dr, du, dvb; a query-major pass recomputes P, dP and dS
+ * per 128-row query tile and writes dq and accumulates dr, du, dvb; a
+ * key-major pass recomputes them per 128-key tile and writes dk, dv (it may
+ * start on the SMs the query-major pass leaves; the call's last launch
+ * completes after both).  dr, du and dvb are accumulated with fp32 atomics
+ * (summation order not fixed); dq, dk and dv are written once per element.  Contractions in bf16 with fp32
  * accumulation: P and dS are rounded to bf16 before their products.
  *
  * workspace: device memory owned by the caller, 256-byte aligned, at least
