@@ -407,9 +407,9 @@ def run_ours(args, wl: W.Workload):
 # the kernel sources still hash to what was captured.
 _TRAFFIC_CAPTURES = {
     "base512_bf16": {
-        "sha256_prefix": {"attn_tc_bf16.cu": "b2034ff4669e1950", "txl_device.cuh": "77bcc7df07e42fb8",
+        "sha256_prefix": {"attn_tc_bf16.cu": "7dd2381a9b741c12", "txl_device.cuh": "77bcc7df07e42fb8",
                           "attn_tc_common.cuh": "a91b70485c74670f"},
-        "bytes_per_launch": 60269056,
+        "bytes_per_launch": 60071552,
         "summary": "profiles/attn_tc_bf16_base512_ncu_full.md",
     },
 }
@@ -834,7 +834,7 @@ def time_backward(wl, calls, rks, u, vb, dev, peak_tf=None, peak_src=""):
     flops = 12 * wl.dh * wl.B * wl.H * wl.visible_pairs()
     tf = flops / (ms * 1e-3) / 1e12
     if need:
-        kern = "forward statistics + attn_bwd_prep_kernel + attn_bwd_q_kernel + attn_bwd_kv_kernel"
+        kern = "attn_tc_bf16_kernel (the forward with lse) + attn_bwd_prep_kernel + attn_bwd_q_kernel + attn_bwd_kv_kernel"
         bound, peak, psrc = "tensor", peak_tf, f"bf16_tflops, burst ({peak_src})"
     else:
         kern = "attn_bwd_tiled_kernel" if wl.dh <= 64 else "attn_bwd_simt_kernel"
@@ -842,7 +842,7 @@ def time_backward(wl, calls, rks, u, vb, dev, peak_tf=None, peak_src=""):
     res = {"kernel": kern, "ms": round(ms, 4), "tflops": round(tf, 3), "bound": bound, "peak": round(peak, 1),
            "frac": round(tf / peak, 4), "peak_source": psrc, "flops": flops,
            "measured": f"the workload's first call alone, CUDA events, {n} calls, whole backward (all launches, "
-                       "the forward statistics recomputed inside)"}
+                       "the forward and its lse recomputed inside)"}
     if need and wl.dh == 64:
         # the same gradients from the forward's saved state (out and the rows'
         # log2-sum-exp, as a training forward keeps them): no recomputed forward

@@ -269,10 +269,10 @@ int txl_attn_bwd(const void* q, const void* k, const void* v, const void* r_k, c
  * 源码阅读笔记", section "Build the model" (RelPartialLearnableMultiHeadAttn.
  * forward: AC + shifted BD, masked softmax, P V) with the memory a constant
  * input ("Transformer-XL" notes, section "Segment-Level Recurrence"), in four
- * launches on `stream`: the forward kernel computes each query row's softmax
- * statistics into the workspace; a small kernel turns them into lse and
- * D = dout . out per row, writes (q+u) and (q+v) scaled by scale * log2 e
- * in bf16 and zeroes dr, du, dvb; a query-major pass recomputes P, dP and dS
+ * launches on `stream`: the forward kernel of txl_attn_fwd_lse writes the
+ * output and each query row's log2-sum-exp into the workspace; a small
+ * kernel computes D = dout . out per row, writes (q+u) and (q+v) scaled by
+ * scale * log2 e in bf16 and zeroes dr, du, dvb; a query-major pass recomputes P, dP and dS
  * per 128-row query tile and writes dq and accumulates dr, du, dvb; a
  * key-major pass recomputes them per 128-key tile and writes dk, dv (it may
  * start on the SMs the query-major pass leaves; the call's last launch

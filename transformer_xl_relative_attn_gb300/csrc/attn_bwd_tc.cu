@@ -17,11 +17,12 @@
 //   du    = scale sum dS_ij k_j,   dv_bias = scale sum dS_ij R_{r(i,j)}
 //
 // Passes, in order on one stream:
-//   1. the forward kernel with every item as one split unit: unnormalised O
-//      and per-row (max, sum) in the workspace (launch_attn_tc_bf16_stats)
-//   2. attn_bwd_prep_kernel: per query row lse = max + log2(sum) (log2
-//      units), D = dout . O / sum, and the score operands (q+u)c, (q+v)c as
-//      bf16 (c = scale log2 e), rounded exactly as the forward rounds them
+//   1. the forward kernel writing the output and each query row's log2-sum-
+//      exp lse into the workspace (launch_attn_tc_bf16_lse); skipped when the
+//      caller passes the forward's saved output and lse
+//   2. attn_bwd_prep_kernel: per query row D = dout . out, and the score
+//      operands (q+u)c, (q+v)c as bf16 (c = scale log2 e), rounded exactly as
+//      the forward rounds them
 //   3. attn_bwd_q_kernel, query-major like the forward: one item is a
 //      (b, h, 128-row query tile) and all its key tiles of 64.  It recomputes
 //      the scores (content AC plus the position band read through the same
@@ -1279,19 +1280,16 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQu, const __grid_consta
     if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Per query row (8 threads, 8 columns each): the row's lse (log2 units) and
-// D = dout . out, and the score operands (q+u)c, (q+v)c rounded to bf16 as the
-// forward rounds them: (float(q) + float(bias)) * c.  SAVED: lse and the
-// bf16 output saved by the forward; otherwise from the forward statistics of
-// the row's item: lse = max + log2(sum), D = dout . O_unnorm / sum.
-template <bool SAVED>
+// Per query row (8 threads, 8 columns each): the row's (lse, D = dout . out)
+// from the forward's bf16 output and lse (log2 units), and the score operands
+// (q+u)c, (q+v)c rounded to bf16 as the forward rounds them:
+// (float(q) + float(bias)) * c.
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ ub,
                      const __nv_bfloat16* __restrict__ vb, const __nv_bfloat16* __restrict__ dout,
-                     const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
                      const __nv_bfloat16* __restrict__ out, const float* __restrict__ lse_in,
                      __nv_bfloat16* __restrict__ qu, __nv_bfloat16* __restrict__ qv, float2* __restrict__ stats,
-                     int n_bh, int H, int L, int n_qtiles, float scale_log2, long long rows,
+                     int H, int L, float scale_log2, long long rows,
                      float4* __restrict__ dr, int n_dr4, float4* __restrict__ du, float4* __restrict__ dvb,
                      int n_b4) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1306,14 +1304,11 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     const int c = (int)(t & 7);
     const bool live = row < rows;
     const long long rr = live ? row : 0;
-    const int bh = (int)(rr / L);
-    const int i = (int)(rr - (long long)bh * L);
-    const int h = bh % H;
-    float2 ml = make_float2(0.f, 1.f);
+    const int h = (int)(rr / L) % H;
     float d = 0.f;
     if (live) {
         float o[8];
-        if constexpr (SAVED) {
+        {
             const uint4 ov = *reinterpret_cast<const uint4*>(out + rr * bw::DH + 8 * c);
             const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
 #pragma unroll
@@ -1322,14 +1317,6 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
                 o[2 * e] = f.x;
                 o[2 * e + 1] = f.y;
             }
-        } else {
-            const long long unit = (long long)(n_qtiles - 1 - i / bw::BM) * n_bh + bh;
-            const int r = i % bw::BM;
-            ml = ws_ml[unit * bw::BM + r];
-            const float4* o4 = reinterpret_cast<const float4*>(ws_o + (unit * bw::BM + r) * bw::DH + 8 * c);
-            const float4 oa = o4[0], ob = o4[1];
-            o[0] = oa.x, o[1] = oa.y, o[2] = oa.z, o[3] = oa.w;
-            o[4] = ob.x, o[5] = ob.y, o[6] = ob.z, o[7] = ob.w;
         }
         const uint4 g = *reinterpret_cast<const uint4*>(dout + rr * bw::DH + 8 * c);
         const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
@@ -1358,25 +1345,20 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     }
     *reinterpret_cast<uint4*>(qu + rr * bw::DH + 8 * c) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
     *reinterpret_cast<uint4*>(qv + rr * bw::DH + 8 * c) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-    if (c == 0) {
-        if constexpr (SAVED)
-            stats[rr] = make_float2(lse_in[rr], d);
-        else
-            stats[rr] = make_float2(ml.x + log2f(ml.y), d / ml.y);
-    }
+    if (c == 0) stats[rr] = make_float2(lse_in[rr], d);
 }
 
 // ---------------------------------------------------------------- host side
-cudaError_t launch_attn_tc_bf16_stats(const void* q, const void* k, const void* v, const void* r,
-                                      const void* ub, const void* vb, int B, int H, int L, int M, float scale,
-                                      float* stats_o, float2* stats_ml, int* status, cudaStream_t stream);
+cudaError_t launch_attn_tc_bf16_lse(const void* q, const void* k, const void* v, const void* r, const void* ub,
+                                    const void* vb, int B, int H, int L, int M, float scale, int lo_shift,
+                                    void* out, float* lse, int* status, cudaStream_t stream);
 
 namespace {
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdWs {
-    float* o;
-    float2* ml;
+    __nv_bfloat16* out;  // the recomputed forward output (no saved state)
+    float* lse;          // and its rows' log2-sum-exp
     __nv_bfloat16* qu;
     __nv_bfloat16* qv;
     float2* stats;
@@ -1384,15 +1366,14 @@ struct BwdWs {
 };
 
 BwdWs bwd_ws_layout(void* base, int B, int H, int L) {
-    const size_t n_items = (size_t)B * H * ((L + bw::BM - 1) / bw::BM);
     const size_t rows = (size_t)B * H * L;
     BwdWs w;
     char* c = static_cast<char*>(base);
     size_t off = 0;
-    w.o = reinterpret_cast<float*>(c + off);
-    off += up256(n_items * bw::BM * bw::DH * sizeof(float));
-    w.ml = reinterpret_cast<float2*>(c + off);
-    off += up256(n_items * bw::BM * sizeof(float2));
+    w.out = reinterpret_cast<__nv_bfloat16*>(c + off);
+    off += up256(rows * bw::DH * 2);
+    w.lse = reinterpret_cast<float*>(c + off);
+    off += up256(rows * sizeof(float));
     w.qu = reinterpret_cast<__nv_bfloat16*>(c + off);
     off += up256(rows * bw::DH * 2);
     w.qv = reinterpret_cast<__nv_bfloat16*>(c + off);
@@ -1430,8 +1411,8 @@ size_t attn_bwd_tc_workspace_bytes(int B, int H, int L, int M) {
 }
 
 // out / lse non-null: the forward's saved output and per-row log2-sum-exp
-// (launch_attn_tc_bf16_lse); otherwise the forward statistics are recomputed
-// into the workspace first.
+// (launch_attn_tc_bf16_lse); otherwise the forward is run first, writing
+// both into the workspace.
 cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
                                const void* vb, const void* out, const float* lse, const void* dout, int B, int H,
                                int L, int M, float scale, float* dq, float* dk, float* dv, float* dr, float* du,
@@ -1455,8 +1436,10 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     cudaError_t e = cudaSuccess;
     const bool saved = out && lse;
     if (!saved) {
-        e = launch_attn_tc_bf16_stats(q, k, v, r, ub, vb, B, H, L, M, scale, w.o, w.ml, status, stream);
+        e = launch_attn_tc_bf16_lse(q, k, v, r, ub, vb, B, H, L, M, scale, 1 << 30, w.out, w.lse, status, stream);
         if (e != cudaSuccess) return e;
+        out = w.out;
+        lse = w.lse;
     }
     const long long rows = (long long)n_bh * L;
     const long long threads = rows * 8;
@@ -1471,14 +1454,8 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* k, const void* v, cons
     auto* du4 = reinterpret_cast<float4*>(du);
     auto* dvb4 = reinterpret_cast<float4*>(dvb);
     const int n_dr4 = K * H * DH / 4, n_b4 = H * DH / 4;
-    if (saved)
-        attn_bwd_prep_kernel<true><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, nullptr, nullptr, ob, lse, w.qu, w.qv,
-                                                                 w.stats, n_bh, H, L, n_qtiles, sl, rows, dr4, n_dr4,
-                                                                 du4, dvb4, n_b4);
-    else
-        attn_bwd_prep_kernel<false><<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, w.o, w.ml, nullptr, nullptr, w.qu,
-                                                                  w.qv, w.stats, n_bh, H, L, n_qtiles, sl, rows, dr4,
-                                                                  n_dr4, du4, dvb4, n_b4);
+    attn_bwd_prep_kernel<<<pgrid, 256, 0, stream>>>(qb, ubb, vbb, gb, ob, lse, w.qu, w.qv, w.stats, H, L, sl, rows,
+                                                    dr4, n_dr4, du4, dvb4, n_b4);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -1030,14 +1030,10 @@ size_t attn_tc_bf16_workspace_bytes(int B, int H, int L, int M) {
     return units * BM * (DH * sizeof(float) + sizeof(float2));
 }
 
-// The launch behind both entry points below.  stats_o / stats_ml non-null:
-// every item runs as a single split unit of attn_tc_bf16_kernel<true, false>
-// and leaves its unnormalised O and per-row (max, sum) there, indexed by the
-// item number (no combine pass, `out` is not written).
+// The launch behind both entry points below.
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* r, const void* ub,
                              const void* vb, int B, int H, int L, int M, float scale, int lo_shift, void* out,
-                             void* workspace, float* stats_o, float2* stats_ml, float* lse, int inject, int* status,
-                             cudaStream_t stream) {
+                             void* workspace, float* lse, int inject, int* status, cudaStream_t stream) {
     using namespace tc;
     static PerDeviceOnce attrs;
     {
@@ -1098,32 +1094,26 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     // the same_length bound runs unsplit (txl_attn_fwd_ex takes no workspace)
     const bool lower = lo_shift < (1 << 30);
     p.nsplit = (workspace && !lower) ? attn_tc_bf16_splits(B, H, L, M) : 1;
-    const bool stats = stats_o != nullptr;
-    if (stats && lower) return cudaErrorInvalidValue;
     if ((long long)p.n_items * p.nsplit + 2ll * num_sms() >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     p.n_units = p.n_items * p.nsplit;
     const size_t units = (size_t)p.n_units;
     p.ws_o = p.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = p.nsplit > 1 ? reinterpret_cast<float2*>(static_cast<float*>(workspace) + units * BM * DH)
                            : nullptr;
-    if (stats) {
-        p.ws_o = stats_o;
-        p.ws_ml = stats_ml;
-    }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.lse = lse;
     if (lse && p.nsplit > 1) return cudaErrorInvalidValue;  // the unsplit kernel writes it
     p.inject = inject;
     p.status = status;
     const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
-    if (p.nsplit > 1 || stats)
+    if (p.nsplit > 1)
         launch_pdl(attn_tc_bf16_kernel<true, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     else if (lower)
         launch_pdl(attn_tc_bf16_kernel<false, true>, grid, stream, mQ, mK, mV, mR, mO, p);
     else
         launch_pdl(attn_tc_bf16_kernel<false, false>, grid, stream, mQ, mK, mV, mR, mO, p);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.nsplit == 1 || stats) return e;
+    if (e != cudaSuccess || p.nsplit == 1) return e;
     const long long threads = (long long)B * H * L * 8;
     if (threads >= 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     attn_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
@@ -1135,8 +1125,8 @@ cudaError_t launch_attn_tc_bf16(const void* q, const void* k, const void* v, con
                                 const void* ub, const void* vb, int B, int H, int L, int M,
                                 float scale, int lo_shift, void* out, void* workspace, int inject,
                                 int* status, cudaStream_t stream) {
-    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, workspace, nullptr, nullptr, nullptr,
-                     inject, status, stream);
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, workspace, nullptr, inject, status,
+                     stream);
 }
 
 // The unsplit forward that also leaves each row's log2-sum-exp of the scores
@@ -1145,21 +1135,7 @@ cudaError_t launch_attn_tc_bf16_lse(const void* q, const void* k, const void* v,
                                     const void* vb, int B, int H, int L, int M, float scale, int lo_shift,
                                     void* out, float* lse, int* status, cudaStream_t stream) {
     if (!lse) return cudaErrorInvalidValue;
-    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, nullptr, nullptr, nullptr, lse, 0,
-                     status, stream);
-}
-
-// Forward statistics for the backward pass: item w = (query tile qq counted
-// from the last, then b*H+h), i.e. w = (n_qtiles-1-qt)*B*H + b*H + h, leaves
-// O_unnorm [w][128][64] (fp32, relative to the row max) in stats_o and
-// (max, sum) [w][128] in log2 units in stats_ml.  No output is written; the
-// output tensor map is encoded over q and never used.
-cudaError_t launch_attn_tc_bf16_stats(const void* q, const void* k, const void* v, const void* r,
-                                      const void* ub, const void* vb, int B, int H, int L, int M, float scale,
-                                      float* stats_o, float2* stats_ml, int* status, cudaStream_t stream) {
-    if (!stats_o || !stats_ml) return cudaErrorInvalidValue;
-    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, 1 << 30, const_cast<void*>(q), nullptr, stats_o,
-                     stats_ml, nullptr, 0, status, stream);
+    return launch_tc(q, k, v, r, ub, vb, B, H, L, M, scale, lo_shift, out, nullptr, lse, 0, status, stream);
 }
 
 TXL_BOUNDS_READER(bounds_word_attn_tc)
