@@ -177,3 +177,24 @@ def test_saved_state_entries_reject_bad_arguments():
     with pytest.raises(txl.TxlError) as e:
         txl.attn_fwd_lse(*_dev(f32), scale=f32.scale)
     assert e.value.code == -2
+
+
+def test_gradients_complete_for_work_queued_after_the_call():
+    """The passes overlap on the GPU (the key-major pass starts on the SMs the
+    query-major pass leaves) but the call's last launch completes after both:
+    stream work queued right after the call, with no host synchronisation,
+    sees every gradient final."""
+    ci = W.random_call_inputs(2, 3, 257, 64, 64, std=0.5, seed=12)
+    d = _dev(ci)
+    g = torch.randn(2, 3, 257, 64, generator=torch.Generator().manual_seed(3)).bfloat16().cuda()
+    ref = txl.attn_bwd(*d, g, ci.scale)
+    torch.cuda.synchronize()
+    grads = {n: torch.full_like(ref[n], float("nan")) for n in NAMES}
+    got = txl.attn_bwd(*d, g, ci.scale, grads=grads)
+    copies = {n: got[n].clone() for n in NAMES}  # queued on the same stream, no sync in between
+    torch.cuda.synchronize()
+    assert txl.sync_status() == 0
+    for n in ("dq", "dk", "dv"):
+        assert torch.equal(copies[n], ref[n]), n
+    for n in ("dr", "du", "dvb"):
+        assert float((copies[n] - ref[n]).abs().max()) <= 1e-5 * float(ref[n].abs().max()) + 1e-6, n
